@@ -1,0 +1,320 @@
+"""Pins for the oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function takes an oracle library handle (so a deliberately
+broken build of the oracle can be run through the same checks) and raises
+AssertionError on a mismatch.  What pins what:
+
+* ``pin_hand_example``  -- values worked by hand (tests/golden/hand_example.json)
+  from the page's semantics: empty bag = 0, repeated id counted twice,
+  column offsets, row gradient = sum of bag gradients, stable key order.
+* ``pin_dense_onehot``  -- the textbook form: with A_t[b, r] = sum of the
+  weights of the lookups of bag (t, b) that name row r, the forward is the
+  matrix product A_t @ W_t and the table gradient is A_t^T @ G_t (numpy
+  float64 matmul, a library routine).
+* ``pin_invariants``    -- column sums, adjoint identity, lookup count,
+  histogram form == gather form bit for bit (exact fp64 sums of fp16).
+* ``pin_sort_vs_numpy`` -- sorted positions equal numpy's stable argsort.
+* ``pin_formats``       -- fp16/bf16 decoding over all 65536 codes and
+  nearest-even rounding against numpy and against a brute-force nearest
+  search.
+* ``pin_special_cases`` -- all-empty batch, single-id bags, one id repeated
+  n times, out-of-range ids, broken offsets.
+"""
+
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+import oracle
+from tbe_inputs import DT_BF16, DT_F16, DT_F32, make_problem, materialize_weights
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _hand_problem(weighted: bool):
+    import torch
+
+    g = json.load(open(os.path.join(GOLDEN, "hand_example.json")))
+    T, B = g["T"], g["B"]
+    offs = np.array(g["offsets"])
+    lens = np.diff(offs).reshape(T, B)
+    ind = np.array(g["indices"])
+    ids = [ind[offs[t * B]: offs[(t + 1) * B]] for t in range(T)]
+    tables = {t: torch.tensor(g["tables"][t], dtype=torch.float32) for t in range(T)}
+    p = make_problem(T, B, rows=[3, 2], D=[2, 1], weights_dtype=[DT_F32, DT_F32], out_dtype=DT_F32,
+                     lengths=lens, ids=ids, grad_out=np.array(g["grad_out"], np.float32),
+                     psw=np.array(g["per_sample_weights"], np.float32) if weighted else None,
+                     host_tables=tables)
+    return g, p
+
+
+def pin_hand_example(lib):
+    for weighted in (False, True):
+        g, p = _hand_problem(weighted)
+        w = materialize_weights(p)
+        st, out, _ = oracle.problem_forward(p, w, lib=lib)
+        assert st == 0
+        exp = g["expected"]["weighted_out" if weighted else "out"]
+        np.testing.assert_array_equal(out, np.array(exp, np.float64))
+        idx, st2, rg, _, pos = oracle.problem_backward(p, lib=lib)
+        assert st2 == 0 and idx["status"] == 0
+        np.testing.assert_array_equal(idx["sorted_pos"], g["expected"]["sorted_pos"])
+        np.testing.assert_array_equal(idx["unique_rows"], g["expected"]["unique_rows"])
+        np.testing.assert_array_equal(idx["run_starts"], g["expected"]["run_starts"])
+        np.testing.assert_array_equal(idx["unique_count"], g["expected"]["unique_count"])
+        exp_rg = g["expected"]["weighted_row_grads" if weighted else "row_grads"]
+        np.testing.assert_array_equal(rg, np.concatenate([np.array(r, np.float64) for r in exp_rg]))
+        # the fp32 output rounding of small integers is exact
+        np.testing.assert_array_equal(oracle.round_to(out, DT_F32, lib=lib), np.array(exp, np.float32))
+
+
+def _random_problem(rng, T, B, dtypes, weighted, max_len=7, max_rows=9):
+    rows = rng.integers(1, max_rows + 1, size=T)
+    D = rng.choice([1, 2, 3, 4, 8], size=T)
+    lens = rng.integers(0, max_len + 1, size=(T, B))
+    ids = [rng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
+    G = rng.standard_normal((B, int(D.sum()))).astype(np.float32)
+    N = int(lens.sum())
+    psw = rng.random(N).astype(np.float32) * 2 - 0.5 if weighted else None
+    tw = None
+    if weighted:
+        tw = (rng.random(T) < 0.6).astype(np.uint8)
+    p = make_problem(T, B, rows=rows, D=D, weights_dtype=[dtypes[t % len(dtypes)] for t in range(T)],
+                     out_dtype=DT_F32, lengths=lens, ids=ids, psw=psw, grad_out=G,
+                     table_weighted=tw, seed=int(rng.integers(1 << 30)))
+    return p
+
+
+def _table_f64(p, w, t):
+    """Decode table t of the packed buffer with numpy's own format support."""
+    import torch
+
+    code = int(p.weights_dtype[t])
+    R, D = int(p.rows[t]), int(p.D[t])
+    off = int(p.weights_offsets[t])
+    eb = 4 if code == DT_F32 else 2
+    raw = w[off: off + R * D * eb]
+    if code == DT_F32:
+        return raw.view(torch.float32).numpy().astype(np.float64).reshape(R, D)
+    if code == DT_F16:
+        return raw.view(torch.float16).numpy().astype(np.float64).reshape(R, D)
+    bits = raw.view(torch.int16).numpy().astype(np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64).reshape(R, D)
+
+
+def pin_dense_onehot(lib, trials=40, seed=5):
+    rng = np.random.default_rng(seed)
+    for k in range(trials):
+        T = int(rng.integers(1, 5))
+        B = int(rng.integers(1, 6))
+        weighted = bool(k % 2)
+        p = _random_problem(rng, T, B, [DT_F32, DT_F16, DT_BF16], weighted)
+        w = materialize_weights(p)
+        st, out, _ = oracle.problem_forward(p, w, lib=lib)
+        assert st == 0
+        idx, st2, rg, _, rpos = oracle.problem_backward(p, lib=lib)
+        assert st2 == 0
+        doff = p.D_offsets
+        trb = p.table_row_base
+        for t in range(T):
+            R = int(p.rows[t])
+            A = np.zeros((B, R), np.float64)
+            for b in range(B):
+                g = t * B + b
+                for i in range(int(p.offsets[g]), int(p.offsets[g + 1])):
+                    wi = 1.0
+                    if p.per_sample_weights is not None and p.table_weighted[t]:
+                        wi = float(p.per_sample_weights[i])
+                    A[b, p.indices[i]] += wi
+            Wt = _table_f64(p, w, t)
+            exp = A @ Wt
+            np.testing.assert_allclose(out[:, doff[t]: doff[t + 1]], exp, rtol=1e-12, atol=1e-12)
+            Gt = p.grad_out[:, doff[t]: doff[t + 1]].astype(np.float64)
+            dense = A.T @ Gt  # [R, D_t]
+            occurring = np.nonzero(np.bincount(p.indices[p.offsets[t * B]: p.offsets[(t + 1) * B]],
+                                               minlength=R))[0]
+            uc = idx["unique_count"]
+            ours_rows = idx["unique_rows"][uc[t]: uc[t + 1]] - trb[t]
+            np.testing.assert_array_equal(ours_rows, occurring)
+            Dt = int(p.D[t])
+            for j, u in enumerate(range(int(uc[t]), int(uc[t + 1]))):
+                got = rg[rpos[u]: rpos[u] + Dt]
+                np.testing.assert_allclose(got, dense[occurring[j]], rtol=1e-12, atol=1e-12)
+
+
+def pin_invariants(lib, trials=30, seed=11):
+    rng = np.random.default_rng(seed)
+    for k in range(trials):
+        T = int(rng.integers(1, 5))
+        B = int(rng.integers(1, 7))
+        weighted = bool(k % 3 == 0)
+        p = _random_problem(rng, T, B, [DT_F16, DT_F32, DT_BF16], weighted, max_len=12, max_rows=20)
+        w = materialize_weights(p)
+        st, out, oabs = oracle.problem_forward(p, w, lib=lib)
+        idx, st2, rg, rabs, rpos = oracle.problem_backward(p, lib=lib)
+        assert st == 0 and st2 == 0
+        # I3: lookup count, strictly increasing rows inside their tables
+        rs = idx["run_starts"]
+        assert rs[0] == 0 and rs[-1] == p.N and np.all(np.diff(rs) > 0)
+        ur = idx["unique_rows"]
+        assert np.all(np.diff(ur) > 0)
+        trb = p.table_row_base
+        uc = idx["unique_count"]
+        for t in range(T):
+            seg = ur[uc[t]: uc[t + 1]]
+            assert np.all((seg >= trb[t]) & (seg < trb[t + 1]))
+        assert sorted(idx["sorted_pos"].tolist()) == list(range(p.N))
+        # I1: per table, sum of row gradients = sum_b (sum of bag weights) * G[b, cols_t]
+        doff = p.D_offsets
+        for t in range(T):
+            Dt = int(p.D[t])
+            tot = np.zeros(Dt)
+            for u in range(int(uc[t]), int(uc[t + 1])):
+                tot += rg[rpos[u]: rpos[u] + Dt]
+            exp = np.zeros(Dt)
+            for b in range(B):
+                g = t * B + b
+                lo, hi = int(p.offsets[g]), int(p.offsets[g + 1])
+                if p.per_sample_weights is not None and p.table_weighted[t]:
+                    wsum = float(np.sum(p.per_sample_weights[lo:hi].astype(np.float64)))
+                else:
+                    wsum = float(hi - lo)
+                exp += wsum * p.grad_out[b, doff[t]: doff[t + 1]].astype(np.float64)
+            np.testing.assert_allclose(tot, exp, rtol=1e-11, atol=1e-11)
+        # I2: adjoint <out, G> = sum_u <row_grad_u, W[row_u]>
+        lhs = float(np.sum(out * p.grad_out.astype(np.float64)))
+        rhs = 0.0
+        for t in range(T):
+            Wt = _table_f64(p, w, t)
+            Dt = int(p.D[t])
+            for u in range(int(uc[t]), int(uc[t + 1])):
+                rhs += float(np.dot(rg[rpos[u]: rpos[u] + Dt], Wt[ur[u] - trb[t]]))
+        assert abs(lhs - rhs) <= 1e-10 * (1 + abs(lhs))
+        # |terms| sums bound the sums
+        assert np.all(np.abs(out) <= oabs + 1e-15) and np.all(np.abs(rg) <= rabs + 1e-15)
+        # I4: histogram form == gather form, bit for bit, for unweighted fp16 tables
+        for t in range(T):
+            if int(p.weights_dtype[t]) != DT_F16:
+                continue
+            if p.per_sample_weights is not None and p.table_weighted[t]:
+                continue
+            st3, cnt = oracle.histogram_counts(T, B, t, int(p.rows[t]), p.indices, p.offsets, lib=lib)
+            assert st3 == 0
+            assert np.array_equal(cnt.sum(axis=1), np.diff(p.offsets)[t * B:(t + 1) * B])
+            hist = oracle.counts_times_table(cnt, w, p.weights_offsets[t], DT_F16, int(p.D[t]), lib=lib)
+            assert np.array_equal(hist, out[:, doff[t]: doff[t + 1]])
+
+
+def pin_sort_vs_numpy(lib, seed=3):
+    rng = np.random.default_rng(seed)
+    for _ in range(5):
+        T, B = 3, 50
+        p = _random_problem(rng, T, B, [DT_F32], False, max_len=30, max_rows=15)
+        idx = oracle.backward_indexing(p.layout_arrays(), p.indices, p.offsets, p.B, lib=lib)
+        t_of = np.repeat(np.arange(T * B) // B, np.diff(p.offsets))
+        keys = p.table_row_base[t_of] + p.indices
+        np.testing.assert_array_equal(idx["sorted_pos"], np.argsort(keys, kind="stable"))
+        sk = keys[np.argsort(keys, kind="stable")]
+        starts = np.nonzero(np.concatenate([[True], sk[1:] != sk[:-1]]))[0]
+        np.testing.assert_array_equal(idx["run_starts"][:-1], starts)
+        np.testing.assert_array_equal(idx["unique_rows"], sk[starts])
+
+
+def _nearest_even_codes(x: np.ndarray, pos_codes: np.ndarray, pos_vals: np.ndarray) -> np.ndarray:
+    """Nearest representable magnitude by search over the sorted value list;
+    ties go to the even code."""
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(pos_vals, a), 1, pos_vals.size - 1)
+    lo = hi - 1
+    dlo, dhi = a - pos_vals[lo], pos_vals[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(pos_codes[lo] % 2 == 0, lo, hi)))
+    out = pos_codes[pick].astype(np.uint16)
+    return np.where(x < 0, out | 0x8000, out).astype(np.uint16)
+
+
+def pin_formats(lib, seed=17):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    # decoding: fp16 against numpy's float16, bf16 against the upper half of float32
+    f16 = codes.view(np.float16).astype(np.float64)
+    dec16 = oracle.decode(codes, oracle.F16, lib=lib)
+    fin = np.isfinite(f16)
+    np.testing.assert_array_equal(dec16[fin], f16[fin])
+    assert np.all(np.isnan(dec16[np.isnan(f16)]))
+    bf = (codes.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    decb = oracle.decode(codes, oracle.BF16, lib=lib)
+    finb = np.isfinite(bf)
+    np.testing.assert_array_equal(decb[finb], bf[finb])
+    # rounding to fp16: exact values, midpoints and random doubles against numpy
+    pos16 = np.unique(np.abs(f16[fin]))
+    mids = (pos16[1:] + pos16[:-1]) / 2
+    rng = np.random.default_rng(seed)
+    rnd = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000),
+                          np.nextafter(mids, 0), np.nextafter(mids, 1)])
+    xs = np.concatenate([pos16, -pos16, mids, -mids, rnd, [70000.0, 65519.0, 65520.0, -1e-9, 0.0]])
+    ours = oracle.round_to(xs, oracle.F16, lib=lib)
+    ref = xs.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+    # rounding to bf16: brute-force nearest representable, ties to even code
+    posb = np.unique(np.abs(bf[finb]))
+    midb = (posb[1:] + posb[:-1]) / 2
+    sel = rng.choice(midb.size, 3000, replace=False)
+    xb = np.concatenate([posb[rng.choice(posb.size, 2000, replace=False)], midb[sel],
+                         rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000)])
+    oursb = oracle.round_to(xb, oracle.BF16, lib=lib)
+    pos_codes = codes[(codes < 0x7F80)]
+    pos_vals = bf[pos_codes.astype(np.int64)]
+    want = _nearest_even_codes(xb, pos_codes, pos_vals)
+    np.testing.assert_array_equal(oursb, want)
+
+
+def pin_special_cases(lib):
+    import torch
+
+    # all bags empty: output 0, no runs
+    p = make_problem(2, 3, rows=[4, 5], D=[4, 8], weights_dtype=[DT_F32, DT_F16], out_dtype=DT_F32,
+                     lengths=np.zeros((2, 3)), ids=[[], []], grad_out=np.ones((3, 12), np.float32))
+    w = materialize_weights(p)
+    st, out, _ = oracle.problem_forward(p, w, lib=lib)
+    assert st == 0 and np.all(out == 0)
+    idx, st2, rg, _, _ = oracle.problem_backward(p, lib=lib)
+    assert idx["U"] == 0 and rg.size == 0 and list(idx["run_starts"]) == [0]
+    # each bag [k]: output rows are copies of W[k]; one id repeated n times gives n*W[k]
+    T, B = 1, 5
+    tbl = torch.tensor(np.arange(6 * 4, dtype=np.float32).reshape(6, 4) / 8)
+    p = make_problem(T, B, rows=[6], D=[4], weights_dtype=[DT_F32], out_dtype=DT_F32,
+                     lengths=[[1, 1, 3, 5, 1]], ids=[[2, 0, 4, 4, 4, 1, 1, 1, 1, 1, 5]],
+                     grad_out=np.ones((5, 4), np.float32), host_tables={0: tbl})
+    w = materialize_weights(p)
+    st, out, _ = oracle.problem_forward(p, w, lib=lib)
+    W = tbl.numpy().astype(np.float64)
+    np.testing.assert_array_equal(out, np.stack([W[2], W[0], 3 * W[4], 5 * W[1], W[5]]))
+    # out-of-range and negative ids: reported, contribute nothing
+    p = make_problem(1, 2, rows=[6], D=[4], weights_dtype=[DT_F32], out_dtype=DT_F32,
+                     lengths=[[3, 2]], ids=[[1, 6, 2, -1, 3]], grad_out=np.ones((2, 4), np.float32),
+                     host_tables={0: tbl})
+    w = materialize_weights(p)
+    st, out, _ = oracle.problem_forward(p, w, lib=lib)
+    assert st == oracle.BAD_INDEX
+    np.testing.assert_array_equal(out, np.stack([W[1] + W[2], W[3]]))
+    idx, st2, rg, _, _ = oracle.problem_backward(p, lib=lib)
+    assert idx["status"] == oracle.BAD_INDEX
+    np.testing.assert_array_equal(idx["unique_rows"], [1, 2, 3])
+    np.testing.assert_array_equal(idx["run_starts"], [0, 1, 2, 3])
+    np.testing.assert_array_equal(idx["sorted_pos"], [0, 2, 4, 1, 3])
+    # broken offsets are reported: not starting at 0, not ending at N, decreasing
+    p = make_problem(1, 3, rows=[6], D=[4], weights_dtype=[DT_F32], out_dtype=DT_F32,
+                     lengths=[[2, 2, 1]], ids=[[1, 2, 3, 4, 5]], grad_out=np.ones((3, 4), np.float32),
+                     host_tables={0: tbl})
+    lay = p.layout_arrays()
+    for bad in ([1, 2, 4, 5], [0, 2, 4, 4], [0, 4, 2, 5]):
+        st = oracle.forward(lay, w, p.indices, np.array(bad), 3, lib=lib)[0]
+        assert st == oracle.BAD_OFFSETS, bad
+        st = oracle.backward_indexing(lay, p.indices, np.array(bad), 3, lib=lib)["status"]
+        assert st == oracle.BAD_OFFSETS, bad
+
+
+ALL_PINS = [pin_hand_example, pin_dense_onehot, pin_invariants, pin_sort_vs_numpy, pin_formats,
+            pin_special_cases]

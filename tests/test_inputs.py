@@ -1,0 +1,52 @@
+"""The seeded input generators: shapes, ranges and reproducibility (CPU only)."""
+
+import numpy as np
+import pytest
+import torch
+
+from tbe_inputs import DT_F16, config_names, make_config, materialize_weights, table_rows
+
+
+@pytest.mark.parametrize("name", config_names())
+def test_config_shapes(name):
+    p = make_config(name, B=64, rows_scale=0.01 if name in ("mixed", "bwd_skew") else 1.0)
+    assert p.offsets.shape == (p.T * p.B + 1,)
+    assert p.offsets[0] == 0 and p.offsets[-1] == p.N and np.all(np.diff(p.offsets) >= 0)
+    for t in range(p.T):
+        seg = p.indices[p.offsets[t * p.B]: p.offsets[(t + 1) * p.B]]
+        assert np.all((seg >= 0) & (seg < p.rows[t]))
+    assert p.grad_out.shape == (p.B, p.total_D) and p.grad_out.dtype == np.float32
+    assert np.all(p.weights_offsets % 256 == 0)
+    if name in ("tiny", "mid_skewed"):
+        assert (np.diff(p.offsets) == 0).any()
+    if name == "mixed":
+        assert p.per_sample_weights is not None and int(p.table_weighted.sum()) == 20
+    # same seed, same batch -> identical draws; another batch -> other ids
+    q = make_config(name, B=64, rows_scale=0.01 if name in ("mixed", "bwd_skew") else 1.0)
+    assert np.array_equal(p.indices, q.indices) and np.array_equal(p.grad_out, q.grad_out)
+    r = make_config(name, B=64, rows_scale=0.01 if name in ("mixed", "bwd_skew") else 1.0, batch=1)
+    assert not np.array_equal(p.indices, r.indices) or p.N == 0
+
+
+def test_table_rows_regenerate_buffer():
+    p = make_config("mixed", B=8, rows_scale=0.002)
+    w = materialize_weights(p)
+    rng = np.random.default_rng(0)
+    for t in range(p.T):
+        R, D = int(p.rows[t]), int(p.D[t])
+        ids = rng.integers(0, R, size=5)
+        got = table_rows(p, t, ids)
+        eb = got.element_size()
+        off = int(p.weights_offsets[t])
+        view = w[off: off + R * D * eb].view(got.dtype).view(R, D)
+        assert torch.equal(view[torch.as_tensor(ids)], got)
+        assert float(got.float().abs().max()) <= 0.0505  # U(-0.05, 0.05) after rounding
+
+
+def test_zipf_is_skewed():
+    p = make_config("mid_skewed", B=2048)
+    seg = p.indices[p.offsets[0]: p.offsets[p.B]]
+    counts = np.bincount(seg, minlength=int(p.rows[0]))
+    top = np.sort(counts)[::-1]
+    assert top[0] > 0.05 * seg.size  # hottest row takes several percent of lookups
+    assert int(p.weights_dtype[0]) == DT_F16
