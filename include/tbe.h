@@ -1,0 +1,233 @@
+/*
+ * tbe.h -- C ABI of libtbe: table-batched embedding bags (TBE) on one GB300.
+ *
+ * The operator is the one described on the page "FBTriton table-batched
+ * embeddings: the backward win is a threshold moved from 32 to 256":
+ *
+ *  - Layout ([FBT] "A lookup table that is most of the model"): every table
+ *    sits in one weight buffer; every feature's bags share one flat
+ *    `indices` array and one `offsets` array laid out feature-major, so bag
+ *    (t, b) is indices[offsets[t*B + b] : offsets[t*B + b + 1]].  The output
+ *    is one [B, sum_t D_t] matrix with feature t at column D_offsets[t].  An
+ *    empty bag leaves its slot zero; a repeated id is added twice.
+ *  - Forward ([FBT] "The forward: a general gather and one clever special
+ *    case"): sum pooling of the rows a bag names, optionally scaled by
+ *    per-sample weights, accumulated in FP32; a small-table path counts ids
+ *    per bag and multiplies the count matrix by the table on tensor cores.
+ *  - Backward ([FBT] "Why the backward is the hard half" and "Three tiers,
+ *    routed by run length"): every lookup gets the key
+ *    table_row_base[t] + id, the keys are sorted, equal keys form runs, and
+ *    each run's row gradient is the sum of the output-gradient slices of the
+ *    bags that read it (times their per-sample weights).  Short runs are
+ *    reduced by one warp each; long runs are cut into chunks whose partial
+ *    sums are combined by the last chunk to finish (fence + counter).
+ *
+ * Conventions for every entry point
+ *  - Pointers named dev_* or documented "device" are CUDA device pointers;
+ *    all others are host pointers.  The caller owns every buffer.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls only enqueue work on it: they never synchronise and
+ *    never allocate device memory.
+ *  - Return value: TBE_OK or a TBE_ERR_* code for errors found on the host
+ *    (bad arguments, unsupported shapes, CUDA launch failures).  Errors that
+ *    depend on the data (ids outside their table, broken offsets, a
+ *    workspace-capacity shortfall, a bounded wait that gave up) are OR-ed
+ *    into the optional device word `dev_status` as TBE_DEV_* bits; kernels
+ *    never trap.  A lookup whose id is outside [0, rows_t) contributes
+ *    nothing, forward or backward.
+ *  - Sizes: N (lookups) < 2^30, T*B < 2^31, sum of table rows < 2^32 - 1,
+ *    rows of one table < 2^31, T <= TBE_MAX_TABLES.  Every table's row must
+ *    be a multiple of 16 bytes and every table must start on a 16-byte
+ *    boundary of `weights`.
+ */
+#ifndef TBE_H_
+#define TBE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes (host) ------------------------------------------------ */
+#define TBE_OK 0
+#define TBE_ERR_INVALID_ARG 1 /* null pointer, negative size, inconsistent layout */
+#define TBE_ERR_UNSUPPORTED 2 /* a shape or dtype outside the stated limits      */
+#define TBE_ERR_CUDA 3        /* a CUDA runtime call or kernel launch failed      */
+#define TBE_ERR_WORKSPACE 4   /* workspace smaller than the size query returned   */
+
+/* ---- device status bits (OR-ed into *dev_status by kernels) --------------- */
+#define TBE_DEV_BAD_INDEX 0x1   /* an id outside [0, rows_t); it was skipped          */
+#define TBE_DEV_BAD_OFFSETS 0x2 /* offsets[0] != 0, decreasing, or offsets[T*B] != N */
+#define TBE_DEV_TIMEOUT 0x4     /* a bounded wait gave up; outputs are not valid      */
+#define TBE_DEV_CAPACITY 0x8    /* row_grads_capacity too small; outputs truncated    */
+
+/* ---- element types ------------------------------------------------------- */
+#define TBE_F32 0
+#define TBE_F16 1
+#define TBE_BF16 2
+
+#define TBE_MAX_TABLES 4096
+
+/* ---- forward path selection ---------------------------------------------- */
+#define TBE_PATH_AUTO 0      /* histogram path where eligible, else gather */
+#define TBE_PATH_GATHER 1    /* always the gather kernel                   */
+#define TBE_PATH_HISTOGRAM 2 /* histogram path; TBE_ERR_UNSUPPORTED if not eligible */
+
+/*
+ * Description of the packed tables (all HOST arrays; copied by
+ * tbe_plan_create, so they may be freed afterwards).
+ *   T                : number of tables (features), 1..TBE_MAX_TABLES
+ *   table_row_base   : [T+1] running sum of table row counts (the page's
+ *                      hash_size_cumsum); rows_t = diff; global row of id in
+ *                      table t is table_row_base[t] + id
+ *   D_offsets        : [T+1] running sum of table widths; D_t = diff; also
+ *                      the output column offset of feature t
+ *   weights_offsets  : [T] byte offset of table t inside `weights`
+ *                      (row-major [rows_t, D_t] in its dtype)
+ *   weights_dtype    : [T] TBE_F32 / TBE_F16 / TBE_BF16
+ *   table_weighted   : [T] 1 if table t uses per_sample_weights; NULL means
+ *                      every table does when per_sample_weights is given
+ *   out_dtype        : forward output element type
+ */
+typedef struct tbe_layout {
+  int32_t T;
+  const int64_t* table_row_base;
+  const int32_t* D_offsets;
+  const int64_t* weights_offsets;
+  const int32_t* weights_dtype;
+  const uint8_t* table_weighted;
+  int32_t out_dtype;
+} tbe_layout;
+
+/* Opaque plan: validated layout, packed per-table metadata and kernel
+ * choices.  The packed metadata lives in caller-provided device memory. */
+typedef struct tbe_plan tbe_plan;
+
+/* Bytes of device memory a plan for T tables needs (256-byte multiple). */
+size_t tbe_plan_device_bytes(int32_t T);
+
+/* Validate `L`, pack its per-table metadata and copy it (asynchronously, on
+ * `stream`) into `dev_meta` (device, >= tbe_plan_device_bytes(T) bytes,
+ * 16-byte aligned, owned by the caller and kept alive while the plan is in
+ * use).  The host-side plan object is returned in *plan_out (heap memory of
+ * the host; release with tbe_plan_destroy).
+ * Errors: TBE_ERR_INVALID_ARG (nulls, T out of range, decreasing
+ * table_row_base or D_offsets, unknown dtype), TBE_ERR_UNSUPPORTED (a row
+ * that is not a multiple of 16 bytes, an unaligned table, row counts beyond
+ * the limits), TBE_ERR_CUDA. */
+int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, void* stream,
+                    tbe_plan** plan_out);
+void tbe_plan_destroy(tbe_plan* plan);
+
+/*
+ * Forward: out[b, D_offsets[t] + c] = sum_{i in bag(t,b)} w_i * W_t[id_i, c]
+ * accumulated in FP32 and rounded once (nearest-even) to out_dtype.
+ *   weights            : device, the packed table buffer
+ *   indices            : device int64 [N], table-local ids
+ *   offsets            : device int64 [T*B + 1], feature-major
+ *   per_sample_weights : device fp32 [N] or NULL (unweighted); applies to
+ *                        the tables the layout marks weighted
+ *   out                : device [B, D_offsets[T]] of out_dtype, row-major;
+ *                        every element is written (empty bags give 0)
+ *   dev_status         : device int32 word or NULL
+ * B == 0 or T*B == 0 is a no-op. */
+int tbe_forward(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
+                const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                int32_t* dev_status, void* stream);
+
+/* Forward with an explicit path (TBE_PATH_*).  The histogram path needs
+ * T == 1, an fp16 table of at most TBE_HIST_MAX_ROWS rows with D a multiple
+ * of 16 and at most 256, and no per-sample weights; otherwise
+ * TBE_ERR_UNSUPPORTED.  TBE_PATH_AUTO additionally requires the mean bag
+ * length N / B to reach the tuned threshold. */
+#define TBE_HIST_MAX_ROWS 64
+int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
+                     const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                     int32_t* dev_status, void* stream, int32_t path);
+
+/* Per-bag id histogram of the single table of a histogram-eligible plan, the
+ * count matrix the histogram path multiplies by the table:
+ * counts[b * rows_0 + r] = #{i in bag(0, b) : id_i = r}  (device int32
+ * [B, rows_0]).  Produced by the same kernel code as the histogram forward. */
+int tbe_histogram_counts(const tbe_plan* plan, const int64_t* indices, int64_t N,
+                         const int64_t* offsets, int32_t B, int32_t* counts, int32_t* dev_status,
+                         void* stream);
+
+/*
+ * Backward (row gradients).  For every global row r read by a valid lookup:
+ *   row_grad[r, c] = sum_{i : table_row_base[t_i] + id_i = r} w_i * G[b_i, D_offsets[t_i] + c]
+ * summed in FP32.
+ *   grad_out          : device fp32 [B, D_offsets[T]]
+ *   indices, offsets, per_sample_weights : as for tbe_forward
+ *   unique_rows       : device int64 [N]; the first U entries receive the
+ *                       ascending distinct global rows
+ *   run_starts        : device int32 [N + 1] or NULL; entries 0..U receive
+ *                       the start of each row's run in sorted order and the
+ *                       number of valid lookups
+ *   sorted_positions  : device int32 [N] or NULL; the lookup positions
+ *                       ordered by (row, position) -- valid lookups first,
+ *                       then those with a bad id in position order
+ *   row_grads         : device fp32, capacity row_grads_capacity floats;
+ *                       run u of table t is written at float offset
+ *                       sum_{t'<t} U_t' * D_t' + (u - unique_count[t]) * D_t
+ *                       (table-major blocks)
+ *   unique_count      : device int64 [T + 1]; unique_count[t] = number of
+ *                       distinct rows of tables < t, so unique_count[T] = U
+ *   workspace         : device, >= tbe_backward_workspace_bytes(plan, B, N)
+ *                       bytes, 256-byte aligned; contents need no
+ *                       initialisation and are scratch after the call
+ * If the row gradients need more than row_grads_capacity floats,
+ * TBE_DEV_CAPACITY is set and the excess is not written. */
+size_t tbe_backward_workspace_bytes(const tbe_plan* plan, int32_t B, int64_t N);
+int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
+                 const int64_t* offsets, int32_t B, const float* per_sample_weights,
+                 int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions,
+                 float* row_grads, int64_t row_grads_capacity, int64_t* unique_count,
+                 void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * Tuning knobs (process-wide; set them before launching work that should
+ * use them, not concurrently with launches).
+ *   long_run_threshold : runs with at least this many lookups take the
+ *                        long-run (chunked, multi-warp) tier; shorter runs
+ *                        are reduced by one warp each
+ *   long_chunk         : lookups per chunk of a long run
+ *   fwd_unroll         : independent row loads in flight per lane group in
+ *                        the forward gather (2, 4 or 8)
+ *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
+ *                        many as fit)
+ *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
+ *                        N / B reaches this
+ * Values outside their ranges are rejected with TBE_ERR_INVALID_ARG. */
+typedef struct tbe_tuning {
+  int32_t long_run_threshold;
+  int32_t long_chunk;
+  int32_t fwd_unroll;
+  int32_t fwd_blocks_per_sm;
+  int32_t hist_min_mean_bag;
+} tbe_tuning;
+int tbe_get_tuning(tbe_tuning* out);
+int tbe_set_tuning(const tbe_tuning* in);
+
+/* Stage timing: when enabled, each tbe_forward / tbe_backward records a CUDA
+ * event after each of its kernels on its stream.  tbe_trace_read waits for
+ * the last recorded call and returns up to max_stages stage durations in
+ * milliseconds (stage k = time between events k-1 and k; stage 0 starts at
+ * the call) plus their names.  Returns the number of stages (>= 0) or a
+ * negative TBE_ERR_* code. */
+int tbe_trace_enable(int32_t on);
+int tbe_trace_read(float* stage_ms, const char** stage_names, int32_t max_stages);
+
+/* Human-readable text for a return code. */
+const char* tbe_status_string(int32_t code);
+
+/* Library version string. */
+const char* tbe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TBE_H_ */

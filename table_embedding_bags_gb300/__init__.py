@@ -1,0 +1,274 @@
+"""Python binding of libtbe (table-batched embedding bags on GB300).
+
+Argument marshalling only: every step of the operator runs in the CUDA
+kernels of ``libtbe.so``; this module passes device pointers, sizes and the
+current CUDA stream through ctypes.  There is no CPU fallback: if the
+library is missing, loading it raises.
+
+Function names mirror the C ABI in ``include/tbe.h``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtbe.so")
+
+TBE_OK, TBE_ERR_INVALID_ARG, TBE_ERR_UNSUPPORTED, TBE_ERR_CUDA, TBE_ERR_WORKSPACE = 0, 1, 2, 3, 4
+TBE_DEV_BAD_INDEX, TBE_DEV_BAD_OFFSETS, TBE_DEV_TIMEOUT, TBE_DEV_CAPACITY = 1, 2, 4, 8
+TBE_F32, TBE_F16, TBE_BF16 = 0, 1, 2
+TBE_PATH_AUTO, TBE_PATH_GATHER, TBE_PATH_HISTOGRAM = 0, 1, 2
+TBE_MAX_TABLES = 4096
+
+# every symbol include/tbe.h declares
+EXPORTED = [
+    "tbe_plan_device_bytes", "tbe_plan_create", "tbe_plan_destroy", "tbe_forward", "tbe_forward_path",
+    "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
+    "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
+]
+
+
+class TBEError(RuntimeError):
+    pass
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("table_row_base", ctypes.c_void_p), ("D_offsets", ctypes.c_void_p),
+                ("weights_offsets", ctypes.c_void_p), ("weights_dtype", ctypes.c_void_p),
+                ("table_weighted", ctypes.c_void_p), ("out_dtype", ctypes.c_int32)]
+
+
+class Tuning(ctypes.Structure):
+    _fields_ = [("long_run_threshold", ctypes.c_int32), ("long_chunk", ctypes.c_int32),
+                ("fwd_unroll", ctypes.c_int32), ("fwd_blocks_per_sm", ctypes.c_int32),
+                ("hist_min_mean_bag", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libtbe.so (no fallback: raises when the CUDA library is absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise TBEError(f"libtbe.so not found at {path}: build it with table_embedding_bags_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.tbe_plan_device_bytes.restype = sz
+    lib.tbe_plan_device_bytes.argtypes = [i32]
+    lib.tbe_plan_create.restype = ctypes.c_int
+    lib.tbe_plan_create.argtypes = [ctypes.POINTER(_Layout), P, sz, P, ctypes.POINTER(P)]
+    lib.tbe_plan_destroy.restype = None
+    lib.tbe_plan_destroy.argtypes = [P]
+    lib.tbe_forward.restype = ctypes.c_int
+    lib.tbe_forward.argtypes = [P, P, P, i64, P, i32, P, P, P, P]
+    lib.tbe_forward_path.restype = ctypes.c_int
+    lib.tbe_forward_path.argtypes = [P, P, P, i64, P, i32, P, P, P, P, i32]
+    lib.tbe_histogram_counts.restype = ctypes.c_int
+    lib.tbe_histogram_counts.argtypes = [P, P, i64, P, i32, P, P, P]
+    lib.tbe_backward_workspace_bytes.restype = sz
+    lib.tbe_backward_workspace_bytes.argtypes = [P, i32, i64]
+    lib.tbe_backward.restype = ctypes.c_int
+    lib.tbe_backward.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, sz, P, P]
+    lib.tbe_get_tuning.restype = ctypes.c_int
+    lib.tbe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
+    lib.tbe_set_tuning.restype = ctypes.c_int
+    lib.tbe_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
+    lib.tbe_trace_enable.restype = ctypes.c_int
+    lib.tbe_trace_enable.argtypes = [i32]
+    lib.tbe_trace_read.restype = ctypes.c_int
+    lib.tbe_trace_read.argtypes = [P, P, i32]
+    lib.tbe_status_string.restype = ctypes.c_char_p
+    lib.tbe_status_string.argtypes = [i32]
+    lib.tbe_version.restype = ctypes.c_char_p
+    lib.tbe_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != TBE_OK:
+        msg = load_library().tbe_status_string(rc).decode()
+        raise TBEError(f"{what} failed: {msg} ({rc})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _np(a, dt):
+    return np.ascontiguousarray(np.asarray(a), dtype=dt)
+
+
+class Plan:
+    """A validated table layout with its packed metadata on the device."""
+
+    def __init__(self, T, table_row_base, D_offsets, weights_offsets, weights_dtype, out_dtype,
+                 table_weighted=None, device="cuda", stream=None):
+        import torch
+
+        lib = load_library()
+        self.T = int(T)
+        self.table_row_base = _np(table_row_base, np.int64)
+        self.D_offsets = _np(D_offsets, np.int32)
+        self.weights_offsets = _np(weights_offsets, np.int64)
+        self.weights_dtype = _np(weights_dtype, np.int32)
+        self.table_weighted = None if table_weighted is None else _np(table_weighted, np.uint8)
+        self.out_dtype = int(out_dtype)
+        self.sumD = int(self.D_offsets[-1])
+        self.D = np.diff(self.D_offsets).astype(np.int64)
+        nbytes = lib.tbe_plan_device_bytes(self.T)
+        if nbytes == 0:
+            raise TBEError("tbe_plan_device_bytes: T out of range")
+        self.dev_meta = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        L = _Layout(self.T, self.table_row_base.ctypes.data, self.D_offsets.ctypes.data,
+                    self.weights_offsets.ctypes.data, self.weights_dtype.ctypes.data,
+                    None if self.table_weighted is None else self.table_weighted.ctypes.data,
+                    self.out_dtype)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(self.dev_meta.device):
+            _check(lib.tbe_plan_create(ctypes.byref(L), _ptr(self.dev_meta), nbytes, _stream(stream),
+                                       ctypes.byref(h)), "tbe_plan_create")
+        self._h = h
+
+    @classmethod
+    def from_problem(cls, p, device="cuda"):
+        lay = p.layout_arrays()
+        return cls(lay["T"], lay["table_row_base"], lay["D_offsets"], lay["weights_offsets"],
+                   lay["weights_dtype"], lay["out_dtype"], lay["table_weighted"], device=device)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.tbe_plan_destroy(h)
+            self._h = None
+
+
+def _out_torch_dtype(code):
+    import torch
+
+    return {TBE_F32: torch.float32, TBE_F16: torch.float16, TBE_BF16: torch.bfloat16}[code]
+
+
+def tbe_forward(plan: Plan, weights, indices, offsets, B: int, per_sample_weights=None, out=None,
+                dev_status=None, path: int = TBE_PATH_AUTO, stream=None):
+    """Pooled forward; returns ``out`` [B, sum D] on the device."""
+    import torch
+
+    lib = load_library()
+    if out is None:
+        out = torch.empty((B, plan.sumD), dtype=_out_torch_dtype(plan.out_dtype), device=indices.device)
+    N = int(indices.numel())
+    rc = lib.tbe_forward_path(plan.handle, _ptr(weights), _ptr(indices), N, _ptr(offsets), int(B),
+                              _ptr(per_sample_weights), _ptr(out), _ptr(dev_status), _stream(stream), int(path))
+    _check(rc, "tbe_forward")
+    return out
+
+
+def tbe_histogram_counts(plan: Plan, indices, offsets, B: int, counts=None, dev_status=None, stream=None):
+    import torch
+
+    lib = load_library()
+    rows = int(plan.table_row_base[1] - plan.table_row_base[0])
+    if counts is None:
+        counts = torch.empty((B, rows), dtype=torch.int32, device=indices.device)
+    rc = lib.tbe_histogram_counts(plan.handle, _ptr(indices), int(indices.numel()), _ptr(offsets), int(B),
+                                  _ptr(counts), _ptr(dev_status), _stream(stream))
+    _check(rc, "tbe_histogram_counts")
+    return counts
+
+
+def tbe_backward_workspace_bytes(plan: Plan, B: int, N: int) -> int:
+    return int(load_library().tbe_backward_workspace_bytes(plan.handle, int(B), int(N)))
+
+
+class BackwardBuffers:
+    """Preallocated outputs + workspace for one (B, N) capacity."""
+
+    def __init__(self, plan: Plan, B: int, N: int, device="cuda", row_grads_capacity=None):
+        import torch
+
+        self.B, self.N = int(B), int(N)
+        ws = tbe_backward_workspace_bytes(plan, B, N)
+        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.unique_rows = torch.empty(max(N, 1), dtype=torch.int64, device=device)
+        self.run_starts = torch.empty(N + 1, dtype=torch.int32, device=device)
+        self.sorted_positions = torch.empty(max(N, 1), dtype=torch.int32, device=device)
+        if row_grads_capacity is None:
+            total_rows = int(plan.table_row_base[-1])
+            row_grads_capacity = min(N, total_rows) * int(plan.D.max()) if N else 0
+        self.row_grads = torch.empty(max(int(row_grads_capacity), 1), dtype=torch.float32, device=device)
+        self.row_grads_capacity = int(row_grads_capacity)
+        self.unique_count = torch.empty(plan.T + 1, dtype=torch.int64, device=device)
+
+
+def tbe_backward(plan: Plan, grad_out, indices, offsets, B: int, per_sample_weights=None, bufs=None,
+                 dev_status=None, want_run_starts=True, want_sorted_positions=True, stream=None):
+    """Row gradients.  Returns the BackwardBuffers whose leading entries hold
+    the results (U = unique_count[T], read it after a synchronisation)."""
+    lib = load_library()
+    N = int(indices.numel())
+    if bufs is None:
+        bufs = BackwardBuffers(plan, B, N, device=indices.device)
+    rc = lib.tbe_backward(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
+                          _ptr(per_sample_weights), _ptr(bufs.unique_rows),
+                          _ptr(bufs.run_starts) if want_run_starts else None,
+                          _ptr(bufs.sorted_positions) if want_sorted_positions else None,
+                          _ptr(bufs.row_grads), bufs.row_grads_capacity, _ptr(bufs.unique_count),
+                          _ptr(bufs.workspace), bufs.workspace.numel(), _ptr(dev_status), _stream(stream))
+    _check(rc, "tbe_backward")
+    return bufs
+
+
+def get_tuning() -> dict:
+    t = Tuning()
+    _check(load_library().tbe_get_tuning(ctypes.byref(t)), "tbe_get_tuning")
+    return t.as_dict()
+
+
+def set_tuning(**kw) -> dict:
+    t = Tuning()
+    lib = load_library()
+    _check(lib.tbe_get_tuning(ctypes.byref(t)), "tbe_get_tuning")
+    for k, v in kw.items():
+        setattr(t, k, int(v))
+    _check(lib.tbe_set_tuning(ctypes.byref(t)), "tbe_set_tuning")
+    return t.as_dict()
+
+
+def trace_enable(on: bool = True):
+    _check(load_library().tbe_trace_enable(1 if on else 0), "tbe_trace_enable")
+
+
+def trace_read(max_stages: int = 32):
+    """[(stage_name, ms), ...] of the last traced call (waits for it)."""
+    ms = (ctypes.c_float * max_stages)()
+    names = (ctypes.c_char_p * max_stages)()
+    n = load_library().tbe_trace_read(ms, names, max_stages)
+    if n < 0:
+        raise TBEError(f"tbe_trace_read failed ({-n})")
+    return [(names[k].decode(), float(ms[k])) for k in range(n)]
+
+
+def version() -> str:
+    return load_library().tbe_version().decode()

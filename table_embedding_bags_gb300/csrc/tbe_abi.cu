@@ -1,0 +1,377 @@
+// tbe_abi.cu -- the C ABI of libtbe: argument validation, plans, dispatch,
+// tuning and stage tracing.  Every entry point only enqueues kernels on the
+// caller's stream; none synchronises or allocates device memory.
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "tbe_internal.cuh"
+
+namespace tbe {
+
+// Defaults come from the measured sweeps recorded with the benchmark.
+static Tuning g_tuning = {/*long_run_threshold=*/256, /*long_chunk=*/256, /*fwd_unroll=*/8,
+                          /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48};
+
+const Tuning& tuning() { return g_tuning; }
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int check_launch() { return cudaGetLastError() == cudaSuccess ? TBE_OK : TBE_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// stage tracing
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kMaxStages = 32;
+struct Trace {
+  std::mutex mu;
+  bool on = false;
+  int device = -1;
+  cudaEvent_t ev[kMaxStages + 1] = {};
+  const char* names[kMaxStages + 1] = {};
+  int n = 0;  // events recorded by the last call (including the start event)
+};
+Trace g_trace;
+}  // namespace
+
+void trace_begin(cudaStream_t s) {
+  if (!g_trace.on) return;
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  g_trace.n = 0;
+  if (cudaEventRecord(g_trace.ev[0], s) == cudaSuccess) g_trace.n = 1;
+  g_trace.names[0] = "start";
+}
+
+void trace_mark(cudaStream_t s, const char* name) {
+  if (!g_trace.on) return;
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  if (g_trace.n == 0 || g_trace.n > kMaxStages) return;
+  if (cudaEventRecord(g_trace.ev[g_trace.n], s) == cudaSuccess) g_trace.names[g_trace.n++] = name;
+}
+
+}  // namespace tbe
+
+using namespace tbe;
+
+struct tbe_plan : public tbe::Plan {};
+
+extern "C" {
+
+const char* tbe_version(void) { return "libtbe 0.1 (sm_103a)"; }
+
+const char* tbe_status_string(int32_t code) {
+  switch (code) {
+    case TBE_OK: return "ok";
+    case TBE_ERR_INVALID_ARG: return "invalid argument";
+    case TBE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case TBE_ERR_CUDA: return "CUDA error";
+    case TBE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int tbe_get_tuning(tbe_tuning* out) {
+  if (!out) return TBE_ERR_INVALID_ARG;
+  out->long_run_threshold = g_tuning.long_run_threshold;
+  out->long_chunk = g_tuning.long_chunk;
+  out->fwd_unroll = g_tuning.fwd_unroll;
+  out->fwd_blocks_per_sm = g_tuning.fwd_blocks_per_sm;
+  out->hist_min_mean_bag = g_tuning.hist_min_mean_bag;
+  return TBE_OK;
+}
+
+int tbe_set_tuning(const tbe_tuning* in) {
+  if (!in) return TBE_ERR_INVALID_ARG;
+  if (in->long_run_threshold < 1 || in->long_run_threshold > (1 << 20)) return TBE_ERR_INVALID_ARG;
+  if (in->long_chunk < 32 || in->long_chunk > 65536 || (in->long_chunk % 32) != 0) return TBE_ERR_INVALID_ARG;
+  if (in->fwd_unroll != 2 && in->fwd_unroll != 4 && in->fwd_unroll != 8) return TBE_ERR_INVALID_ARG;
+  if (in->fwd_blocks_per_sm < 0 || in->fwd_blocks_per_sm > 32) return TBE_ERR_INVALID_ARG;
+  if (in->hist_min_mean_bag < 0) return TBE_ERR_INVALID_ARG;
+  g_tuning.long_run_threshold = in->long_run_threshold;
+  g_tuning.long_chunk = in->long_chunk;
+  g_tuning.fwd_unroll = in->fwd_unroll;
+  g_tuning.fwd_blocks_per_sm = in->fwd_blocks_per_sm;
+  g_tuning.hist_min_mean_bag = in->hist_min_mean_bag;
+  return TBE_OK;
+}
+
+int tbe_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TBE_ERR_CUDA;
+  if (on && (g_trace.device != dev || g_trace.ev[0] == nullptr)) {
+    for (int k = 0; k <= kMaxStages; ++k) {
+      if (g_trace.ev[k]) cudaEventDestroy(g_trace.ev[k]);
+      if (cudaEventCreate(&g_trace.ev[k]) != cudaSuccess) return TBE_ERR_CUDA;
+    }
+    g_trace.device = dev;
+  }
+  g_trace.on = on != 0;
+  g_trace.n = 0;
+  return TBE_OK;
+}
+
+int tbe_trace_read(float* stage_ms, const char** stage_names, int32_t max_stages) {
+  std::lock_guard<std::mutex> lk(g_trace.mu);
+  if (g_trace.n < 1) return 0;
+  if (cudaEventSynchronize(g_trace.ev[g_trace.n - 1]) != cudaSuccess) return -TBE_ERR_CUDA;
+  int ns = std::min<int>(g_trace.n - 1, max_stages);
+  for (int k = 0; k < ns; ++k) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_trace.ev[k], g_trace.ev[k + 1]) != cudaSuccess) return -TBE_ERR_CUDA;
+    if (stage_ms) stage_ms[k] = ms;
+    if (stage_names) stage_names[k] = g_trace.names[k + 1];
+  }
+  return ns;
+}
+
+// ---------------------------------------------------------------------------
+// plans
+// ---------------------------------------------------------------------------
+
+size_t tbe_plan_device_bytes(int32_t T) {
+  if (T < 1 || T > TBE_MAX_TABLES) return 0;
+  size_t b = sizeof(TableMeta) * (size_t)(T + 1);
+  return (b + 255) / 256 * 256;
+}
+
+static int elem_size(int32_t dt) { return dt == TBE_F32 ? 4 : 2; }
+
+int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, void* stream,
+                    tbe_plan** plan_out) {
+  if (!L || !plan_out || !dev_meta) return TBE_ERR_INVALID_ARG;
+  *plan_out = nullptr;
+  const int32_t T = L->T;
+  if (T < 1 || T > TBE_MAX_TABLES) return TBE_ERR_INVALID_ARG;
+  if (!L->table_row_base || !L->D_offsets || !L->weights_offsets || !L->weights_dtype)
+    return TBE_ERR_INVALID_ARG;
+  if (L->out_dtype < TBE_F32 || L->out_dtype > TBE_BF16) return TBE_ERR_INVALID_ARG;
+  if (dev_meta_bytes < tbe_plan_device_bytes(T) || ((uintptr_t)dev_meta & 15)) return TBE_ERR_INVALID_ARG;
+  if (L->table_row_base[0] != 0 || L->D_offsets[0] != 0) return TBE_ERR_INVALID_ARG;
+
+  tbe_plan* p = new (std::nothrow) tbe_plan();
+  if (!p) return TBE_ERR_INVALID_ARG;
+  p->hmeta = new (std::nothrow) TableMeta[T + 1];
+  if (!p->hmeta) { delete p; return TBE_ERR_INVALID_ARG; }
+  std::memset(p->hmeta, 0, sizeof(TableMeta) * (T + 1));
+  int status = TBE_OK;
+  int dtype_mask = 0, any_weighted = 0, maxD = 0;
+  const int osz = elem_size(L->out_dtype);
+  int out_vec_ok = 1;
+  for (int32_t t = 0; t < T && status == TBE_OK; ++t) {
+    const int64_t rows = L->table_row_base[t + 1] - L->table_row_base[t];
+    const int32_t D = L->D_offsets[t + 1] - L->D_offsets[t];
+    const int32_t dt = L->weights_dtype[t];
+    if (rows < 0 || D <= 0 || dt < TBE_F32 || dt > TBE_BF16 || L->weights_offsets[t] < 0) {
+      status = TBE_ERR_INVALID_ARG;
+      break;
+    }
+    if (rows >= (int64_t(1) << 31) || ((int64_t)D * elem_size(dt)) % 16 != 0 ||
+        (L->weights_offsets[t] % 16) != 0) {
+      status = TBE_ERR_UNSUPPORTED;
+      break;
+    }
+    TableMeta& m = p->hmeta[t];
+    m.w_off = L->weights_offsets[t];
+    m.row_base = L->table_row_base[t];
+    m.rows = (int32_t)rows;
+    m.col_off = L->D_offsets[t];
+    m.D = D;
+    m.dtype = (uint8_t)dt;
+    m.weighted = L->table_weighted ? (L->table_weighted[t] ? 1 : 0) : 1;
+    dtype_mask |= 1 << dt;
+    any_weighted |= m.weighted;
+    maxD = std::max(maxD, D);
+    if (((int64_t)m.col_off * osz) % 16 != 0) out_vec_ok = 0;
+  }
+  const int64_t total_rows = L->table_row_base[T];
+  if (status == TBE_OK && (total_rows >= 0xffffffffLL || (int64_t)L->D_offsets[T] >= (int64_t(1) << 31)))
+    status = TBE_ERR_UNSUPPORTED;
+  if (status != TBE_OK) {
+    delete[] p->hmeta;
+    delete p;
+    return status;
+  }
+  p->hmeta[T].row_base = total_rows;
+  p->T = T;
+  p->out_dtype = L->out_dtype;
+  p->sumD = L->D_offsets[T];
+  p->maxD = maxD;
+  p->total_rows = total_rows;
+  int kb = 1;
+  while (kb < 32 && (total_rows >> kb) != 0) ++kb;
+  p->key_bits = kb;
+  p->dtype_mask = dtype_mask;
+  p->any_weighted = any_weighted;
+  if (((int64_t)p->sumD * osz) % 16 != 0) out_vec_ok = 0;
+  p->out_vec_ok = out_vec_ok;
+  p->hist_ok = (T == 1 && L->weights_dtype[0] == TBE_F16 && p->hmeta[0].rows >= 1 &&
+                p->hmeta[0].rows <= TBE_HIST_MAX_ROWS && p->hmeta[0].D % 16 == 0 && p->hmeta[0].D <= 256);
+  cudaGetDevice(&p->device);
+  p->dmeta = reinterpret_cast<const TableMeta*>(dev_meta);
+  if (cudaMemcpyAsync(dev_meta, p->hmeta, sizeof(TableMeta) * (T + 1), cudaMemcpyHostToDevice,
+                      (cudaStream_t)stream) != cudaSuccess) {
+    delete[] p->hmeta;
+    delete p;
+    return TBE_ERR_CUDA;
+  }
+  *plan_out = p;
+  return TBE_OK;
+}
+
+void tbe_plan_destroy(tbe_plan* plan) {
+  if (!plan) return;
+  delete[] plan->hmeta;
+  delete plan;
+}
+
+// ---------------------------------------------------------------------------
+// forward
+// ---------------------------------------------------------------------------
+
+static int check_common(const tbe_plan* plan, const int64_t* indices, int64_t N, const int64_t* offsets,
+                        int32_t B) {
+  if (!plan) return TBE_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || N >= (int64_t(1) << 30)) return TBE_ERR_INVALID_ARG;
+  if ((int64_t)plan->T * B >= (int64_t(1) << 31)) return TBE_ERR_UNSUPPORTED;
+  if ((int64_t)plan->T * B > 0 && !offsets) return TBE_ERR_INVALID_ARG;
+  if ((int64_t)plan->T * B == 0 && N != 0) return TBE_ERR_INVALID_ARG;  // no bag can hold a lookup
+  if (N > 0 && !indices) return TBE_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TBE_ERR_CUDA;
+  if (dev != plan->device) return TBE_ERR_INVALID_ARG;
+  return TBE_OK;
+}
+
+static bool hist_eligible(const tbe_plan* plan, const float* psw) {
+  return plan->hist_ok && (psw == nullptr || !plan->hmeta[0].weighted);
+}
+
+int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
+                     const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                     int32_t* dev_status, void* stream, int32_t path) {
+  int st = check_common(plan, indices, N, offsets, B);
+  if (st != TBE_OK) return st;
+  if (path < TBE_PATH_AUTO || path > TBE_PATH_HISTOGRAM) return TBE_ERR_INVALID_ARG;
+  if ((int64_t)plan->T * B == 0) return TBE_OK;
+  if (!out || !weights) return TBE_ERR_INVALID_ARG;
+  if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  FwdArgs a;
+  a.weights = reinterpret_cast<const uint8_t*>(weights);
+  a.meta = plan->dmeta;
+  a.indices = indices;
+  a.offsets = offsets;
+  a.psw = per_sample_weights;
+  a.out = out;
+  a.status = dev_status;
+  a.T = plan->T;
+  a.B = B;
+  a.N = N;
+  a.sumD = plan->sumD;
+  a.out_vec_ok = plan->out_vec_ok && (((uintptr_t)out & 15) == 0);
+  bool hist = false;
+  if (path == TBE_PATH_HISTOGRAM) {
+    if (!hist_eligible(plan, per_sample_weights)) return TBE_ERR_UNSUPPORTED;
+    hist = true;
+  } else if (path == TBE_PATH_AUTO) {
+    hist = hist_eligible(plan, per_sample_weights) &&
+           N >= (int64_t)g_tuning.hist_min_mean_bag * (int64_t)B;
+  }
+  trace_begin(s);
+  st = hist ? launch_forward_histogram(*plan, a, nullptr, s) : launch_forward_gather(*plan, a, s);
+  trace_mark(s, hist ? "fwd_histogram" : "fwd_gather");
+  return st;
+}
+
+int tbe_forward(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
+                const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                int32_t* dev_status, void* stream) {
+  return tbe_forward_path(plan, weights, indices, N, offsets, B, per_sample_weights, out, dev_status,
+                          stream, TBE_PATH_AUTO);
+}
+
+int tbe_histogram_counts(const tbe_plan* plan, const int64_t* indices, int64_t N, const int64_t* offsets,
+                         int32_t B, int32_t* counts, int32_t* dev_status, void* stream) {
+  int st = check_common(plan, indices, N, offsets, B);
+  if (st != TBE_OK) return st;
+  if (!plan->hist_ok) return TBE_ERR_UNSUPPORTED;
+  if (B == 0) return TBE_OK;
+  if (!counts) return TBE_ERR_INVALID_ARG;
+  FwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.meta = plan->dmeta;
+  a.indices = indices;
+  a.offsets = offsets;
+  a.status = dev_status;
+  a.T = plan->T;
+  a.B = B;
+  a.N = N;
+  a.sumD = plan->sumD;
+  return launch_forward_histogram(*plan, a, counts, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------------------
+// backward
+// ---------------------------------------------------------------------------
+
+size_t tbe_backward_workspace_bytes(const tbe_plan* plan, int32_t B, int64_t N) {
+  if (!plan || B < 0 || N < 0) return 0;
+  return backward_workspace_bytes(*plan, B, N);
+}
+
+int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
+                 const int64_t* offsets, int32_t B, const float* per_sample_weights,
+                 int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
+                 int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  int st = check_common(plan, indices, N, offsets, B);
+  if (st != TBE_OK) return st;
+  if (!unique_count || row_grads_capacity < 0) return TBE_ERR_INVALID_ARG;
+  if (N > 0 && (!unique_rows || !grad_out || (!row_grads && row_grads_capacity > 0)))
+    return TBE_ERR_INVALID_ARG;
+  if ((uintptr_t)grad_out & 15) return TBE_ERR_UNSUPPORTED;
+  if ((plan->sumD % 4) != 0) return TBE_ERR_UNSUPPORTED;
+  for (int t = 0; t < plan->T; ++t)
+    if (plan->hmeta[t].D % 4 != 0) return TBE_ERR_UNSUPPORTED;
+  const size_t need = backward_workspace_bytes(*plan, B, N);
+  if (workspace_bytes < need || (need > 0 && !workspace)) return TBE_ERR_WORKSPACE;
+  if (((uintptr_t)workspace & 255) != 0) return TBE_ERR_INVALID_ARG;
+  BwdArgs a;
+  a.grad_out = grad_out;
+  a.meta = plan->dmeta;
+  a.indices = indices;
+  a.offsets = offsets;
+  a.psw = per_sample_weights;
+  a.unique_rows = unique_rows;
+  a.run_starts = run_starts;
+  a.sorted_positions = sorted_positions;
+  a.row_grads = row_grads;
+  a.row_grads_capacity = row_grads_capacity;
+  a.unique_count = unique_count;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.status = dev_status;
+  a.T = plan->T;
+  a.B = B;
+  a.N = N;
+  a.sumD = plan->sumD;
+  cudaStream_t s = (cudaStream_t)stream;
+  trace_begin(s);
+  return launch_backward(*plan, a, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,1005 @@
+// tbe_backward.cu -- sparse row-gradient backward of table-batched embedding bags.
+//
+// [FBT] = the page "FBTriton table-batched embeddings: the backward win is a
+// threshold moved from 32 to 256".
+//
+// What is computed ([FBT] "Why the backward is the hard half"): the table
+// gradient is zero except on rows some bag read; row r receives
+//   row_grad[r, c] = sum_{i : table_row_base[t_i] + id_i = r} w_i * G[b_i, D_offsets[t_i] + c].
+// The batch is inverted by sorting: every lookup gets the key
+// table_row_base[t] + id (rows of different tables never collide), equal
+// keys form runs, and each run is an independent unit reduced without
+// atomics on its output row.  Runs are routed by length ([FBT] "Three tiers,
+// routed by run length"): a run shorter than the threshold is reduced by
+// one warp; a longer run is cut into chunks whose partial sums meet in a
+// workspace and are combined by the last chunk to finish, which learns it
+// is last from a counter decremented after a device-scope fence ([FBT]
+// "Three tiers, routed by run length", the fused tier).
+//
+// Kernels, in stream order (no host synchronisation anywhere):
+//   0. memset of the counter / look-back region of the workspace
+//   1. linearize: bag of every position, key = row base + id (or the
+//      sentinel total_rows for an id outside its table), bag sample index,
+//      and the digit histograms of every radix pass
+//   2. one onesweep pass per 8-bit digit: stable LSD radix sort of
+//      (key, position) with per-tile digit ranks and a decoupled look-back
+//      over tiles taken in launch order (every wait is bounded)
+//   3. run-length segmentation: unique rows and run starts (look-back scan)
+//   4. classify: long runs are compacted with one atomic per block; the
+//      counts stay on the device ([FBT] "Three tiers, routed by run
+//      length", the classification kernel); also the per-table run counts
+//   5. reduce: one persistent kernel whose warps take work items from a
+//      device counter -- first the long-run chunks, then batches of 32
+//      consecutive runs whose short runs the warp reduces itself.
+#include <algorithm>
+
+#include "tbe_internal.cuh"
+
+namespace tbe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// tile sizes and look-back flags
+// ---------------------------------------------------------------------------
+constexpr int kLinThreads = 256;
+constexpr int kLinTile = 2048;       // positions per linearize block
+constexpr int kLinOffs = 2048;       // bag offsets staged in shared memory
+
+constexpr int kSortThreads = 256;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSortIPT = 12;         // keys per thread
+constexpr int kSortTile = kSortThreads * kSortIPT;
+
+constexpr int kRleThreads = 256;
+constexpr int kRleIPT = 8;
+constexpr int kRleTile = kRleThreads * kRleIPT;
+
+constexpr int kClsThreads = 256;
+constexpr int kRedThreads = 256;
+constexpr int kFanIn = 32;           // children per node of the long-run combine tree
+
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagInc = 2u << 30;
+constexpr uint32_t kValMask = (1u << 30) - 1;
+constexpr int kSpinLimit = 1 << 22;  // polls before a wait gives up (TBE_DEV_TIMEOUT)
+
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits (bounded) for a published look-back word; returns 0 on time-out.
+__device__ __forceinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status) {
+  for (int it = 0; it < kSpinLimit; ++it) {
+    uint32_t v = ld_relaxed(p);
+    if (v & (kFlagAgg | kFlagInc)) return v;
+    if (it > 64) __nanosleep(100);
+  }
+  report(status, TBE_DEV_TIMEOUT);
+  return kFlagInc;  // treat as an inclusive zero so no later tile waits on it
+}
+
+__device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T, int64_t row) {
+  int lo = 0, hi = T - 1;  // largest t with row_base[t] <= row
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(&meta[mid].row_base) <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+struct Layout {
+  size_t keys_a, keys_b, vals_a, vals_b, bag_of, run_starts, long_list, gofs, partials;
+  size_t zero_begin, hist, sort_tiles, sort_lookback, rle_tile, rle_lookback, counters, combine,
+      zero_end;
+  size_t total;
+  int npass, sort_ntiles, rle_ntiles;
+  int64_t long_cap, chunk_cap;
+  int32_t slot_floats;
+};
+
+// counters: 8-byte slots; kCntLong holds (long runs << 32) | chunks
+enum Counter { kCntU = 0, kCntInvalid = 1, kCntWork = 2, kCntLong = 4, kNumCounters = 8 };
+
+static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+Layout make_layout(const Plan& p, int32_t B, int64_t N) {
+  (void)B;
+  Layout L{};
+  const Tuning& tu = tuning();
+  L.npass = (p.key_bits + 7) / 8;
+  L.sort_ntiles = (int)((N + kSortTile - 1) / kSortTile);
+  L.rle_ntiles = (int)((N + kRleTile - 1) / kRleTile);
+  const int64_t tau = std::max(1, tu.long_run_threshold);
+  const int64_t C = tu.long_chunk;
+  L.long_cap = N / tau + 1;
+  L.chunk_cap = N / C + L.long_cap + 1;
+  L.slot_floats = (p.maxD + 3) / 4 * 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
+  L.keys_a = take(4 * (size_t)N);
+  L.keys_b = take(4 * (size_t)N);
+  L.vals_a = take(4 * (size_t)N);
+  L.vals_b = take(4 * (size_t)N);
+  L.bag_of = take(4 * (size_t)N);
+  L.run_starts = take(4 * (size_t)(N + 1));
+  L.long_list = take(16 * (size_t)L.long_cap);
+  L.gofs = take(8 * (size_t)(p.T + 1));
+  L.partials = take(4 * (size_t)L.chunk_cap * L.slot_floats);
+  L.zero_begin = off;
+  L.hist = take(4 * 4 * 256);
+  L.sort_tiles = take(4 * 4);
+  L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * 256);
+  L.rle_tile = take(4);
+  L.rle_lookback = take(4 * (size_t)L.rle_ntiles);
+  L.counters = take(8 * kNumCounters);
+  L.combine = take(4 * (size_t)L.chunk_cap);
+  L.zero_end = off;
+  L.total = off;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// 1. linearize + digit histograms
+// ---------------------------------------------------------------------------
+struct LinArgs {
+  const int64_t* indices;
+  const int64_t* offsets;
+  const TableMeta* meta;
+  uint32_t* keys;
+  int32_t* bag_of;
+  uint32_t* hist;      // [4][256]
+  uint32_t* counters;  // kCntInvalid
+  int32_t* status;
+  int64_t N;
+  int32_t T, B, npass;
+  uint32_t sentinel;   // total_rows
+};
+
+// largest g in [lo, hi] with offsets[g] <= pos (global memory)
+__device__ __forceinline__ int32_t bag_search_global(const int64_t* offsets, int32_t lo, int32_t hi,
+                                                     int64_t pos) {
+  while (lo < hi) {
+    int32_t mid = lo + ((hi - lo + 1) >> 1);
+    if (__ldg(offsets + mid) <= pos) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a) {
+  __shared__ uint32_t s_hist[4][256];
+  __shared__ int64_t s_off[kLinOffs];
+  __shared__ int32_t s_g0, s_ng;
+  const int tid = threadIdx.x;
+  const int32_t nb = a.T * a.B;
+  for (int k = tid; k < 4 * 256; k += kLinThreads) (&s_hist[0][0])[k] = 0;
+  const int64_t p0 = (int64_t)blockIdx.x * kLinTile;
+  const int64_t p1 = min(a.N, p0 + kLinTile);
+  if (tid == 0) {
+    int32_t g0 = bag_search_global(a.offsets, 0, nb - 1, p0);
+    int32_t g1 = bag_search_global(a.offsets, g0, nb - 1, p1 - 1);
+    s_g0 = g0;
+    s_ng = g1 - g0 + 1;
+  }
+  __syncthreads();
+  const int32_t g0 = s_g0, ng = s_ng;
+  const bool staged = ng <= kLinOffs;
+  if (staged)
+    for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
+  __syncthreads();
+  int bad = 0, invalid = 0;
+  for (int64_t i = p0 + tid; i < p1; i += kLinThreads) {
+    int32_t g;
+    if (staged) {
+      int lo = 0, hi = ng - 1;
+      while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      g = g0 + lo;
+    } else {
+      g = bag_search_global(a.offsets, g0, g0 + ng - 1, i);
+    }
+    const int32_t t = g / a.B;
+    const int32_t b = g - t * a.B;
+    const int64_t id = ld_stream_i64(a.indices + i);
+    const int32_t rows = __ldg(&a.meta[t].rows);
+    uint32_t key = a.sentinel;
+    if ((uint64_t)id < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id);
+    else { bad = 1; ++invalid; }
+    a.keys[i] = key;
+    a.bag_of[i] = b;
+    for (int p = 0; p < a.npass; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xff], 1u);
+  }
+  // offsets must start at 0, never decrease and end at N
+  const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
+  for (int64_t g = (int64_t)blockIdx.x * kLinThreads + tid; g < nb; g += gstride) {
+    const int64_t o0 = __ldg(a.offsets + g), o1 = __ldg(a.offsets + g + 1);
+    if (o1 < o0 || (g == 0 && o0 != 0) || (g == nb - 1 && o1 != a.N)) bad |= 2;
+  }
+  if (bad & 1) report(a.status, TBE_DEV_BAD_INDEX);
+  if (bad & 2) report(a.status, TBE_DEV_BAD_OFFSETS);
+  if (invalid) atomicAdd(&a.counters[kCntInvalid * 2], (uint32_t)invalid);
+  __syncthreads();
+  for (int k = tid; k < a.npass * 256; k += kLinThreads) {
+    const uint32_t c = (&s_hist[0][0])[k];
+    if (c) atomicAdd(&a.hist[k], c);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. onesweep radix pass
+// ---------------------------------------------------------------------------
+struct SortArgs {
+  const uint32_t* keys_in;
+  const int32_t* vals_in;  // nullptr: values are the positions themselves
+  uint32_t* keys_out;
+  int32_t* vals_out;
+  const uint32_t* hist;    // [256] digit counts of this pass
+  uint32_t* lookback;      // [ntiles][256]
+  uint32_t* tile_counter;
+  int32_t* status;
+  int32_t N;
+  int32_t shift;
+};
+
+__global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs a) {
+  __shared__ uint32_t s_wcnt[kSortWarps][256];
+  __shared__ uint32_t s_start[256];   // tile-local first slot of each digit
+  __shared__ int32_t s_gbase[256];    // global position of slot 0 of each digit, minus s_start
+  __shared__ uint32_t s_keys[kSortTile];
+  __shared__ int32_t s_vals[kSortTile];
+  __shared__ uint32_t s_scan[kSortWarps];
+  __shared__ int32_t s_tile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
+  for (int k = tid; k < kSortWarps * 256; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
+  __syncthreads();
+  const int32_t tile = s_tile;
+  const int32_t wbase = tile * kSortTile + warp * (32 * kSortIPT);
+
+  uint32_t key[kSortIPT];
+  int32_t val[kSortIPT];
+  uint32_t rank[kSortIPT];
+#pragma unroll
+  for (int k = 0; k < kSortIPT; ++k) {
+    const int32_t idx = wbase + k * 32 + lane;
+    const bool ok = idx < a.N;
+    key[k] = ok ? __ldg(a.keys_in + idx) : 0u;
+    val[k] = ok ? (a.vals_in ? __ldg(a.vals_in + idx) : idx) : 0;
+  }
+  // stable rank inside the warp: items are ordered (k, lane)
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int k = 0; k < kSortIPT; ++k) {
+    const int32_t idx = wbase + k * 32 + lane;
+    const uint32_t d = idx < a.N ? ((key[k] >> a.shift) & 0xffu) : 256u;
+    const uint32_t peers = __match_any_sync(kFull, d);
+    uint32_t before = 0;
+    if (d < 256) before = s_wcnt[warp][d];
+    __syncwarp();
+    if (d < 256) {
+      rank[k] = before + __popc(peers & lt_mask);
+      if ((peers & lt_mask) == 0) s_wcnt[warp][d] = before + __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // per digit: warp-exclusive prefixes and the tile count (thread tid = digit)
+  uint32_t cnt = 0;
+  {
+    const int d = tid;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t c = s_wcnt[w][d];
+      s_wcnt[w][d] = cnt;
+      cnt += c;
+    }
+  }
+  // block exclusive scan of the digit counts -> s_start
+  uint32_t x = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  // global digit base: exclusive scan of this pass's histogram
+  uint32_t h = __ldg(a.hist + tid);
+  uint32_t hx = h;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, hx, o);
+    if (lane >= o) hx += y;
+  }
+  __syncthreads();
+  uint32_t wsum = 0;
+  for (int w = 0; w < warp; ++w) wsum += s_scan[w];
+  s_start[tid] = wsum + x - cnt;
+  __syncthreads();
+  if (lane == 31) s_scan[warp] = hx;
+  __syncthreads();
+  uint32_t hsum = 0;
+  for (int w = 0; w < warp; ++w) hsum += s_scan[w];
+  const uint32_t gdigit = hsum + hx - h;
+  // decoupled look-back over earlier tiles for this digit
+  uint32_t* my = a.lookback + (size_t)tile * 256 + tid;
+  uint32_t excl = 0;
+  if (tile == 0) {
+    st_relaxed(my, kFlagInc | cnt);
+  } else {
+    st_relaxed(my, kFlagAgg | cnt);
+    for (int32_t pt = tile - 1; pt >= 0; --pt) {
+      const uint32_t v = wait_flag(a.lookback + (size_t)pt * 256 + tid, a.status);
+      excl += v & kValMask;
+      if (v & kFlagInc) break;
+    }
+    st_relaxed(my, kFlagInc | ((excl + cnt) & kValMask));
+  }
+  s_gbase[tid] = (int32_t)(gdigit + excl) - (int32_t)s_start[tid];
+  __syncthreads();
+  // place items in tile-local sorted order
+#pragma unroll
+  for (int k = 0; k < kSortIPT; ++k) {
+    const int32_t idx = wbase + k * 32 + lane;
+    if (idx < a.N) {
+      const uint32_t d = (key[k] >> a.shift) & 0xffu;
+      const uint32_t slot = s_start[d] + s_wcnt[warp][d] + rank[k];
+      s_keys[slot] = key[k];
+      s_vals[slot] = val[k];
+    }
+  }
+  __syncthreads();
+  const int32_t n_tile = min(kSortTile, a.N - tile * kSortTile);
+  for (int i = tid; i < n_tile; i += kSortThreads) {
+    const uint32_t k = s_keys[i];
+    const int32_t dst = s_gbase[(k >> a.shift) & 0xffu] + i;
+    if ((uint32_t)dst < (uint32_t)a.N) {  // always true unless a wait timed out
+      a.keys_out[dst] = k;
+      a.vals_out[dst] = s_vals[i];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. run-length segmentation
+// ---------------------------------------------------------------------------
+struct RleArgs {
+  const uint32_t* keys;  // sorted
+  int64_t* unique_rows;
+  int32_t* run_starts;
+  uint32_t* lookback;
+  uint32_t* tile_counter;
+  uint32_t* counters;
+  int32_t* status;
+  int32_t N;
+  int32_t ntiles;
+  uint32_t sentinel;
+};
+
+__global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
+  __shared__ uint32_t s_scan[kRleThreads / 32];
+  __shared__ uint32_t s_excl;
+  __shared__ int32_t s_tile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
+  __syncthreads();
+  const int32_t tile = s_tile;
+  const int32_t j0 = tile * kRleTile + tid * kRleIPT;
+  uint32_t k[kRleIPT];
+  uint32_t prev = (j0 > 0 && j0 - 1 < a.N) ? __ldg(a.keys + j0 - 1) : 0xffffffffu;
+  uint32_t flags = 0, nflag = 0;
+#pragma unroll
+  for (int q = 0; q < kRleIPT; ++q) {
+    const int32_t j = j0 + q;
+    k[q] = j < a.N ? __ldg(a.keys + j) : a.sentinel;
+    const bool f = j < a.N && k[q] < a.sentinel && (j == 0 || k[q] != prev);
+    prev = k[q];
+    flags |= (uint32_t)f << q;
+    nflag += f;
+  }
+  uint32_t x = nflag;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_scan[warp] = x;
+  __syncthreads();
+  uint32_t wsum = 0, total = 0;
+  for (int w = 0; w < kRleThreads / 32; ++w) {
+    if (w < warp) wsum += s_scan[w];
+    total += s_scan[w];
+  }
+  const uint32_t mine = wsum + x - nflag;
+  if (tid == 0) {
+    uint32_t* my = a.lookback + tile;
+    uint32_t excl = 0;
+    if (tile == 0) {
+      st_relaxed(my, kFlagInc | total);
+    } else {
+      st_relaxed(my, kFlagAgg | total);
+      for (int32_t pt = tile - 1; pt >= 0; --pt) {
+        const uint32_t v = wait_flag(a.lookback + pt, a.status);
+        excl += v & kValMask;
+        if (v & kFlagInc) break;
+      }
+      st_relaxed(my, kFlagInc | ((excl + total) & kValMask));
+    }
+    s_excl = excl;
+    if (tile == a.ntiles - 1) {
+      const uint32_t U = min(excl + total, (uint32_t)a.N);
+      const uint32_t n_valid = (uint32_t)a.N - a.counters[kCntInvalid * 2];
+      a.counters[kCntU * 2] = U;
+      a.run_starts[U] = (int32_t)n_valid;
+    }
+  }
+  __syncthreads();
+  uint32_t u = s_excl + mine;
+#pragma unroll
+  for (int q = 0; q < kRleIPT; ++q) {
+    if ((flags & (1u << q)) && u < (uint32_t)a.N) {  // u < N unless a wait timed out
+      a.unique_rows[u] = (int64_t)k[q];
+      a.run_starts[u] = j0 + q;
+      ++u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 4. classify runs; per-table run counts and row-gradient offsets
+// ---------------------------------------------------------------------------
+struct ClsArgs {
+  const int64_t* unique_rows;
+  const int32_t* run_starts;
+  const TableMeta* meta;
+  int4* long_list;          // {u, first chunk, chunks, length}
+  unsigned long long* long_counter;  // (runs << 32) | chunks
+  const uint32_t* counters;
+  int64_t* unique_count;    // [T+1]
+  int64_t* gofs;            // [T+1] float offset of each table's block
+  int32_t* status;
+  int64_t capacity;
+  int32_t T;
+  int32_t tau;
+  int32_t chunk;
+};
+
+__global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) {
+  __shared__ uint32_t s_scan[2][kClsThreads / 32];
+  __shared__ unsigned long long s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t U = (int32_t)a.counters[kCntU * 2];
+  if (blockIdx.x == 0) {
+    // unique_count[t] = number of unique rows below table_row_base[t]
+    for (int t = tid; t <= a.T; t += kClsThreads) {
+      const int64_t base = __ldg(&a.meta[t].row_base);
+      int lo = 0, hi = U;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a.unique_rows[mid] < base) lo = mid + 1; else hi = mid;
+      }
+      a.unique_count[t] = lo;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int64_t acc = 0;
+      for (int t = 0; t < a.T; ++t) {
+        a.gofs[t] = acc;
+        acc += (a.unique_count[t + 1] - a.unique_count[t]) * (int64_t)__ldg(&a.meta[t].D);
+      }
+      a.gofs[a.T] = acc;
+      if (acc > a.capacity) report(a.status, TBE_DEV_CAPACITY);
+    }
+  }
+  const int32_t stride = gridDim.x * kClsThreads;
+  for (int32_t u0 = blockIdx.x * kClsThreads; u0 < U; u0 += stride) {
+    const int32_t u = u0 + tid;
+    int32_t len = 0;
+    if (u < U) len = a.run_starts[u + 1] - a.run_starts[u];
+    const bool is_long = u < U && len >= a.tau;
+    const uint32_t nch = is_long ? (uint32_t)((len + a.chunk - 1) / a.chunk) : 0u;
+    uint32_t x0 = is_long, x1 = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y0 = __shfl_up_sync(kFull, x0, o), y1 = __shfl_up_sync(kFull, x1, o);
+      if (lane >= o) { x0 += y0; x1 += y1; }
+    }
+    if (lane == 31) { s_scan[0][warp] = x0; s_scan[1][warp] = x1; }
+    __syncthreads();
+    uint32_t w0 = 0, w1 = 0, t0 = 0, t1 = 0;
+    for (int w = 0; w < kClsThreads / 32; ++w) {
+      if (w < warp) { w0 += s_scan[0][w]; w1 += s_scan[1][w]; }
+      t0 += s_scan[0][w];
+      t1 += s_scan[1][w];
+    }
+    if (tid == 0 && t0 > 0)
+      s_base = atomicAdd(a.long_counter, ((unsigned long long)t0 << 32) | (unsigned long long)t1);
+    __syncthreads();
+    if (is_long) {
+      const uint32_t lpos = (uint32_t)(s_base >> 32) + w0 + x0 - 1;
+      const uint32_t cpos = (uint32_t)(s_base & 0xffffffffu) + w1 + x1 - nch;
+      a.long_list[lpos] = make_int4(u, (int)cpos, (int)nch, len);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 5. reduce: long-run chunks (with the last-arriver combine) and short runs
+// ---------------------------------------------------------------------------
+struct RedArgs {
+  const float* grad_out;
+  const TableMeta* meta;
+  const float* psw;
+  const int32_t* sorted_pos;
+  const int32_t* bag_of;
+  const int64_t* unique_rows;
+  const int32_t* run_starts;
+  const int4* long_list;
+  const unsigned long long* long_counter;
+  uint32_t* counters;
+  uint32_t* combine;
+  float* partials;
+  const int64_t* unique_count;
+  const int64_t* gofs;
+  float* row_grads;
+  int32_t* status;
+  int64_t capacity;
+  int32_t T, sumD, tau, chunk, slot_floats;
+};
+
+// Where run u's row gradient goes and how wide it is.
+struct RunInfo {
+  int64_t out_off;   // float offset in row_grads
+  int32_t col_off;   // first grad_out column of its table
+  int32_t D;
+  int32_t weighted;
+};
+
+__device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
+  const int64_t row = a.unique_rows[u];
+  const int32_t t = table_of_row(a.meta, a.T, row);
+  RunInfo r;
+  r.D = __ldg(&a.meta[t].D);
+  r.col_off = __ldg(&a.meta[t].col_off);
+  r.weighted = (a.psw != nullptr) && __ldg(&a.meta[t].weighted);
+  r.out_off = a.gofs[t] + (int64_t)(u - a.unique_count[t]) * r.D;
+  return r;
+}
+
+// Accumulator of one lane: KB chunks of 4 floats, two interleaved sets.
+template <int KB>
+struct Acc {
+  float v[2][KB][4];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+      for (int k = 0; k < KB; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[s][k][e] = 0.f;
+  }
+  __device__ __forceinline__ void add(int s, int k, const float4& g, float w, bool weighted) {
+    const float f[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[s][k][e] = __fadd_rn(v[s][k][e], weighted ? __fmul_rn(w, f[e]) : f[e]);
+  }
+  __device__ __forceinline__ float4 sum(int k) const {
+    return make_float4(__fadd_rn(v[0][k][0], v[1][k][0]), __fadd_rn(v[0][k][1], v[1][k][1]),
+                       __fadd_rn(v[0][k][2], v[1][k][2]), __fadd_rn(v[0][k][3], v[1][k][3]));
+  }
+};
+
+__device__ __forceinline__ float4 ld_grad(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+constexpr int kKB = 1;                 // chunks of 4 floats per lane -> 128 columns per pass
+constexpr int kColsPerPass = 32 * kKB * 4;
+constexpr int kRedUnroll = 8;          // grad_out slices in flight per warp
+
+// Sum of lookups [j0, j1) of one run (columns [cb, cb + kColsPerPass)).
+__device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int32_t j1, int cb, int lane,
+                            Acc<kKB>& acc) {
+  const int C4 = r.D >> 2;
+  for (int32_t jb = j0; jb < j1; jb += 32) {
+    const int n = min(32, j1 - jb);
+    int32_t my_b = 0;
+    float my_w = 1.f;
+    if (lane < n) {
+      const int32_t pos = __ldg(a.sorted_pos + jb + lane);
+      my_b = __ldg(a.bag_of + pos);
+      if (r.weighted) my_w = __ldg(a.psw + pos);
+    }
+    for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
+      float4 g[kRedUnroll][kKB];
+      float w[kRedUnroll];
+#pragma unroll
+      for (int u = 0; u < kRedUnroll; ++u) {
+        const int q = q0 + u;
+        const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+        w[u] = __shfl_sync(kFull, my_w, q & 31);
+        const float* row = a.grad_out + (int64_t)b * a.sumD + r.col_off;
+#pragma unroll
+        for (int k = 0; k < kKB; ++k) {
+          const int c = (cb >> 2) + lane + 32 * k;
+          g[u][k] = (q < n && c < C4) ? ld_grad(row + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRedUnroll; ++u)
+#pragma unroll
+        for (int k = 0; k < kKB; ++k) acc.add(u & 1, k, g[u][k], w[u], r.weighted);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_cols(float* dst, const float4* v, int cb, int C4, int lane,
+                                           int64_t limit_floats, int64_t dst_off) {
+#pragma unroll
+  for (int k = 0; k < kKB; ++k) {
+    const int c = (cb >> 2) + lane + 32 * k;
+    if (c < C4 && dst_off + 4 * c + 4 <= limit_floats)
+      *reinterpret_cast<float4*>(dst + dst_off + 4 * c) = v[k];
+  }
+}
+
+// One chunk of a long run.  Its partial sum (all columns) goes to its own
+// workspace slot; then, level by level of a fan-in-32 tree, the chunk that
+// finishes last at a node (it sees the node's arrival counter reach
+// children-1 after a device-scope fence) sums the children in index order
+// and writes the node's slot, or the row gradient at the root.  The order of
+// every sum is fixed, so the result does not depend on arrival order.
+__device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
+  const unsigned long long lc = *a.long_counter;
+  const int32_t n_long = (int32_t)(lc >> 32);
+  // long run whose first chunk e0 <= item (first chunks ascend along the list)
+  int lo = 0, hi = n_long - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.long_list[mid].y <= item) lo = mid; else hi = mid - 1;
+  }
+  const int4 rec = a.long_list[lo];
+  const int32_t u = rec.x, e0 = rec.y, nch = rec.z, len = rec.w;
+  const int32_t k = item - e0;
+  const RunInfo r = run_info(a, u);
+  const int32_t rs = a.run_starts[u];
+  const int32_t j0 = rs + k * a.chunk, j1 = min(rs + len, j0 + a.chunk);
+  const int C4 = r.D >> 2;
+  for (int cb = 0; cb < r.D; cb += kColsPerPass) {
+    Acc<kKB> acc;
+    acc.zero();
+    sum_lookups(a, r, j0, j1, cb, lane, acc);
+    float4 v[kKB];
+#pragma unroll
+    for (int q = 0; q < kKB; ++q) v[q] = acc.sum(q);
+    if (nch == 1)
+      store_cols(a.row_grads, v, cb, C4, lane, a.capacity, r.out_off);
+    else
+      store_cols(a.partials + (int64_t)(e0 + k) * a.slot_floats, v, cb, C4, lane, (int64_t)1 << 62, 0);
+  }
+  if (nch == 1) return;
+  int32_t node = k, span = 1, nodes = nch, cbase = e0;
+  while (true) {
+    const int32_t parent = node / kFanIn;
+    const int32_t pnodes = (nodes + kFanIn - 1) / kFanIn;
+    const int32_t nchild = min(kFanIn, nodes - parent * kFanIn);
+    __threadfence();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) old = atomicAdd(a.combine + cbase + parent, 1u);
+    old = __shfl_sync(kFull, old, 0);
+    if (old != (uint32_t)(nchild - 1)) return;  // another child is still running
+    __threadfence();
+    const int32_t pspan = span * kFanIn;
+    for (int cb = 0; cb < r.D; cb += kColsPerPass) {
+      float4 s[kKB];
+#pragma unroll
+      for (int q = 0; q < kKB; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int ch = 0; ch < nchild; ++ch) {
+        const float* cs = a.partials + (int64_t)(e0 + (parent * kFanIn + ch) * span) * a.slot_floats;
+#pragma unroll
+        for (int q = 0; q < kKB; ++q) {
+          const int c = (cb >> 2) + lane + 32 * q;
+          if (c < C4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(cs + 4 * c));
+            s[q].x = __fadd_rn(s[q].x, x.x);
+            s[q].y = __fadd_rn(s[q].y, x.y);
+            s[q].z = __fadd_rn(s[q].z, x.z);
+            s[q].w = __fadd_rn(s[q].w, x.w);
+          }
+        }
+      }
+      if (pnodes == 1)
+        store_cols(a.row_grads, s, cb, C4, lane, a.capacity, r.out_off);
+      else
+        store_cols(a.partials + (int64_t)(e0 + parent * pspan) * a.slot_floats, s, cb, C4, lane,
+                   (int64_t)1 << 62, 0);
+    }
+    if (pnodes == 1) return;  // root written: the row gradient is complete
+    span = pspan;
+    cbase += pnodes;  // counters of the next level follow this level's
+    node = parent;
+    nodes = pnodes;
+  }
+}
+
+// Batch of 32 consecutive runs; the warp reduces the short ones in run order.
+__device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane) {
+  const int32_t u = batch * 32 + lane;
+  int32_t rs = 0, len = 0;
+  RunInfo r{0, 0, 4, 0};
+  if (u < U) {
+    rs = a.run_starts[u];
+    len = a.run_starts[u + 1] - rs;
+    r = run_info(a, u);
+  }
+  const int32_t cnt = (u < U && len < a.tau) ? len : 0;
+  int32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int32_t total = __shfl_sync(kFull, incl, 31);
+  int maxD = r.D;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) maxD = max(maxD, __shfl_xor_sync(kFull, maxD, o));
+  for (int cb = 0; cb < maxD; cb += kColsPerPass) {
+    Acc<kKB> acc;
+    acc.zero();
+    int cur = -1;  // lane (run) currently accumulated
+    for (int32_t fb = 0; fb < total; fb += 32) {
+      const int n = min(32, total - fb);
+      // lookup f = fb + lane belongs to the first run whose inclusive count exceeds f
+      const int32_t f = fb + lane;
+      int my_r = 0;  // number of runs whose inclusive count is <= f (binary lifting)
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (__shfl_sync(kFull, incl, my_r + step - 1) <= f) my_r += step;
+      int32_t my_b = 0;
+      float my_w = 1.f;
+      {
+        const int32_t r_rs = __shfl_sync(kFull, rs, my_r);
+        const int32_t r_excl = __shfl_sync(kFull, incl - cnt, my_r);
+        const int32_t r_wt = __shfl_sync(kFull, r.weighted, my_r);
+        if (lane < n) {
+          const int32_t pos = __ldg(a.sorted_pos + r_rs + (f - r_excl));
+          my_b = __ldg(a.bag_of + pos);
+          if (r_wt) my_w = __ldg(a.psw + pos);
+        }
+      }
+      for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
+        float4 g[kRedUnroll][kKB];
+        float w[kRedUnroll];
+        int rr[kRedUnroll];
+#pragma unroll
+        for (int uu = 0; uu < kRedUnroll; ++uu) {
+          const int q = q0 + uu;
+          rr[uu] = __shfl_sync(kFull, my_r, q & 31);
+          const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+          w[uu] = __shfl_sync(kFull, my_w, q & 31);
+          const int32_t coff = __shfl_sync(kFull, r.col_off, rr[uu]);
+          const int32_t C4 = __shfl_sync(kFull, r.D, rr[uu]) >> 2;
+          const float* row = a.grad_out + (int64_t)b * a.sumD + coff;
+#pragma unroll
+          for (int k = 0; k < kKB; ++k) {
+            const int c = (cb >> 2) + lane + 32 * k;
+            g[uu][k] = (q < n && c < C4) ? ld_grad(row + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int uu = 0; uu < kRedUnroll; ++uu) {
+          const int q = q0 + uu;
+          if (q >= n) break;
+          if (rr[uu] != cur) {
+            if (cur >= 0) {  // the previous run is complete
+              float4 v[kKB];
+#pragma unroll
+              for (int k = 0; k < kKB; ++k) v[k] = acc.sum(k);
+              const int64_t off = __shfl_sync(kFull, r.out_off, cur);
+              const int C4c = __shfl_sync(kFull, r.D, cur) >> 2;
+              store_cols(a.row_grads, v, cb, C4c, lane, a.capacity, off);
+              acc.zero();
+            }
+            cur = rr[uu];
+          }
+          const int wt = __shfl_sync(kFull, r.weighted, rr[uu]);
+#pragma unroll
+          for (int k = 0; k < kKB; ++k) acc.add(q & 1, k, g[uu][k], w[uu], wt);
+        }
+      }
+    }
+    if (cur >= 0) {
+      float4 v[kKB];
+#pragma unroll
+      for (int k = 0; k < kKB; ++k) v[k] = acc.sum(k);
+      const int64_t off = __shfl_sync(kFull, r.out_off, cur);
+      const int C4c = __shfl_sync(kFull, r.D, cur) >> 2;
+      store_cols(a.row_grads, v, cb, C4c, lane, a.capacity, off);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const RedArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int32_t U = (int32_t)a.counters[kCntU * 2];
+  const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
+  const int32_t n_items = n_chunks + (U + 31) / 32;
+  while (true) {
+    uint32_t item = 0;
+    if (lane == 0) item = atomicAdd(&a.counters[kCntWork * 2], 1u);
+    item = __shfl_sync(kFull, item, 0);
+    if ((int32_t)item >= n_items) break;
+    if ((int32_t)item < n_chunks) long_chunk(a, (int32_t)item, lane);
+    else short_batch(a, (int32_t)item - n_chunks, U, lane);
+  }
+}
+
+int grid_for(const void* kernel, int threads, size_t smem = 0) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess ||
+      per_sm <= 0)
+    per_sm = 1;
+  return per_sm * sm_count();
+}
+
+}  // namespace
+
+size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N) {
+  return make_layout(p, B, N).total;
+}
+
+int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
+  const int64_t N = a.N;
+  if (N == 0) {
+    if (cudaMemsetAsync(a.unique_count, 0, sizeof(int64_t) * (p.T + 1), s) != cudaSuccess) return TBE_ERR_CUDA;
+    if (a.run_starts && cudaMemsetAsync(a.run_starts, 0, sizeof(int32_t), s) != cudaSuccess) return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_empty");
+    return TBE_OK;
+  }
+  const Layout L = make_layout(p, a.B, N);
+  void* ws = a.workspace;
+  if (cudaMemsetAsync(at<char>(ws, L.zero_begin), 0, L.zero_end - L.zero_begin, s) != cudaSuccess)
+    return TBE_ERR_CUDA;
+  trace_mark(s, "bwd_memset");
+  uint32_t* counters = at<uint32_t>(ws, L.counters);
+  const uint32_t sentinel = (uint32_t)p.total_rows;
+
+  LinArgs la;
+  la.indices = a.indices;
+  la.offsets = a.offsets;
+  la.meta = a.meta;
+  la.keys = at<uint32_t>(ws, L.keys_a);
+  la.bag_of = at<int32_t>(ws, L.bag_of);
+  la.hist = at<uint32_t>(ws, L.hist);
+  la.counters = counters;
+  la.status = a.status;
+  la.N = N;
+  la.T = a.T;
+  la.B = a.B;
+  la.npass = L.npass;
+  la.sentinel = sentinel;
+  const int lin_blocks = (int)((N + kLinTile - 1) / kLinTile);
+  linearize_kernel<<<lin_blocks, kLinThreads, 0, s>>>(la);
+  if (check_launch()) return TBE_ERR_CUDA;
+  trace_mark(s, "bwd_linearize");
+
+  int32_t* final_pos = a.sorted_positions ? a.sorted_positions : at<int32_t>(ws, L.vals_b);
+  uint32_t* kin = at<uint32_t>(ws, L.keys_a);
+  uint32_t* kout = at<uint32_t>(ws, L.keys_b);
+  int32_t* vin = nullptr;
+  int32_t* vbuf[2] = {at<int32_t>(ws, L.vals_a), at<int32_t>(ws, L.vals_b)};
+  for (int pass = 0; pass < L.npass; ++pass) {
+    const bool last = pass == L.npass - 1;
+    int32_t* vout = last ? final_pos : vbuf[pass & 1];
+    if (!last && vout == final_pos) vout = vbuf[(pass + 1) & 1];
+    if (vout == vin) vout = (vin == vbuf[0]) ? vbuf[1] : vbuf[0];
+    SortArgs sa;
+    sa.keys_in = kin;
+    sa.vals_in = vin;
+    sa.keys_out = kout;
+    sa.vals_out = vout;
+    sa.hist = at<uint32_t>(ws, L.hist) + 256 * pass;
+    sa.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * 256;
+    sa.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
+    sa.status = a.status;
+    sa.N = (int32_t)N;
+    sa.shift = 8 * pass;
+    sort_pass_kernel<<<L.sort_ntiles, kSortThreads, 0, s>>>(sa);
+    if (check_launch()) return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_sort_pass");
+    std::swap(kin, kout);
+    vin = vout;
+  }
+  const uint32_t* sorted_keys = kin;
+
+  int32_t* run_starts = a.run_starts ? a.run_starts : at<int32_t>(ws, L.run_starts);
+  RleArgs ra;
+  ra.keys = sorted_keys;
+  ra.unique_rows = a.unique_rows;
+  ra.run_starts = run_starts;
+  ra.lookback = at<uint32_t>(ws, L.rle_lookback);
+  ra.tile_counter = at<uint32_t>(ws, L.rle_tile);
+  ra.counters = counters;
+  ra.status = a.status;
+  ra.N = (int32_t)N;
+  ra.ntiles = L.rle_ntiles;
+  ra.sentinel = sentinel;
+  rle_kernel<<<L.rle_ntiles, kRleThreads, 0, s>>>(ra);
+  if (check_launch()) return TBE_ERR_CUDA;
+  trace_mark(s, "bwd_rle");
+
+  const Tuning& tu = tuning();
+  unsigned long long* long_counter = reinterpret_cast<unsigned long long*>(counters + kCntLong * 2);
+  ClsArgs ca;
+  ca.unique_rows = a.unique_rows;
+  ca.run_starts = run_starts;
+  ca.meta = a.meta;
+  ca.long_list = at<int4>(ws, L.long_list);
+  ca.long_counter = long_counter;
+  ca.counters = counters;
+  ca.unique_count = a.unique_count;
+  ca.gofs = at<int64_t>(ws, L.gofs);
+  ca.status = a.status;
+  ca.capacity = a.row_grads_capacity;
+  ca.T = a.T;
+  ca.tau = tu.long_run_threshold;
+  ca.chunk = tu.long_chunk;
+  const int cls_blocks = (int)std::min<int64_t>((N + kClsThreads - 1) / kClsThreads, 4 * sm_count());
+  classify_kernel<<<std::max(cls_blocks, 1), kClsThreads, 0, s>>>(ca);
+  if (check_launch()) return TBE_ERR_CUDA;
+  trace_mark(s, "bwd_classify");
+
+  RedArgs rd;
+  rd.grad_out = a.grad_out;
+  rd.meta = a.meta;
+  rd.psw = a.psw;
+  rd.sorted_pos = final_pos;
+  rd.bag_of = at<int32_t>(ws, L.bag_of);
+  rd.unique_rows = a.unique_rows;
+  rd.run_starts = run_starts;
+  rd.long_list = at<int4>(ws, L.long_list);
+  rd.long_counter = long_counter;
+  rd.counters = counters;
+  rd.combine = at<uint32_t>(ws, L.combine);
+  rd.partials = at<float>(ws, L.partials);
+  rd.unique_count = a.unique_count;
+  rd.gofs = at<int64_t>(ws, L.gofs);
+  rd.row_grads = a.row_grads;
+  rd.status = a.status;
+  rd.capacity = a.row_grads_capacity;
+  rd.T = a.T;
+  rd.sumD = a.sumD;
+  rd.tau = tu.long_run_threshold;
+  rd.chunk = tu.long_chunk;
+  rd.slot_floats = L.slot_floats;
+  static int red_grid[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) dev = 63;
+  if (red_grid[dev] == 0) red_grid[dev] = grid_for((const void*)reduce_kernel, kRedThreads);
+  const int64_t want = ((N + 31) / 32 + 7) / 8 + 1;
+  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[dev], want));
+  reduce_kernel<<<rgrid, kRedThreads, 0, s>>>(rd);
+  if (check_launch()) return TBE_ERR_CUDA;
+  trace_mark(s, "bwd_reduce");
+  return TBE_OK;
+}
+
+}  // namespace tbe

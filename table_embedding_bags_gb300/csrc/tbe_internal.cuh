@@ -1,0 +1,230 @@
+// tbe_internal.cuh -- shared definitions of the libtbe translation units.
+//
+// Page cited throughout: "FBTriton table-batched embeddings: the backward win
+// is a threshold moved from 32 to 256" ([FBT] + section title).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tbe.h"
+
+namespace tbe {
+
+// Packed per-table metadata, one 32-byte record per table plus a sentinel
+// record T whose row_base is the total row count.  Lives in device memory
+// owned by the caller (see tbe_plan_create) and is read through the
+// read-only cache; every warp reads the record of the table it works on.
+struct __align__(16) TableMeta {
+  int64_t w_off;     // byte offset of the table in the packed weight buffer
+  int64_t row_base;  // global row of id 0 ([FBT] hash_size_cumsum[t])
+  int32_t rows;      // rows of the table
+  int32_t col_off;   // output column offset (D_offsets[t])
+  int32_t D;         // width
+  uint8_t dtype;     // TBE_F32 / TBE_F16 / TBE_BF16
+  uint8_t weighted;  // lookups of this table are scaled by per-sample weights
+  uint8_t pad[2];
+};
+static_assert(sizeof(TableMeta) == 32, "TableMeta must stay 32 bytes");
+
+// Host-side plan.
+struct Plan {
+  int32_t T;
+  int32_t out_dtype;
+  int32_t sumD;
+  int32_t maxD;
+  int64_t total_rows;
+  int32_t key_bits;      // bits needed for a global row or the sentinel total_rows
+  int32_t dtype_mask;    // bit d set if some table has dtype d
+  int32_t any_weighted;  // some table is marked weighted
+  int32_t out_vec_ok;    // every output segment start is 16-byte aligned
+  int32_t hist_ok;       // static part of the histogram-path eligibility
+  int32_t device;        // device the plan was created on
+  const TableMeta* dmeta;  // device copy (caller memory)
+  TableMeta* hmeta;        // host copy (T+1 records)
+};
+
+// Process-wide tuning (tbe_set_tuning).
+struct Tuning {
+  int32_t long_run_threshold;
+  int32_t long_chunk;
+  int32_t fwd_unroll;
+  int32_t fwd_blocks_per_sm;
+  int32_t hist_min_mean_bag;
+};
+const Tuning& tuning();
+
+// Stage tracing (tbe_trace_enable / tbe_trace_read).
+void trace_begin(cudaStream_t s);
+void trace_mark(cudaStream_t s, const char* name);
+
+int sm_count();
+int check_launch();  // TBE_OK or TBE_ERR_CUDA after a kernel launch
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void report(int32_t* status, int32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// 16-byte read-only load of table rows (several rows of one bag are in
+// flight at once; the read-only path keeps hot rows in L1/L2).
+__device__ __forceinline__ uint4 ld_row16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Streaming 8-byte load for index / offset arrays that are read once.
+__device__ __forceinline__ int64_t ld_stream_i64(const int64_t* p) {
+  int64_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_stream_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// Elements of a 16-byte chunk as floats.
+template <int DT>
+struct Chunk;
+
+template <>
+struct Chunk<TBE_F32> {
+  static constexpr int kElems = 4;
+  __device__ __forceinline__ static void to_float(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+};
+
+template <>
+struct Chunk<TBE_F16> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void to_float(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[k]);
+      float2 p = __half22float2(h);
+      f[2 * k] = p.x;
+      f[2 * k + 1] = p.y;
+    }
+  }
+};
+
+template <>
+struct Chunk<TBE_BF16> {
+  static constexpr int kElems = 8;
+  __device__ __forceinline__ static void to_float(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {  // bf16 -> fp32 is exact: the bits move up 16 places
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+};
+
+// Store n (4 or 8) floats rounded to the output type; `vec` selects 16-byte
+// stores when the destination is 16-byte aligned.
+template <typename OutT>
+__device__ __forceinline__ void store_out(OutT* dst, const float* f, int n, bool vec);
+
+template <>
+__device__ __forceinline__ void store_out<float>(float* dst, const float* f, int n, bool vec) {
+  if (vec) {
+    for (int k = 0; k < n; k += 4)
+      *reinterpret_cast<float4*>(dst + k) = make_float4(f[k], f[k + 1], f[k + 2], f[k + 3]);
+  } else {
+    for (int k = 0; k < n; ++k) dst[k] = f[k];
+  }
+}
+
+template <>
+__device__ __forceinline__ void store_out<__half>(__half* dst, const float* f, int n, bool vec) {
+  if (vec && n == 8) {
+    uint4 v;
+    __half2 h0 = __floats2half2_rn(f[0], f[1]), h1 = __floats2half2_rn(f[2], f[3]);
+    __half2 h2 = __floats2half2_rn(f[4], f[5]), h3 = __floats2half2_rn(f[6], f[7]);
+    v.x = *reinterpret_cast<uint32_t*>(&h0);
+    v.y = *reinterpret_cast<uint32_t*>(&h1);
+    v.z = *reinterpret_cast<uint32_t*>(&h2);
+    v.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(dst) = v;
+  } else {
+    for (int k = 0; k < n; ++k) dst[k] = __float2half_rn(f[k]);
+  }
+}
+
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* dst, const float* f, int n,
+                                                         bool vec) {
+  if (vec && n == 8) {
+    uint4 v;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(f[0], f[1]), h1 = __floats2bfloat162_rn(f[2], f[3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(f[4], f[5]), h3 = __floats2bfloat162_rn(f[6], f[7]);
+    v.x = *reinterpret_cast<uint32_t*>(&h0);
+    v.y = *reinterpret_cast<uint32_t*>(&h1);
+    v.z = *reinterpret_cast<uint32_t*>(&h2);
+    v.w = *reinterpret_cast<uint32_t*>(&h3);
+    *reinterpret_cast<uint4*>(dst) = v;
+  } else {
+    for (int k = 0; k < n; ++k) dst[k] = __float2bfloat16_rn(f[k]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers (host)
+// ---------------------------------------------------------------------------
+
+struct FwdArgs {
+  const uint8_t* weights;
+  const TableMeta* meta;
+  const int64_t* indices;
+  const int64_t* offsets;
+  const float* psw;
+  void* out;
+  int32_t* status;
+  int32_t T;
+  int32_t B;
+  int64_t N;
+  int32_t sumD;
+  int32_t out_vec_ok;
+};
+
+int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s);
+int launch_forward_histogram(const Plan& p, const FwdArgs& a, int32_t* counts_out, cudaStream_t s);
+
+struct BwdArgs {
+  const float* grad_out;
+  const TableMeta* meta;
+  const int64_t* indices;
+  const int64_t* offsets;
+  const float* psw;
+  int64_t* unique_rows;
+  int32_t* run_starts;
+  int32_t* sorted_positions;
+  float* row_grads;
+  int64_t row_grads_capacity;
+  int64_t* unique_count;
+  void* workspace;
+  size_t workspace_bytes;
+  int32_t* status;
+  int32_t T;
+  int32_t B;
+  int64_t N;
+  int32_t sumD;
+};
+
+size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N);
+int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s);
+
+}  // namespace tbe
