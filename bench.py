@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the table-batched embedding-bag (TBE) hot path on GB300.
+
+One step = one forward (pooled gather) + one backward (sort, segment,
+short/long-run reduce) over one batch of the mid-size skewed workload:
+T=8 fp16 tables of 100,000 rows, D=128, B=2048, Poisson(20) bag lengths,
+Zipf(1.05) ids, fp16 output, fp32 output gradients.  Four index batches are
+generated once, kept resident on the device and rotated; the 129 MB L2 is
+flushed (a 256 MB write, then a 256 MB read of another buffer) before every
+timed step, outside its events.
+
+Metric: effective bytes per second -- every lookup's row (forward) and every
+lookup's output-gradient slice (backward) counted, plus indices, offsets,
+outputs and the unique-row gradients written; see effective_bytes().
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+operator has no exchange step in this build); rank 0 prints the whole-job
+line.  ``--impl reference`` times the CPU oracle on the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "TBE fwd/bwd effective HBM GB/s & M lookups/s (% of 8 TB/s peak)"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = "mid_skewed"
+WORKLOAD_DESC = ("TBE mid-size skewed: T=8 fp16 tables x 100000 rows, D=128, B=2048, bag lengths "
+                 "Poisson(20) (one empty bag per table), ids Zipf(1.05) through a per-table permutation, "
+                 "fp16 output, fp32 grad_out; forward + backward (row gradients)")
+N_BATCHES = 4
+FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def effective_bytes(p, unique_per_table):
+    """Algorithmic bytes of one forward and one backward (no dedup credit).
+
+    FWD = sum_i (D_t*s_w + 8 + 4*weighted) + (T*B+1)*8 + B*sumD*s_out
+    BWD = sum_i (4*D_t + 8 + 4*weighted) + (T*B+1)*8 + sum_t U_t*(8 + 4*D_t)
+    """
+    from tbe_inputs import ELEM_BYTES
+
+    lens = np.diff(p.offsets).reshape(p.T, p.B).sum(axis=1).astype(np.int64)  # lookups per table
+    sw = np.array([ELEM_BYTES[int(d)] for d in p.weights_dtype], np.int64)
+    D = p.D.astype(np.int64)
+    w = (p.table_weighted.astype(np.int64) if p.per_sample_weights is not None else np.zeros(p.T, np.int64))
+    s_out = ELEM_BYTES[int(p.out_dtype)]
+    offs = (p.T * p.B + 1) * 8
+    fwd = int(np.sum(lens * (D * sw + 8 + 4 * w)) + offs + p.B * int(D.sum()) * s_out)
+    U = np.asarray(unique_per_table, np.int64)
+    bwd = int(np.sum(lens * (4 * D + 8 + 4 * w)) + offs + np.sum(U * (8 + 4 * D)))
+    return fwd, bwd
+
+
+def kernel_bytes(p, U_total, npass):
+    """Algorithmic bytes of each backward kernel for one launch (the
+    forward gather's are the forward's effective bytes)."""
+    N = p.N
+    D = int(p.D[0])
+    tb = p.T * p.B
+    return {
+        "bwd_linearize": 8 * N + 8 * (tb + 1) + 4 * N + 4 * N,
+        "bwd_sort_pass": 16 * N,
+        "bwd_rle": 4 * N + 12 * U_total,
+        "bwd_classify": 4 * U_total,
+        "bwd_reduce": N * (4 * D + 4 + 4) + U_total * (8 + 4 + 4 * D),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for _, _, r in rows for k in range(4) if r[k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+class L2Flush:
+    """Evicts the 129 MB L2 between steps: a 256 MB write, then a 256 MB read
+    of another buffer so that the write's dirty lines are written back
+    before the step starts (the step then sees a cold, clean L2)."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def __call__(self, k):
+        import torch
+
+        self.w.fill_(float(k))
+        torch.sum(self.r, dim=0, out=self.acc)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def traffic_from_profiles(kernel):
+    """DRAM bytes per launch measured by ncu for `kernel`, if the committed
+    summary was taken from the current source of that kernel."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    srcs = {"fwd_gather": "tbe_forward.cu", "bwd_reduce": "tbe_backward.cu",
+            "bwd_sort_pass": "tbe_backward.cu", "fwd_histogram": "tbe_histogram.cu"}
+    src = srcs.get(kernel)
+    if src is None:
+        return None
+    h = hashlib.sha256(open(os.path.join(ROOT, "table_embedding_bags_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        if line.startswith("traffic:"):
+            f = dict(kv.split("=", 1) for kv in line[len("traffic:"):].split())
+            if f.get("kernel") == kernel and f.get("src_sha") == h and f.get("workload") == WORKLOAD:
+                return float(f["bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import table_embedding_bags_gb300 as tbe
+    from tbe_inputs import make_config, materialize_weights
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tbe.load_library()
+    probs = [make_config(args.workload, batch=k) for k in range(N_BATCHES)]
+    p0 = probs[0]
+    weights = materialize_weights(p0, device=dev)
+    plan = tbe.Plan.from_problem(p0, device=dev)
+    nmax = max(p.N for p in probs)
+    bufs = tbe.BackwardBuffers(plan, p0.B, nmax, device=dev)
+    out = torch.empty((p0.B, p0.total_D), dtype=torch.float16 if p0.out_dtype == 1 else torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dev_in = []
+    for p in probs:
+        dev_in.append(dict(indices=torch.from_numpy(p.indices).to(dev), offsets=torch.from_numpy(p.offsets).to(dev),
+                           grad=torch.from_numpy(p.grad_out).to(dev),
+                           psw=None if p.per_sample_weights is None else torch.from_numpy(p.per_sample_weights).to(dev)))
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    tbe.trace_enable(True)
+
+    def step(k):
+        d = dev_in[k % N_BATCHES]
+        tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status)
+        tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p0.B, d["psw"], bufs=bufs,
+                         dev_status=status, want_run_starts=False, want_sorted_positions=False)
+
+    for k in range(args.warmup):
+        flush(k)
+        step(k)
+    torch.cuda.synchronize()
+    # unique rows per table of every batch (for the effective bytes)
+    uniq = []
+    for k in range(N_BATCHES):
+        step(k)
+        torch.cuda.synchronize()
+        uc = bufs.unique_count.cpu().numpy()
+        uniq.append(np.diff(uc))
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # one CUDA graph per index batch for the forward and one for the backward:
+    # the timed step replays them, so no host launch gap enters the events
+    graphs = []
+    for k in range(N_BATCHES):
+        d = dev_in[k]
+        gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf):
+            tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status)
+        with torch.cuda.graph(gb):
+            tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p0.B, d["psw"], bufs=bufs,
+                             dev_status=status, want_run_starts=False, want_sorted_positions=False)
+        graphs.append((gf, gb))
+    for k in range(args.warmup):
+        flush(k)
+        graphs[k % N_BATCHES][0].replay()
+        graphs[k % N_BATCHES][1].replay()
+    torch.cuda.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    fwd_ms, bwd_ms, stage = [], [], {}
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush(k)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        gf, gb = graphs[k % N_BATCHES]
+        e0.record(stream)
+        gf.replay()
+        e1.record(stream)
+        gb.replay()
+        e2.record(stream)
+        e2.synchronize()
+        fwd_ms.append(e0.elapsed_time(e1))
+        bwd_ms.append(e1.elapsed_time(e2))
+        for name, ms in tbe.trace_read():
+            stage.setdefault(name, []).append(ms)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    tbe.trace_enable(False)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    eff = [effective_bytes(probs[k % N_BATCHES], uniq[k % N_BATCHES]) for k in range(args.steps)]
+    fwd_bytes = sum(f for f, _ in eff)
+    bwd_bytes = sum(b for _, b in eff)
+    lookups = sum(probs[k % N_BATCHES].N for k in range(args.steps))
+    step_ms = [f + b for f, b in zip(fwd_ms, bwd_ms)]
+    tot_s = sum(step_ms) / 1e3
+
+    # dominant kernel: the forward gather against each backward kernel (the
+    # trace holds one event per launch; the radix passes share one name)
+    npass = (int(p0.table_row_base[-1]).bit_length() + 7) // 8
+    per_kernel = {"fwd_gather": float(np.mean(fwd_ms))}
+    for name, v in stage.items():
+        if name.startswith("bwd_") and name != "bwd_memset":
+            per_kernel[name] = float(np.mean(v))
+    U_mean = float(np.mean([u.sum() for u in uniq]))
+    kb = kernel_bytes(p0, U_mean, npass)
+    kb["fwd_gather"] = float(np.mean([f for f, _ in eff]))
+    dom = max(per_kernel, key=lambda n: per_kernel[n])
+    peak, peak_kind = load_peaks()
+    achieved = kb[dom] / (per_kernel[dom] * 1e-3) / 1e9
+
+    # e2e through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, tbe, torch, plan, probs, weights, out, bufs, status, dev, flush, uniq)
+
+    res = dict(
+        metric=METRIC,
+        value=(fwd_bytes + bwd_bytes) / tot_s / 1e9,
+        unit="GB/s",
+        lookups_per_s_M=lookups / tot_s / 1e6,
+        fwd=dict(GBps=fwd_bytes / (sum(fwd_ms) / 1e3) / 1e9, ms=float(np.mean(fwd_ms)),
+                 Mlookups_per_s=lookups / (sum(fwd_ms) / 1e3) / 1e6,
+                 pct_of_8TBs=100 * fwd_bytes / (sum(fwd_ms) / 1e3) / 1e9 / NOMINAL_HBM_GBS),
+        bwd=dict(GBps=bwd_bytes / (sum(bwd_ms) / 1e3) / 1e9, ms=float(np.mean(bwd_ms)),
+                 Mlookups_per_s=lookups / (sum(bwd_ms) / 1e3) / 1e6,
+                 pct_of_8TBs=100 * bwd_bytes / (sum(bwd_ms) / 1e3) / 1e9 / NOMINAL_HBM_GBS),
+        pct_of_8TBs=100 * (fwd_bytes + bwd_bytes) / tot_s / 1e9 / NOMINAL_HBM_GBS,
+        pct_of_measured_peak=100 * (fwd_bytes + bwd_bytes) / tot_s / 1e9 / peak,
+        stages_ms={k: float(np.mean(v)) for k, v in stage.items()},
+        n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=float(np.mean(step_ms)),
+        wall_s=t_wall,
+        higher_is_better=True, scaling="weak", vs_baseline=None,
+        dtype="f32", data="synthetic",
+        config=dict(workload=WORKLOAD_DESC, global_batch=p0.B * world, tables=p0.T,
+                    lookups_per_step=int(np.mean([p.N for p in probs])), index_batches=N_BATCHES,
+                    l2="flushed before every step (256 MB write + 256 MB read of another buffer, outside the step events)",
+                    table_dtype="f16", accumulate="f32", out_dtype="f16", parallelism=f"replicas x{world}"),
+        roofline=dict(bound="hbm", kernel=dom, achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
+                      peak_kind=f"{peak_kind} (copy)", bytes_per_launch=kb[dom], launch_ms=per_kernel[dom],
+                      traffic=traffic_from_profiles(dom)),
+        clocks=clocks,
+        gpu_launches=args.steps * (1 + 4 + npass),
+        launch="CUDA graph per step (forward graph + backward graph)",
+    )
+    if e2e is not None:
+        res["e2e"] = e2e
+    return res, (fwd_bytes + bwd_bytes), tot_s, lookups
+
+
+def run_e2e(args, tbe, torch, plan, probs, weights, out, bufs, status, dev, flush, uniq):
+    """Same metric through the public API with pinned host buffers: the
+    timed step copies the batch in, runs forward + backward, and reads the
+    results back (pooled output, unique rows and their row gradients)."""
+    host = []
+    for p in probs:
+        host.append(dict(indices=torch.from_numpy(p.indices).pin_memory(),
+                         offsets=torch.from_numpy(p.offsets).pin_memory(),
+                         grad=torch.from_numpy(p.grad_out).pin_memory()))
+    nmax = max(p.N for p in probs)
+    d_ind = torch.empty(nmax, dtype=torch.int64, device=dev)
+    d_off = torch.empty(probs[0].offsets.shape[0], dtype=torch.int64, device=dev)
+    d_grad = torch.empty(probs[0].grad_out.shape, dtype=torch.float32, device=dev)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_rows = torch.empty(nmax, dtype=torch.int64).pin_memory()
+    h_rg = torch.empty(bufs.row_grads.numel(), dtype=torch.float32).pin_memory()
+    h_uc = torch.empty(plan.T + 1, dtype=torch.int64).pin_memory()
+    D = int(probs[0].D[0])
+    times, bin_, bout, nbytes = [], 0, 0, 0
+    for k in range(args.warmup + args.steps):
+        p = probs[k % N_BATCHES]
+        h = host[k % N_BATCHES]
+        flush(k)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        n = p.N
+        d_ind[:n].copy_(h["indices"], non_blocking=True)
+        d_off.copy_(h["offsets"], non_blocking=True)
+        d_grad.copy_(h["grad"], non_blocking=True)
+        tbe.tbe_forward(plan, weights, d_ind[:n], d_off, p.B, None, out=out, dev_status=status)
+        tbe.tbe_backward(plan, d_grad, d_ind[:n], d_off, p.B, None, bufs=bufs, dev_status=status,
+                         want_run_starts=False, want_sorted_positions=False)
+        h_out.copy_(out, non_blocking=True)
+        h_uc.copy_(bufs.unique_count, non_blocking=True)
+        torch.cuda.synchronize()
+        U = int(h_uc[-1])
+        h_rows[:U].copy_(bufs.unique_rows[:U], non_blocking=True)
+        h_rg[:U * D].copy_(bufs.row_grads[:U * D], non_blocking=True)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if k >= args.warmup:
+            times.append(t1 - t0)
+            bi = n * 8 + p.offsets.nbytes + p.grad_out.nbytes
+            bo = out.numel() * out.element_size() + h_uc.numel() * 8 + U * 8 + U * D * 4
+            bin_ += bi
+            bout += bo
+            f, b = effective_bytes(p, uniq[k % N_BATCHES])
+            nbytes += f + b
+    steps = len(times)
+    return dict(value=nbytes / sum(times) / 1e9, unit="GB/s", h2d_bytes_per_step=bin_ // steps,
+                d2h_bytes_per_step=bout // steps, ms_per_step=1e3 * float(np.mean(times)))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and CPU baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_steps(workload, seconds=None, steps=None, nthreads=0):
+    """Time the oracle's forward + backward on full batches of the workload.
+    Returns (effective bytes, seconds, lookups, steps, threads)."""
+    import oracle
+    from tbe_inputs import make_config, materialize_weights
+
+    nthreads = nthreads or (os.cpu_count() or 1)
+    probs = [make_config(workload, batch=k) for k in range(N_BATCHES)]
+    w = materialize_weights(probs[0]).numpy()
+    lay = probs[0].layout_arrays()
+    done, tot_s, tot_b, tot_n = 0, 0.0, 0, 0
+    while True:
+        p = probs[done % N_BATCHES]
+        t0 = time.perf_counter()
+        st, _, _ = oracle.forward(lay, w, p.indices, p.offsets, p.B, p.per_sample_weights, nthreads=nthreads)
+        idx = oracle.backward_indexing(lay, p.indices, p.offsets, p.B)
+        st2, _, _, _ = oracle.backward_values(lay, p.offsets, p.B, p.grad_out, idx, p.per_sample_weights,
+                                              nthreads=nthreads)
+        dt = time.perf_counter() - t0
+        assert st == 0 and st2 == 0
+        f, b = effective_bytes(p, np.diff(idx["unique_count"]))
+        tot_s += dt
+        tot_b += f + b
+        tot_n += p.N
+        done += 1
+        if steps is not None and done >= steps:
+            break
+        if steps is None and tot_s >= seconds:
+            break
+    return tot_b, tot_s, tot_n, done, nthreads
+
+
+def run_reference(args):
+    import oracle
+
+    oracle.load()
+    oracle_steps(args.workload, steps=max(args.warmup, 0) or 1)  # warm-up (page-in, build)
+    b, s, n, steps, cores = oracle_steps(args.workload, steps=args.steps)
+    v = b / s / 1e9
+    return dict(
+        impl="reference", metric=METRIC, value=v, unit="GB/s", lookups_per_s_M=n / s / 1e6,
+        n_gpus=args.gpus, steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * s / steps,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+        config=dict(workload=WORKLOAD_DESC, global_batch=2048, parallelism="cpu"),
+        cpu_baseline=dict(value=v, unit="GB/s", cores=cores, kind="oracle",
+                          sample=f"{steps} full forward+backward batches of the workload (oracle, fp64)"),
+        e2e=dict(value=v, unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+    )
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    res, nbytes, tot_s, lookups = run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([tot_s, nbytes, lookups], dtype=torch.float64, device="cuda")
+        mx = t.clone()
+        dist.all_reduce(mx[:1], op=dist.ReduceOp.MAX)
+        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
+        tot_s = float(mx[0])
+        res["value"] = float(t[1]) / tot_s / 1e9
+        res["lookups_per_s_M"] = float(t[2]) / tot_s / 1e6
+        res["ms_per_step"] = 1e3 * tot_s / args.steps
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            b, s, n, steps, cores = oracle_steps(args.workload, seconds=args.cpu_seconds)
+            res["cpu_baseline"] = dict(value=b / s / 1e9, unit="GB/s", cores=cores, kind="oracle",
+                                       sample=f"{steps} full forward+backward batches of the workload "
+                                              f"({s:.1f} s of CPU work, fp64 oracle)")
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

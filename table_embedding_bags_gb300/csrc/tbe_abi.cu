@@ -11,7 +11,7 @@
 namespace tbe {
 
 // Defaults come from the measured sweeps recorded with the benchmark.
-static Tuning g_tuning = {/*long_run_threshold=*/256, /*long_chunk=*/256, /*fwd_unroll=*/8,
+static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/256, /*fwd_unroll=*/8,
                           /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48};
 
 const Tuning& tuning() { return g_tuning; }
@@ -47,11 +47,20 @@ struct Trace {
 Trace g_trace;
 }  // namespace
 
+// Records `ev` on `s`; inside a stream capture the record becomes a graph
+// node (external record), so replays of the graph time the same stages.
+static cudaError_t record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  return cudaEventRecord(ev, s);
+}
+
 void trace_begin(cudaStream_t s) {
   if (!g_trace.on) return;
   std::lock_guard<std::mutex> lk(g_trace.mu);
   g_trace.n = 0;
-  if (cudaEventRecord(g_trace.ev[0], s) == cudaSuccess) g_trace.n = 1;
+  if (record(g_trace.ev[0], s) == cudaSuccess) g_trace.n = 1;
   g_trace.names[0] = "start";
 }
 
@@ -59,7 +68,7 @@ void trace_mark(cudaStream_t s, const char* name) {
   if (!g_trace.on) return;
   std::lock_guard<std::mutex> lk(g_trace.mu);
   if (g_trace.n == 0 || g_trace.n > kMaxStages) return;
-  if (cudaEventRecord(g_trace.ev[g_trace.n], s) == cudaSuccess) g_trace.names[g_trace.n++] = name;
+  if (record(g_trace.ev[g_trace.n], s) == cudaSuccess) g_trace.names[g_trace.n++] = name;
 }
 
 }  // namespace tbe

@@ -85,6 +85,28 @@ __device__ __forceinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status
   return kFlagInc;  // treat as an inclusive zero so no later tile waits on it
 }
 
+// Exclusive prefix of tile `tile` from the look-back words of its
+// predecessors, read 32 at a time by one warp: the nearest inclusive word
+// ends the walk, aggregate words before it are added.  Every wait is
+// bounded (wait_flag).
+__device__ __forceinline__ uint32_t lookback_window(const uint32_t* words, int32_t tile, int lane,
+                                                    int32_t* status) {
+  uint32_t excl = 0;
+  for (int32_t end = tile - 1; end >= 0; end -= 32) {
+    const int32_t k = end - lane;
+    uint32_t v = k >= 0 ? ld_relaxed(words + k) : kFlagInc;
+    if (!(v & (kFlagAgg | kFlagInc))) v = wait_flag(words + k, status);
+    const unsigned inc = __ballot_sync(kFull, (v & kFlagInc) != 0);
+    const int first = inc ? __ffs(inc) - 1 : 31;  // nearest inclusive predecessor in the window
+    uint32_t x = lane <= first ? (v & kValMask) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    excl += x;
+    if (inc) break;
+  }
+  return excl;
+}
+
 __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T, int64_t row) {
   int lo = 0, hi = T - 1;  // largest t with row_base[t] <= row
   while (lo < hi) {
@@ -98,9 +120,9 @@ __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t keys_a, keys_b, vals_a, vals_b, bag_of, run_starts, long_list, gofs, partials;
-  size_t zero_begin, hist, sort_tiles, sort_lookback, rle_tile, rle_lookback, counters, combine,
-      zero_end;
+  size_t keys_a, keys_b, vals_a, vals_b, bag_of, bag_sorted, psw_sorted, run_starts, long_list, gofs, partials;
+  size_t zero_begin, hist, sort_tiles, rle_tile, counters, zero_end;
+  size_t lin_zero_begin, sort_lookback, rle_lookback, combine, lin_zero_end;
   size_t total;
   int npass, sort_ntiles, rle_ntiles;
   int64_t long_cap, chunk_cap;
@@ -131,19 +153,23 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.vals_a = take(4 * (size_t)N);
   L.vals_b = take(4 * (size_t)N);
   L.bag_of = take(4 * (size_t)N);
+  L.bag_sorted = take(4 * (size_t)N);
+  L.psw_sorted = take(4 * (size_t)N);
   L.run_starts = take(4 * (size_t)(N + 1));
   L.long_list = take(16 * (size_t)L.long_cap);
   L.gofs = take(8 * (size_t)(p.T + 1));
   L.partials = take(4 * (size_t)L.chunk_cap * L.slot_floats);
-  L.zero_begin = off;
+  L.zero_begin = off;  // cleared by a memset before the first kernel
   L.hist = take(4 * 4 * 256);
   L.sort_tiles = take(4 * 4);
-  L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * 256);
   L.rle_tile = take(4);
-  L.rle_lookback = take(4 * (size_t)L.rle_ntiles);
   L.counters = take(8 * kNumCounters);
-  L.combine = take(4 * (size_t)L.chunk_cap);
   L.zero_end = off;
+  L.lin_zero_begin = off;  // cleared by the linearize kernel
+  L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * 256);
+  L.rle_lookback = take(4 * (size_t)L.rle_ntiles);
+  L.combine = take(4 * (size_t)L.chunk_cap);
+  L.lin_zero_end = off;
   L.total = off;
   return L;
 }
@@ -165,6 +191,8 @@ struct LinArgs {
   uint32_t* hist;      // [4][256]
   uint32_t* counters;  // kCntInvalid
   int32_t* status;
+  void* zero;          // look-back words and combine counters, cleared here
+  int64_t zero_words4; // ... in 16-byte words
   int64_t N;
   int32_t T, B, npass;
   uint32_t sentinel;   // total_rows
@@ -180,21 +208,49 @@ __device__ __forceinline__ int32_t bag_search_global(const int64_t* offsets, int
   return lo;
 }
 
+// Largest g in [0, nb) with offsets[g] <= pos, found by one warp with a
+// 32-ary search: each round the lanes probe 32 evenly spaced bags and keep
+// the sub-range after the last probe that is <= pos (3 rounds for 16K bags).
+// Broken (non-monotone) offsets still give an index inside [0, nb).
+__device__ __forceinline__ int32_t bag_search_warp(const int64_t* offsets, int32_t nb, int64_t pos, int lane) {
+  int32_t lo = 0, hi = nb - 1;
+  while (hi > lo) {
+    const int32_t step = (hi - lo + 32) / 32;  // ceil((hi - lo + 1) / 32)
+    const int32_t cand = lo + lane * step;
+    const bool ok = cand <= hi && __ldg(offsets + cand) <= pos;
+    const unsigned m = __ballot_sync(kFull, ok);
+    if (m == 0) break;  // pos precedes every probe: lo
+    const int last = 31 - __clz(m);
+    lo = lo + last * step;
+    hi = min(hi, lo + step - 1);
+    if (step == 1) break;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a) {
   __shared__ uint32_t s_hist[4][256];
   __shared__ int64_t s_off[kLinOffs];
   __shared__ int32_t s_g0, s_ng;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int32_t nb = a.T * a.B;
   for (int k = tid; k < 4 * 256; k += kLinThreads) (&s_hist[0][0])[k] = 0;
+  // clear the look-back words and combine counters the later kernels use
+  {
+    const int64_t gtid = (int64_t)blockIdx.x * kLinThreads + tid;
+    const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
+    uint4* z = reinterpret_cast<uint4*>(a.zero);
+    for (int64_t k = gtid; k < a.zero_words4; k += gstride) z[k] = make_uint4(0, 0, 0, 0);
+  }
   const int64_t p0 = (int64_t)blockIdx.x * kLinTile;
   const int64_t p1 = min(a.N, p0 + kLinTile);
-  if (tid == 0) {
-    int32_t g0 = bag_search_global(a.offsets, 0, nb - 1, p0);
-    int32_t g1 = bag_search_global(a.offsets, g0, nb - 1, p1 - 1);
-    s_g0 = g0;
-    s_ng = g1 - g0 + 1;
+  if (tid < 64) {  // warp 0 finds the bag of p0, warp 1 the bag of p1 - 1
+    const int32_t g = bag_search_warp(a.offsets, nb, tid < 32 ? p0 : p1 - 1, lane);
+    if (tid == 0) s_g0 = g;
+    if (tid == 32) s_ng = g;
   }
+  __syncthreads();
+  if (tid == 0) s_ng = max(s_ng - s_g0 + 1, 1);
   __syncthreads();
   const int32_t g0 = s_g0, ng = s_ng;
   const bool staged = ng <= kLinOffs;
@@ -202,28 +258,37 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
   __syncthreads();
   int bad = 0, invalid = 0;
-  for (int64_t i = p0 + tid; i < p1; i += kLinThreads) {
-    int32_t g;
-    if (staged) {
-      int lo = 0, hi = ng - 1;
-      while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
-      }
-      g = g0 + lo;
-    } else {
-      g = bag_search_global(a.offsets, g0, g0 + ng - 1, i);
-    }
-    const int32_t t = g / a.B;
-    const int32_t b = g - t * a.B;
-    const int64_t id = ld_stream_i64(a.indices + i);
-    const int32_t rows = __ldg(&a.meta[t].rows);
+  for (int64_t ib = p0; ib < p1; ib += kLinThreads) {
+    const int64_t i = ib + tid;
+    const bool in = i < p1;
     uint32_t key = a.sentinel;
-    if ((uint64_t)id < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id);
-    else { bad = 1; ++invalid; }
-    a.keys[i] = key;
-    a.bag_of[i] = b;
-    for (int p = 0; p < a.npass; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xff], 1u);
+    if (in) {
+      int32_t g;
+      if (staged) {
+        int lo = 0, hi = ng - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        g = g0 + lo;
+      } else {
+        g = bag_search_global(a.offsets, g0, g0 + ng - 1, i);
+      }
+      const int32_t t = g / a.B;
+      const int32_t b = g - t * a.B;
+      const int64_t id = ld_stream_i64(a.indices + i);
+      const int32_t rows = __ldg(&a.meta[t].rows);
+      if ((uint64_t)id < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id);
+      else { bad = 1; ++invalid; }
+      a.keys[i] = key;
+      a.bag_of[i] = b;
+    }
+    // digit histograms: lanes holding the same digit add once (hot rows repeat keys)
+    for (int p = 0; p < a.npass; ++p) {
+      const uint32_t d = in ? ((key >> (8 * p)) & 0xffu) : 256u;
+      const unsigned peers = __match_any_sync(kFull, d);
+      if (in && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&s_hist[p][d], (uint32_t)__popc(peers));
+    }
   }
   // offsets must start at 0, never decrease and end at N
   const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
@@ -253,6 +318,10 @@ struct SortArgs {
   uint32_t* lookback;      // [ntiles][256]
   uint32_t* tile_counter;
   int32_t* status;
+  const int32_t* bag_of;   // last pass only: bag sample index per position
+  const float* psw;        // last pass only (may be null): weight per position
+  int32_t* bag_sorted;     // last pass only: bag sample index per sorted lookup
+  float* psw_sorted;       // last pass only: weight per sorted lookup
   int32_t N;
   int32_t shift;
 };
@@ -343,10 +412,19 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
     st_relaxed(my, kFlagInc | cnt);
   } else {
     st_relaxed(my, kFlagAgg | cnt);
-    for (int32_t pt = tile - 1; pt >= 0; --pt) {
-      const uint32_t v = wait_flag(a.lookback + (size_t)pt * 256 + tid, a.status);
-      excl += v & kValMask;
-      if (v & kFlagInc) break;
+    // walk back four tiles per round: the four words are requested together
+    bool done = false;
+    for (int32_t pt = tile - 1; pt >= 0 && !done; pt -= 4) {
+      uint32_t v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = pt - q >= 0 ? ld_relaxed(a.lookback + (size_t)(pt - q) * 256 + tid) : kFlagInc;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (done) break;
+        if (!(v[q] & (kFlagAgg | kFlagInc))) v[q] = wait_flag(a.lookback + (size_t)(pt - q) * 256 + tid, a.status);
+        excl += v[q] & kValMask;
+        if (v[q] & kFlagInc) done = true;
+      }
     }
     st_relaxed(my, kFlagInc | ((excl + cnt) & kValMask));
   }
@@ -369,8 +447,13 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
     const uint32_t k = s_keys[i];
     const int32_t dst = s_gbase[(k >> a.shift) & 0xffu] + i;
     if ((uint32_t)dst < (uint32_t)a.N) {  // always true unless a wait timed out
+      const int32_t v = s_vals[i];
       a.keys_out[dst] = k;
-      a.vals_out[dst] = s_vals[i];
+      a.vals_out[dst] = v;
+      if (a.bag_sorted) {  // carry each lookup's bag and weight through the same order
+        a.bag_sorted[dst] = __ldg(a.bag_of + v);
+        if (a.psw_sorted) a.psw_sorted[dst] = __ldg(a.psw + v);
+      }
     }
   }
 }
@@ -426,21 +509,18 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
     total += s_scan[w];
   }
   const uint32_t mine = wsum + x - nflag;
-  if (tid == 0) {
+  if (warp == 0) {
     uint32_t* my = a.lookback + tile;
     uint32_t excl = 0;
-    if (tile == 0) {
-      st_relaxed(my, kFlagInc | total);
-    } else {
-      st_relaxed(my, kFlagAgg | total);
-      for (int32_t pt = tile - 1; pt >= 0; --pt) {
-        const uint32_t v = wait_flag(a.lookback + pt, a.status);
-        excl += v & kValMask;
-        if (v & kFlagInc) break;
-      }
-      st_relaxed(my, kFlagInc | ((excl + total) & kValMask));
+    if (lane == 0) st_relaxed(my, (tile == 0 ? kFlagInc : kFlagAgg) | total);
+    if (tile > 0) {
+      excl = lookback_window(a.lookback, tile, lane, a.status);
+      if (lane == 0) st_relaxed(my, kFlagInc | ((excl + total) & kValMask));
     }
-    s_excl = excl;
+    if (lane == 0) s_excl = excl;
+  }
+  if (tid == 0) {
+    const uint32_t excl = s_excl;
     if (tile == a.ntiles - 1) {
       const uint32_t U = min(excl + total, (uint32_t)a.N);
       const uint32_t n_valid = (uint32_t)a.N - a.counters[kCntInvalid * 2];
@@ -545,9 +625,8 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
 struct RedArgs {
   const float* grad_out;
   const TableMeta* meta;
-  const float* psw;
-  const int32_t* sorted_pos;
-  const int32_t* bag_of;
+  const int32_t* bag_sorted;  // bag sample index of every sorted lookup
+  const float* psw_sorted;    // weight of every sorted lookup (null: unweighted)
   const int64_t* unique_rows;
   const int32_t* run_starts;
   const int4* long_list;
@@ -560,7 +639,7 @@ struct RedArgs {
   float* row_grads;
   int32_t* status;
   int64_t capacity;
-  int32_t T, sumD, tau, chunk, slot_floats;
+  int32_t T, B, sumD, tau, chunk, slot_floats;
 };
 
 // Where run u's row gradient goes and how wide it is.
@@ -577,7 +656,7 @@ __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
   RunInfo r;
   r.D = __ldg(&a.meta[t].D);
   r.col_off = __ldg(&a.meta[t].col_off);
-  r.weighted = (a.psw != nullptr) && __ldg(&a.meta[t].weighted);
+  r.weighted = (a.psw_sorted != nullptr) && __ldg(&a.meta[t].weighted);
   r.out_off = a.gofs[t] + (int64_t)(u - a.unique_count[t]) * r.D;
   return r;
 }
@@ -613,27 +692,36 @@ constexpr int kKB = 1;                 // chunks of 4 floats per lane -> 128 col
 constexpr int kColsPerPass = 32 * kKB * 4;
 constexpr int kRedUnroll = 8;          // grad_out slices in flight per warp
 
-// Sum of lookups [j0, j1) of one run (columns [cb, cb + kColsPerPass)).
+__device__ __forceinline__ int32_t clamp_bag(int32_t b, int32_t B) {
+  return (uint32_t)b < (uint32_t)B ? b : 0;  // defensive: b < B always holds for valid inputs
+}
+
+// Sum of sorted lookups [j0, j1) of one run (columns [cb, cb + kColsPerPass)).
+// The bags of the next 32 lookups are requested while the current 32
+// gradient slices are in flight.
 __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int32_t j1, int cb, int lane,
                             Acc<kKB>& acc) {
   const int C4 = r.D >> 2;
+  int32_t nxt_b = 0;
+  float nxt_w = 1.f;
+  if (j0 + lane < j1) {
+    nxt_b = __ldg(a.bag_sorted + j0 + lane);
+    if (r.weighted) nxt_w = __ldg(a.psw_sorted + j0 + lane);
+  }
   for (int32_t jb = j0; jb < j1; jb += 32) {
     const int n = min(32, j1 - jb);
-    int32_t my_b = 0;
-    float my_w = 1.f;
-    if (lane < n) {
-      const int32_t pos = __ldg(a.sorted_pos + jb + lane);
-      my_b = __ldg(a.bag_of + pos);
-      if (r.weighted) my_w = __ldg(a.psw + pos);
+    const int32_t my_b = clamp_bag(nxt_b, a.B);
+    const float my_w = nxt_w;
+    if (jb + 32 + lane < j1) {
+      nxt_b = __ldg(a.bag_sorted + jb + 32 + lane);
+      if (r.weighted) nxt_w = __ldg(a.psw_sorted + jb + 32 + lane);
     }
     for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
       float4 g[kRedUnroll][kKB];
-      float w[kRedUnroll];
 #pragma unroll
       for (int u = 0; u < kRedUnroll; ++u) {
         const int q = q0 + u;
         const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-        w[u] = __shfl_sync(kFull, my_w, q & 31);
         const float* row = a.grad_out + (int64_t)b * a.sumD + r.col_off;
 #pragma unroll
         for (int k = 0; k < kKB; ++k) {
@@ -642,9 +730,11 @@ __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int3
         }
       }
 #pragma unroll
-      for (int u = 0; u < kRedUnroll; ++u)
+      for (int u = 0; u < kRedUnroll; ++u) {
+        const float w = __shfl_sync(kFull, my_w, (q0 + u) & 31);
 #pragma unroll
-        for (int k = 0; k < kKB; ++k) acc.add(u & 1, k, g[u][k], w[u], r.weighted);
+        for (int k = 0; k < kKB; ++k) acc.add(u & 1, k, g[u][k], w, r.weighted);
+      }
     }
   }
 }
@@ -739,7 +829,11 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   }
 }
 
-// Batch of 32 consecutive runs; the warp reduces the short ones in run order.
+// Batch of 32 consecutive runs; the warp reduces the short ones in run order
+// as one flattened stream of lookups (the warp's lane l holds the metadata
+// of run 32*batch + l), flushing a run's row gradient when the stream moves
+// on to the next run.  Long runs of the batch are skipped (their chunks are
+// separate work items).
 __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane) {
   const int32_t u = batch * 32 + lane;
   int32_t rs = 0, len = 0;
@@ -756,46 +850,52 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
     const int32_t y = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += y;
   }
+  const int32_t excl = incl - cnt;
   const int32_t total = __shfl_sync(kFull, incl, 31);
   int maxD = r.D;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxD = max(maxD, __shfl_xor_sync(kFull, maxD, o));
+
+  // run, bag and weight of flattened lookup f = fb + lane
+  auto fetch = [&](int32_t fb, int& my_r, int32_t& my_b, float& my_w) {
+    const int32_t f = fb + lane;
+    my_r = 0;  // number of runs whose inclusive count is <= f (binary lifting)
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (__shfl_sync(kFull, incl, my_r + step - 1) <= f) my_r += step;
+    const int32_t j = __shfl_sync(kFull, rs, my_r) + (f - __shfl_sync(kFull, excl, my_r));
+    const int wt = __shfl_sync(kFull, r.weighted, my_r);
+    my_b = 0;
+    my_w = 1.f;
+    if (f < total) {
+      my_b = clamp_bag(__ldg(a.bag_sorted + j), a.B);
+      if (wt) my_w = __ldg(a.psw_sorted + j);
+    }
+  };
+
   for (int cb = 0; cb < maxD; cb += kColsPerPass) {
     Acc<kKB> acc;
     acc.zero();
     int cur = -1;  // lane (run) currently accumulated
+    int nxt_r;
+    int32_t nxt_b;
+    float nxt_w;
+    fetch(0, nxt_r, nxt_b, nxt_w);
     for (int32_t fb = 0; fb < total; fb += 32) {
       const int n = min(32, total - fb);
-      // lookup f = fb + lane belongs to the first run whose inclusive count exceeds f
-      const int32_t f = fb + lane;
-      int my_r = 0;  // number of runs whose inclusive count is <= f (binary lifting)
-#pragma unroll
-      for (int step = 16; step > 0; step >>= 1)
-        if (__shfl_sync(kFull, incl, my_r + step - 1) <= f) my_r += step;
-      int32_t my_b = 0;
-      float my_w = 1.f;
-      {
-        const int32_t r_rs = __shfl_sync(kFull, rs, my_r);
-        const int32_t r_excl = __shfl_sync(kFull, incl - cnt, my_r);
-        const int32_t r_wt = __shfl_sync(kFull, r.weighted, my_r);
-        if (lane < n) {
-          const int32_t pos = __ldg(a.sorted_pos + r_rs + (f - r_excl));
-          my_b = __ldg(a.bag_of + pos);
-          if (r_wt) my_w = __ldg(a.psw + pos);
-        }
-      }
+      const int my_r = nxt_r;
+      const int32_t my_b = nxt_b;
+      const float my_w = nxt_w;
+      if (fb + 32 < total) fetch(fb + 32, nxt_r, nxt_b, nxt_w);
       for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
         float4 g[kRedUnroll][kKB];
-        float w[kRedUnroll];
-        int rr[kRedUnroll];
 #pragma unroll
         for (int uu = 0; uu < kRedUnroll; ++uu) {
           const int q = q0 + uu;
-          rr[uu] = __shfl_sync(kFull, my_r, q & 31);
+          const int rr = __shfl_sync(kFull, my_r, q & 31);
           const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-          w[uu] = __shfl_sync(kFull, my_w, q & 31);
-          const int32_t coff = __shfl_sync(kFull, r.col_off, rr[uu]);
-          const int32_t C4 = __shfl_sync(kFull, r.D, rr[uu]) >> 2;
+          const int32_t coff = __shfl_sync(kFull, r.col_off, rr);
+          const int32_t C4 = __shfl_sync(kFull, r.D, rr) >> 2;
           const float* row = a.grad_out + (int64_t)b * a.sumD + coff;
 #pragma unroll
           for (int k = 0; k < kKB; ++k) {
@@ -807,7 +907,8 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
         for (int uu = 0; uu < kRedUnroll; ++uu) {
           const int q = q0 + uu;
           if (q >= n) break;
-          if (rr[uu] != cur) {
+          const int rr = __shfl_sync(kFull, my_r, q & 31);
+          if (rr != cur) {
             if (cur >= 0) {  // the previous run is complete
               float4 v[kKB];
 #pragma unroll
@@ -817,11 +918,12 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
               store_cols(a.row_grads, v, cb, C4c, lane, a.capacity, off);
               acc.zero();
             }
-            cur = rr[uu];
+            cur = rr;
           }
-          const int wt = __shfl_sync(kFull, r.weighted, rr[uu]);
+          const float w = __shfl_sync(kFull, my_w, q & 31);
+          const int wt = __shfl_sync(kFull, r.weighted, rr);
 #pragma unroll
-          for (int k = 0; k < kKB; ++k) acc.add(q & 1, k, g[uu][k], w[uu], wt);
+          for (int k = 0; k < kKB; ++k) acc.add(q & 1, k, g[uu][k], w, wt);
         }
       }
     }
@@ -836,7 +938,7 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
   }
 }
 
-__global__ void __launch_bounds__(kRedThreads) reduce_kernel(const RedArgs a) {
+__global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a) {
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
@@ -890,6 +992,8 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   la.hist = at<uint32_t>(ws, L.hist);
   la.counters = counters;
   la.status = a.status;
+  la.zero = at<char>(ws, L.lin_zero_begin);
+  la.zero_words4 = (int64_t)((L.lin_zero_end - L.lin_zero_begin) / 16);
   la.N = N;
   la.T = a.T;
   la.B = a.B;
@@ -919,6 +1023,10 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     sa.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * 256;
     sa.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
     sa.status = a.status;
+    sa.bag_of = at<int32_t>(ws, L.bag_of);
+    sa.psw = a.psw;
+    sa.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
+    sa.psw_sorted = (last && a.psw) ? at<float>(ws, L.psw_sorted) : nullptr;
     sa.N = (int32_t)N;
     sa.shift = 8 * pass;
     sort_pass_kernel<<<L.sort_ntiles, kSortThreads, 0, s>>>(sa);
@@ -969,9 +1077,8 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   RedArgs rd;
   rd.grad_out = a.grad_out;
   rd.meta = a.meta;
-  rd.psw = a.psw;
-  rd.sorted_pos = final_pos;
-  rd.bag_of = at<int32_t>(ws, L.bag_of);
+  rd.bag_sorted = at<int32_t>(ws, L.bag_sorted);
+  rd.psw_sorted = a.psw ? at<float>(ws, L.psw_sorted) : nullptr;
   rd.unique_rows = a.unique_rows;
   rd.run_starts = run_starts;
   rd.long_list = at<int4>(ws, L.long_list);
@@ -985,6 +1092,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.status = a.status;
   rd.capacity = a.row_grads_capacity;
   rd.T = a.T;
+  rd.B = a.B;
   rd.sumD = a.sumD;
   rd.tau = tu.long_run_threshold;
   rd.chunk = tu.long_chunk;
