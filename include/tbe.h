@@ -188,6 +188,32 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
                  void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * Backward without a caller-provided workspace (the page has no counterpart;
+ * this is an entry point for callers that cannot allocate device memory,
+ * such as a plugin that an engine hands only a stream and its tensors, or
+ * code running while a global-mode stream capture forbids cudaMalloc).
+ * Same arguments and results as tbe_backward, minus the workspace: the
+ * scratch space is one array of TBE_STATIC_WORKSPACE_BYTES compiled into the
+ * library, held on every GPU that loads it until the process exits.
+ *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ *     call); inputs and outputs are still the caller's.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Batches whose scratch exceeds TBE_STATIC_WORKSPACE_BYTES (check with
+ *     tbe_backward_workspace_bytes) are refused with TBE_ERR_WORKSPACE.
+ *   - Every call on a device shares the array; calls whose work overlaps on
+ *     the GPU (other streams, concurrent graph replays) race and must be
+ *     serialised by the caller.
+ */
+#define TBE_STATIC_WORKSPACE_BYTES (32u << 20)
+int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, const int64_t* indices,
+                                  int64_t N, const int64_t* offsets, int32_t B,
+                                  const float* per_sample_weights, int64_t* unique_rows,
+                                  int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
+                                  int64_t row_grads_capacity, int64_t* unique_count,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * Tuning knobs (process-wide; set them before launching work that should
  * use them, not concurrently with launches).
  *   long_run_threshold : runs with at least this many lookups take the

@@ -29,7 +29,9 @@ EXPORTED = [
     "tbe_plan_device_bytes", "tbe_plan_create", "tbe_plan_destroy", "tbe_forward", "tbe_forward_path",
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
+    "tbe_backward_static_workspace",
 ]
+TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
 
 class TBEError(RuntimeError):
@@ -79,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_backward_workspace_bytes.argtypes = [P, i32, i64]
     lib.tbe_backward.restype = ctypes.c_int
     lib.tbe_backward.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, sz, P, P]
+    lib.tbe_backward_static_workspace.restype = ctypes.c_int
+    lib.tbe_backward_static_workspace.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, P]
     lib.tbe_get_tuning.restype = ctypes.c_int
     lib.tbe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
     lib.tbe_set_tuning.restype = ctypes.c_int
@@ -237,6 +241,24 @@ def tbe_backward(plan: Plan, grad_out, indices, offsets, B: int, per_sample_weig
                           _ptr(bufs.row_grads), bufs.row_grads_capacity, _ptr(bufs.unique_count),
                           _ptr(bufs.workspace), bufs.workspace.numel(), _ptr(dev_status), _stream(stream))
     _check(rc, "tbe_backward")
+    return bufs
+
+
+def tbe_backward_static_workspace(plan: Plan, grad_out, indices, offsets, B: int, per_sample_weights=None,
+                                  bufs=None, dev_status=None, stream=None):
+    """Row gradients using the library's built-in scratch array instead of a
+    workspace (for callers that cannot allocate device memory).  ``bufs``
+    supplies the outputs; its workspace is not used."""
+    lib = load_library()
+    N = int(indices.numel())
+    if bufs is None:
+        bufs = BackwardBuffers(plan, B, N, device=indices.device)
+    rc = lib.tbe_backward_static_workspace(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
+                                           _ptr(per_sample_weights), _ptr(bufs.unique_rows), _ptr(bufs.run_starts),
+                                           _ptr(bufs.sorted_positions), _ptr(bufs.row_grads),
+                                           bufs.row_grads_capacity, _ptr(bufs.unique_count), _ptr(dev_status),
+                                           _stream(stream))
+    _check(rc, "tbe_backward_static_workspace")
     return bufs
 
 
