@@ -57,6 +57,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--B", type=int, default=None, help="batch size override (profiling of smaller cases)")
+    ap.add_argument("--only", choices=["both", "fwd", "bwd"], default="both")
+    ap.add_argument("--path", choices=["auto", "gather", "histogram"], default="auto")
+    ap.add_argument("--profile", action="store_true",
+                    help="plain launch loop for a profiler: --warmup then --steps eager steps, one JSON line")
     return ap.parse_args()
 
 
@@ -209,6 +214,39 @@ def traffic_from_profiles(kernel):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+
+def run_profile(args):
+    """Eager steps of one workload for a profiler (no graphs, no timing hygiene)."""
+    import torch
+
+    import table_embedding_bags_gb300 as tbe
+    from tbe_inputs import make_config, materialize_weights
+
+    tbe.load_library()
+    p = make_config(args.workload, B=args.B, with_grad=args.only != "fwd")
+    plan = tbe.Plan.from_problem(p)
+    ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
+    psw = None if p.per_sample_weights is None else torch.from_numpy(p.per_sample_weights).cuda()
+    path = {"auto": tbe.TBE_PATH_AUTO, "gather": tbe.TBE_PATH_GATHER, "histogram": tbe.TBE_PATH_HISTOGRAM}[args.path]
+    w = materialize_weights(p, device="cuda") if args.only != "bwd" else None
+    G = torch.from_numpy(p.grad_out).cuda() if args.only != "fwd" else None
+    bufs = tbe.BackwardBuffers(plan, p.B, p.N) if args.only != "fwd" else None
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = None
+    for k in range(args.warmup + args.steps):
+        if k == args.warmup:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        if args.only != "bwd":
+            tbe.tbe_forward(plan, w, ind, off, p.B, psw, dev_status=status, path=path)
+        if args.only != "fwd":
+            tbe.tbe_backward(plan, G, ind, off, p.B, psw, bufs=bufs, dev_status=status,
+                             want_run_starts=False, want_sorted_positions=False)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    return dict(profile=True, workload=args.workload, B=p.B, N=p.N, only=args.only, path=args.path,
+                steps=args.steps, wall_ms_per_step=1e3 * (time.perf_counter() - t0) / max(args.steps, 1))
+
 
 def run_ours(args, world, rank, local):
     import torch
@@ -479,6 +517,9 @@ def main():
         return
     import torch
 
+    if args.profile:
+        print(json.dumps(run_profile(args)), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
 

@@ -463,6 +463,9 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
 // ---------------------------------------------------------------------------
 struct RleArgs {
   const uint32_t* keys;  // sorted
+  const TableMeta* meta;
+  int64_t* unique_count; // [T+1] per-table prefix of the unique rows
+  int32_t T;
   int64_t* unique_rows;
   int32_t* run_starts;
   uint32_t* lookback;
@@ -530,13 +533,32 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   }
   __syncthreads();
   uint32_t u = s_excl + mine;
+  // per-table counts: unique_count[t] = number of unique rows below
+  // table_row_base[t].  A run start whose previous key lies in an earlier
+  // table writes the count for every table boundary in between; the last
+  // valid key writes U for the tables after it.
+  int64_t prevk = (j0 > 0 && j0 - 1 < a.N) ? (int64_t)__ldg(a.keys + j0 - 1) : -1;
+  if (prevk >= (int64_t)a.sentinel) prevk = -1;
+  const uint32_t knext = (j0 + kRleIPT < a.N) ? __ldg(a.keys + j0 + kRleIPT) : a.sentinel;
+  if (j0 == 0 && (a.N == 0 || k[0] >= a.sentinel))  // no valid lookup at all
+    for (int t = 0; t <= a.T; ++t) a.unique_count[t] = 0;
 #pragma unroll
   for (int q = 0; q < kRleIPT; ++q) {
+    const int32_t j = j0 + q;
     if ((flags & (1u << q)) && u < (uint32_t)a.N) {  // u < N unless a wait timed out
       a.unique_rows[u] = (int64_t)k[q];
-      a.run_starts[u] = j0 + q;
+      a.run_starts[u] = j;
+      const int tk = table_of_row(a.meta, a.T, (int64_t)k[q]);
+      const int tp = prevk < 0 ? -1 : table_of_row(a.meta, a.T, prevk);
+      for (int t = tp + 1; t <= tk; ++t) a.unique_count[t] = u;
       ++u;
     }
+    const uint32_t nk = q + 1 < kRleIPT ? k[q + 1] : knext;
+    if (j < a.N && k[q] < a.sentinel && (j == a.N - 1 || nk >= a.sentinel)) {  // last valid key
+      const int tk = table_of_row(a.meta, a.T, (int64_t)k[q]);
+      for (int t = tk + 1; t <= a.T; ++t) a.unique_count[t] = min(u, (uint32_t)a.N);
+    }
+    if (j < a.N && k[q] < a.sentinel) prevk = (int64_t)k[q];
   }
 }
 
@@ -550,7 +572,7 @@ struct ClsArgs {
   int4* long_list;          // {u, first chunk, chunks, length}
   unsigned long long* long_counter;  // (runs << 32) | chunks
   const uint32_t* counters;
-  int64_t* unique_count;    // [T+1]
+  const int64_t* unique_count;  // [T+1], written by the segmentation kernel
   int64_t* gofs;            // [T+1] float offset of each table's block
   int32_t* status;
   int64_t capacity;
@@ -565,26 +587,37 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   if (blockIdx.x == 0) {
-    // unique_count[t] = number of unique rows below table_row_base[t]
-    for (int t = tid; t <= a.T; t += kClsThreads) {
-      const int64_t base = __ldg(&a.meta[t].row_base);
-      int lo = 0, hi = U;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a.unique_rows[mid] < base) lo = mid + 1; else hi = mid;
+    // float offset of each table's block of row gradients:
+    // gofs[t] = sum_{t' < t} (unique rows of t') * D_t'
+    const int per = (a.T + kClsThreads - 1) / kClsThreads;
+    int64_t mine = 0;
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) mine += (a.unique_count[t + 1] - a.unique_count[t]) * (int64_t)__ldg(&a.meta[t].D);
+    }
+    __shared__ int64_t s_part[kClsThreads / 32];
+    int64_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    int64_t run = x - mine;
+    for (int w = 0; w < warp; ++w) run += s_part[w];
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) {
+        a.gofs[t] = run;
+        run += (a.unique_count[t + 1] - a.unique_count[t]) * (int64_t)__ldg(&a.meta[t].D);
       }
-      a.unique_count[t] = lo;
+    }
+    if (tid == kClsThreads - 1) {
+      a.gofs[a.T] = run;
+      if (run > a.capacity) report(a.status, TBE_DEV_CAPACITY);
     }
     __syncthreads();
-    if (tid == 0) {
-      int64_t acc = 0;
-      for (int t = 0; t < a.T; ++t) {
-        a.gofs[t] = acc;
-        acc += (a.unique_count[t + 1] - a.unique_count[t]) * (int64_t)__ldg(&a.meta[t].D);
-      }
-      a.gofs[a.T] = acc;
-      if (acc > a.capacity) report(a.status, TBE_DEV_CAPACITY);
-    }
   }
   const int32_t stride = gridDim.x * kClsThreads;
   for (int32_t u0 = blockIdx.x * kClsThreads; u0 < U; u0 += stride) {
@@ -1040,6 +1073,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   int32_t* run_starts = a.run_starts ? a.run_starts : at<int32_t>(ws, L.run_starts);
   RleArgs ra;
   ra.keys = sorted_keys;
+  ra.meta = a.meta;
+  ra.unique_count = a.unique_count;
+  ra.T = a.T;
   ra.unique_rows = a.unique_rows;
   ra.run_starts = run_starts;
   ra.lookback = at<uint32_t>(ws, L.rle_lookback);
