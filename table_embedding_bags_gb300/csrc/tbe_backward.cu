@@ -258,37 +258,37 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
   __syncthreads();
   int bad = 0, invalid = 0;
-  for (int64_t ib = p0; ib < p1; ib += kLinThreads) {
-    const int64_t i = ib + tid;
-    const bool in = i < p1;
-    uint32_t key = a.sentinel;
-    if (in) {
-      int32_t g;
-      if (staged) {
-        int lo = 0, hi = ng - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
-        }
-        g = g0 + lo;
-      } else {
-        g = bag_search_global(a.offsets, g0, g0 + ng - 1, i);
+  constexpr int kIPT = kLinTile / kLinThreads;
+  int64_t id[kIPT];
+#pragma unroll
+  for (int q = 0; q < kIPT; ++q) {  // all of this thread's ids are requested first
+    const int64_t i = p0 + q * kLinThreads + tid;
+    id[q] = i < p1 ? ld_stream_i64(a.indices + i) : 0;
+  }
+#pragma unroll
+  for (int q = 0; q < kIPT; ++q) {
+    const int64_t i = p0 + q * kLinThreads + tid;
+    if (i >= p1) break;
+    int32_t g;
+    if (staged) {
+      int lo = 0, hi = ng - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] <= i) lo = mid; else hi = mid - 1;
       }
-      const int32_t t = g / a.B;
-      const int32_t b = g - t * a.B;
-      const int64_t id = ld_stream_i64(a.indices + i);
-      const int32_t rows = __ldg(&a.meta[t].rows);
-      if ((uint64_t)id < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id);
-      else { bad = 1; ++invalid; }
-      a.keys[i] = key;
-      a.bag_of[i] = b;
+      g = g0 + lo;
+    } else {
+      g = bag_search_global(a.offsets, g0, g0 + ng - 1, i);
     }
-    // digit histograms: lanes holding the same digit add once (hot rows repeat keys)
-    for (int p = 0; p < a.npass; ++p) {
-      const uint32_t d = in ? ((key >> (8 * p)) & 0xffu) : 256u;
-      const unsigned peers = __match_any_sync(kFull, d);
-      if (in && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&s_hist[p][d], (uint32_t)__popc(peers));
-    }
+    const int32_t t = g / a.B;
+    const int32_t b = g - t * a.B;
+    const int32_t rows = __ldg(&a.meta[t].rows);
+    uint32_t key = a.sentinel;
+    if ((uint64_t)id[q] < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id[q]);
+    else { bad = 1; ++invalid; }
+    a.keys[i] = key;
+    a.bag_of[i] = b;
+    for (int p = 0; p < a.npass; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xffu], 1u);
   }
   // offsets must start at 0, never decrease and end at N
   const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
@@ -694,26 +694,25 @@ __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
   return r;
 }
 
-// Accumulator of one lane: KB chunks of 4 floats, two interleaved sets.
-template <int KB>
+// Accumulator of one lane: one float4 column chunk, two interleaved sets
+// (successive lookups alternate between them, halving the serial depth).
 struct Acc {
-  float v[2][KB][4];
+  float4 v[2];
   __device__ __forceinline__ void zero() {
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-#pragma unroll
-      for (int k = 0; k < KB; ++k)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) v[s][k][e] = 0.f;
+    v[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    v[1] = v[0];
   }
-  __device__ __forceinline__ void add(int s, int k, const float4& g, float w, bool weighted) {
-    const float f[4] = {g.x, g.y, g.z, g.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) v[s][k][e] = __fadd_rn(v[s][k][e], weighted ? __fmul_rn(w, f[e]) : f[e]);
+  template <bool W>
+  __device__ __forceinline__ void add(int s, const float4& g, float w) {
+    // weighted: the product is rounded to fp32, then added (w = 1 is exact)
+    v[s].x = __fadd_rn(v[s].x, W ? __fmul_rn(w, g.x) : g.x);
+    v[s].y = __fadd_rn(v[s].y, W ? __fmul_rn(w, g.y) : g.y);
+    v[s].z = __fadd_rn(v[s].z, W ? __fmul_rn(w, g.z) : g.z);
+    v[s].w = __fadd_rn(v[s].w, W ? __fmul_rn(w, g.w) : g.w);
   }
-  __device__ __forceinline__ float4 sum(int k) const {
-    return make_float4(__fadd_rn(v[0][k][0], v[1][k][0]), __fadd_rn(v[0][k][1], v[1][k][1]),
-                       __fadd_rn(v[0][k][2], v[1][k][2]), __fadd_rn(v[0][k][3], v[1][k][3]));
+  __device__ __forceinline__ float4 sum() const {
+    return make_float4(__fadd_rn(v[0].x, v[1].x), __fadd_rn(v[0].y, v[1].y), __fadd_rn(v[0].z, v[1].z),
+                       __fadd_rn(v[0].w, v[1].w));
   }
 };
 
@@ -721,64 +720,72 @@ __device__ __forceinline__ float4 ld_grad(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
 }
 
-constexpr int kKB = 1;                 // chunks of 4 floats per lane -> 128 columns per pass
-constexpr int kColsPerPass = 32 * kKB * 4;
+constexpr int kColsPerPass = 128;      // 32 lanes x one float4
 constexpr int kRedUnroll = 8;          // grad_out slices in flight per warp
 
 __device__ __forceinline__ int32_t clamp_bag(int32_t b, int32_t B) {
   return (uint32_t)b < (uint32_t)B ? b : 0;  // defensive: b < B always holds for valid inputs
 }
 
-// Sum of sorted lookups [j0, j1) of one run (columns [cb, cb + kColsPerPass)).
-// The bags of the next 32 lookups are requested while the current 32
-// gradient slices are in flight.
-__device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int32_t j1, int cb, int lane,
-                            Acc<kKB>& acc) {
-  const int C4 = r.D >> 2;
-  int32_t nxt_b = 0;
-  float nxt_w = 1.f;
-  if (j0 + lane < j1) {
-    nxt_b = __ldg(a.bag_sorted + j0 + lane);
-    if (r.weighted) nxt_w = __ldg(a.psw_sorted + j0 + lane);
-  }
-  for (int32_t jb = j0; jb < j1; jb += 32) {
-    const int n = min(32, j1 - jb);
-    const int32_t my_b = clamp_bag(nxt_b, a.B);
-    const float my_w = nxt_w;
-    if (jb + 32 + lane < j1) {
-      nxt_b = __ldg(a.bag_sorted + jb + 32 + lane);
-      if (r.weighted) nxt_w = __ldg(a.psw_sorted + jb + 32 + lane);
-    }
-    for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
-      float4 g[kRedUnroll][kKB];
-#pragma unroll
-      for (int u = 0; u < kRedUnroll; ++u) {
-        const int q = q0 + u;
-        const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-        const float* row = a.grad_out + (int64_t)b * a.sumD + r.col_off;
-#pragma unroll
-        for (int k = 0; k < kKB; ++k) {
-          const int c = (cb >> 2) + lane + 32 * k;
-          g[u][k] = (q < n && c < C4) ? ld_grad(row + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kRedUnroll; ++u) {
-        const float w = __shfl_sync(kFull, my_w, (q0 + u) & 31);
-#pragma unroll
-        for (int k = 0; k < kKB; ++k) acc.add(u & 1, k, g[u][k], w, r.weighted);
-      }
-    }
+__device__ __forceinline__ void store_col(float* dst, const float4& v, int c, int C4, int64_t limit_floats,
+                                          int64_t dst_off) {
+  if (c < C4 && dst_off + 4 * c + 4 <= limit_floats) *reinterpret_cast<float4*>(dst + dst_off + 4 * c) = v;
+}
+
+// Bag and weight of sorted lookup j (lanes past the end get bag 0, weight 1).
+// `weighted`: the lookup's table uses per-sample weights (otherwise w = 1).
+template <bool W>
+__device__ __forceinline__ void fetch_lookup(const RedArgs& a, int32_t j, bool ok, bool weighted, int32_t& b,
+                                             float& w) {
+  b = 0;
+  w = 1.f;
+  if (ok) {
+    b = clamp_bag(__ldg(a.bag_sorted + j), a.B);
+    if (W && weighted) w = __ldg(a.psw_sorted + j);
   }
 }
 
-__device__ __forceinline__ void store_cols(float* dst, const float4* v, int cb, int C4, int lane,
-                                           int64_t limit_floats, int64_t dst_off) {
+// Sum of sorted lookups [j0, j1) of one run (columns [cb, cb + 128)).  The
+// bags of the next 32 lookups are requested while the current 32 gradient
+// slices are in flight.
+template <bool W>
+__device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int32_t j1, int cb, int lane,
+                            Acc& acc) {
+  const int C4 = r.D >> 2;
+  const int c = (cb >> 2) + lane;
+  const bool full_cols = C4 - (cb >> 2) >= 32;  // uniform: every lane owns a column chunk
+  const float* gcol = a.grad_out + r.col_off + 4 * c;
+  int32_t nxt_b;
+  float nxt_w;
+  fetch_lookup<W>(a, j0 + lane, j0 + lane < j1, r.weighted, nxt_b, nxt_w);
+  for (int32_t jb = j0; jb < j1; jb += 32) {
+    const int n = min(32, j1 - jb);
+    const int32_t my_b = nxt_b;
+    const float my_w = nxt_w;
+    fetch_lookup<W>(a, jb + 32 + lane, jb + 32 + lane < j1, r.weighted, nxt_b, nxt_w);
+    if (n == 32 && full_cols) {  // full group: no predicates
 #pragma unroll
-  for (int k = 0; k < kKB; ++k) {
-    const int c = (cb >> 2) + lane + 32 * k;
-    if (c < C4 && dst_off + 4 * c + 4 <= limit_floats)
-      *reinterpret_cast<float4*>(dst + dst_off + 4 * c) = v[k];
+      for (int q0 = 0; q0 < 32; q0 += kRedUnroll) {
+        float4 g[kRedUnroll];
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u)
+          g[u] = ld_grad(gcol + (int64_t)__shfl_sync(kFull, my_b, q0 + u) * a.sumD);
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) acc.add<W>(u & 1, g[u], W ? __shfl_sync(kFull, my_w, q0 + u) : 1.f);
+      }
+    } else {
+      for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
+        float4 g[kRedUnroll];
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) {
+          const int q = q0 + u;
+          const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+          g[u] = (q < n && c < C4) ? ld_grad(gcol + (int64_t)b * a.sumD) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) acc.add<W>(u & 1, g[u], W ? __shfl_sync(kFull, my_w, (q0 + u) & 31) : 1.f);
+      }
+    }
   }
 }
 
@@ -788,6 +795,7 @@ __device__ __forceinline__ void store_cols(float* dst, const float4* v, int cb, 
 // children-1 after a device-scope fence) sums the children in index order
 // and writes the node's slot, or the row gradient at the root.  The order of
 // every sum is fixed, so the result does not depend on arrival order.
+template <bool W>
 __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   const unsigned long long lc = *a.long_counter;
   const int32_t n_long = (int32_t)(lc >> 32);
@@ -805,16 +813,15 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   const int32_t j0 = rs + k * a.chunk, j1 = min(rs + len, j0 + a.chunk);
   const int C4 = r.D >> 2;
   for (int cb = 0; cb < r.D; cb += kColsPerPass) {
-    Acc<kKB> acc;
+    Acc acc;
     acc.zero();
-    sum_lookups(a, r, j0, j1, cb, lane, acc);
-    float4 v[kKB];
-#pragma unroll
-    for (int q = 0; q < kKB; ++q) v[q] = acc.sum(q);
+    sum_lookups<W>(a, r, j0, j1, cb, lane, acc);
+    const float4 v = acc.sum();
+    const int c = (cb >> 2) + lane;
     if (nch == 1)
-      store_cols(a.row_grads, v, cb, C4, lane, a.capacity, r.out_off);
+      store_col(a.row_grads, v, c, C4, a.capacity, r.out_off);
     else
-      store_cols(a.partials + (int64_t)(e0 + k) * a.slot_floats, v, cb, C4, lane, (int64_t)1 << 62, 0);
+      store_col(a.partials + (int64_t)(e0 + k) * a.slot_floats, v, c, C4, (int64_t)1 << 62, 0);
   }
   if (nch == 1) return;
   int32_t node = k, span = 1, nodes = nch, cbase = e0;
@@ -831,28 +838,22 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
     __threadfence();
     const int32_t pspan = span * kFanIn;
     for (int cb = 0; cb < r.D; cb += kColsPerPass) {
-      float4 s[kKB];
-#pragma unroll
-      for (int q = 0; q < kKB; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int ch = 0; ch < nchild; ++ch) {
-        const float* cs = a.partials + (int64_t)(e0 + (parent * kFanIn + ch) * span) * a.slot_floats;
-#pragma unroll
-        for (int q = 0; q < kKB; ++q) {
-          const int c = (cb >> 2) + lane + 32 * q;
-          if (c < C4) {
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(cs + 4 * c));
-            s[q].x = __fadd_rn(s[q].x, x.x);
-            s[q].y = __fadd_rn(s[q].y, x.y);
-            s[q].z = __fadd_rn(s[q].z, x.z);
-            s[q].w = __fadd_rn(s[q].w, x.w);
-          }
+      const int c = (cb >> 2) + lane;
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < C4) {
+        for (int ch = 0; ch < nchild; ++ch) {
+          const float* cs = a.partials + (int64_t)(e0 + (parent * kFanIn + ch) * span) * a.slot_floats;
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(cs + 4 * c));
+          s.x = __fadd_rn(s.x, x.x);
+          s.y = __fadd_rn(s.y, x.y);
+          s.z = __fadd_rn(s.z, x.z);
+          s.w = __fadd_rn(s.w, x.w);
         }
       }
       if (pnodes == 1)
-        store_cols(a.row_grads, s, cb, C4, lane, a.capacity, r.out_off);
+        store_col(a.row_grads, s, c, C4, a.capacity, r.out_off);
       else
-        store_cols(a.partials + (int64_t)(e0 + parent * pspan) * a.slot_floats, s, cb, C4, lane,
-                   (int64_t)1 << 62, 0);
+        store_col(a.partials + (int64_t)(e0 + parent * pspan) * a.slot_floats, s, c, C4, (int64_t)1 << 62, 0);
     }
     if (pnodes == 1) return;  // root written: the row gradient is complete
     span = pspan;
@@ -863,10 +864,10 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
 }
 
 // Batch of 32 consecutive runs; the warp reduces the short ones in run order
-// as one flattened stream of lookups (the warp's lane l holds the metadata
-// of run 32*batch + l), flushing a run's row gradient when the stream moves
-// on to the next run.  Long runs of the batch are skipped (their chunks are
-// separate work items).
+// as one flattened stream of lookups (lane l holds the metadata of run
+// 32*batch + l) and stores a run's row gradient at its last lookup.  Long
+// runs of the batch are skipped (their chunks are separate work items).
+template <bool W>
 __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane) {
   const int32_t u = batch * 32 + lane;
   int32_t rs = 0, len = 0;
@@ -885,92 +886,97 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
   }
   const int32_t excl = incl - cnt;
   const int32_t total = __shfl_sync(kFull, incl, 31);
-  int maxD = r.D;
+  if (total == 0) return;
+  // do all short runs of the batch belong to one table?  (then every lookup
+  // shares the column offset and width)
+  const unsigned act = __ballot_sync(kFull, cnt > 0);
+  const int first = __ffs(act) - 1;
+  const int32_t coff0 = __shfl_sync(kFull, r.col_off, first);
+  const int32_t D0 = __shfl_sync(kFull, r.D, first);
+  const bool one_table = __all_sync(kFull, cnt == 0 || (r.col_off == coff0 && r.D == D0));
+  int maxD = cnt > 0 ? r.D : 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxD = max(maxD, __shfl_xor_sync(kFull, maxD, o));
 
-  // run, bag and weight of flattened lookup f = fb + lane
-  auto fetch = [&](int32_t fb, int& my_r, int32_t& my_b, float& my_w) {
-    const int32_t f = fb + lane;
-    my_r = 0;  // number of runs whose inclusive count is <= f (binary lifting)
-#pragma unroll
-    for (int step = 16; step > 0; step >>= 1)
-      if (__shfl_sync(kFull, incl, my_r + step - 1) <= f) my_r += step;
-    const int32_t j = __shfl_sync(kFull, rs, my_r) + (f - __shfl_sync(kFull, excl, my_r));
-    const int wt = __shfl_sync(kFull, r.weighted, my_r);
-    my_b = 0;
-    my_w = 1.f;
-    if (f < total) {
-      my_b = clamp_bag(__ldg(a.bag_sorted + j), a.B);
-      if (wt) my_w = __ldg(a.psw_sorted + j);
-    }
-  };
-
   for (int cb = 0; cb < maxD; cb += kColsPerPass) {
-    Acc<kKB> acc;
+    const int c = (cb >> 2) + lane;
+    Acc acc;
     acc.zero();
-    int cur = -1;  // lane (run) currently accumulated
+    // run, bag and weight of flattened lookup f = fb + lane, and whether it
+    // is the last lookup of its run
+    auto fetch = [&](int32_t fb, int& my_r, int32_t& my_b, float& my_w, bool& my_end) {
+      const int32_t f = fb + lane;
+      my_r = 0;  // number of runs whose inclusive count is <= f (binary lifting)
+#pragma unroll
+      for (int step = 16; step > 0; step >>= 1)
+        if (__shfl_sync(kFull, incl, my_r + step - 1) <= f) my_r += step;
+      my_r = min(my_r, 31);
+      const int32_t j = __shfl_sync(kFull, rs, my_r) + (f - __shfl_sync(kFull, excl, my_r));
+      const int32_t r_incl = __shfl_sync(kFull, incl, my_r);  // every lane takes part in the shuffle
+      my_end = (f < total) && (f == r_incl - 1);
+      const bool wt = __shfl_sync(kFull, r.weighted, my_r) != 0;
+      fetch_lookup<W>(a, j, f < total, wt, my_b, my_w);
+    };
     int nxt_r;
     int32_t nxt_b;
     float nxt_w;
-    fetch(0, nxt_r, nxt_b, nxt_w);
+    bool nxt_end;
+    fetch(0, nxt_r, nxt_b, nxt_w, nxt_end);
     for (int32_t fb = 0; fb < total; fb += 32) {
       const int n = min(32, total - fb);
       const int my_r = nxt_r;
       const int32_t my_b = nxt_b;
       const float my_w = nxt_w;
-      if (fb + 32 < total) fetch(fb + 32, nxt_r, nxt_b, nxt_w);
-      for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
-        float4 g[kRedUnroll][kKB];
+      const unsigned ends = __ballot_sync(kFull, nxt_end);
+      if (fb + 32 < total) fetch(fb + 32, nxt_r, nxt_b, nxt_w, nxt_end);
+      auto flush = [&](int q) {  // lookup q ends its run: store the run's row gradient
+        const int rr = __shfl_sync(kFull, my_r, q);
+        const int64_t off = __shfl_sync(kFull, r.out_off, rr);
+        const int C4r = __shfl_sync(kFull, r.D, rr) >> 2;
+        store_col(a.row_grads, acc.sum(), c, C4r, a.capacity, off);
+        acc.zero();
+      };
+      if (one_table && n == 32 && (D0 >> 2) - (cb >> 2) >= 32) {  // fast path
+        const float* gcol = a.grad_out + coff0 + 4 * c;
 #pragma unroll
-        for (int uu = 0; uu < kRedUnroll; ++uu) {
-          const int q = q0 + uu;
-          const int rr = __shfl_sync(kFull, my_r, q & 31);
-          const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-          const int32_t coff = __shfl_sync(kFull, r.col_off, rr);
-          const int32_t C4 = __shfl_sync(kFull, r.D, rr) >> 2;
-          const float* row = a.grad_out + (int64_t)b * a.sumD + coff;
+        for (int q0 = 0; q0 < 32; q0 += kRedUnroll) {
+          float4 g[kRedUnroll];
 #pragma unroll
-          for (int k = 0; k < kKB; ++k) {
-            const int c = (cb >> 2) + lane + 32 * k;
-            g[uu][k] = (q < n && c < C4) ? ld_grad(row + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int uu = 0; uu < kRedUnroll; ++uu)
+            g[uu] = ld_grad(gcol + (int64_t)__shfl_sync(kFull, my_b, q0 + uu) * a.sumD);
+#pragma unroll
+          for (int uu = 0; uu < kRedUnroll; ++uu) {
+            acc.add<W>(uu & 1, g[uu], W ? __shfl_sync(kFull, my_w, q0 + uu) : 1.f);
+            if ((ends >> (q0 + uu)) & 1u) flush(q0 + uu);
           }
         }
+      } else {
+        for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
+          float4 g[kRedUnroll];
 #pragma unroll
-        for (int uu = 0; uu < kRedUnroll; ++uu) {
-          const int q = q0 + uu;
-          if (q >= n) break;
-          const int rr = __shfl_sync(kFull, my_r, q & 31);
-          if (rr != cur) {
-            if (cur >= 0) {  // the previous run is complete
-              float4 v[kKB];
-#pragma unroll
-              for (int k = 0; k < kKB; ++k) v[k] = acc.sum(k);
-              const int64_t off = __shfl_sync(kFull, r.out_off, cur);
-              const int C4c = __shfl_sync(kFull, r.D, cur) >> 2;
-              store_cols(a.row_grads, v, cb, C4c, lane, a.capacity, off);
-              acc.zero();
-            }
-            cur = rr;
+          for (int uu = 0; uu < kRedUnroll; ++uu) {
+            const int q = q0 + uu;
+            const int rr = __shfl_sync(kFull, my_r, q & 31);
+            const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+            const int32_t coff = __shfl_sync(kFull, r.col_off, rr);
+            const int32_t C4 = __shfl_sync(kFull, r.D, rr) >> 2;
+            g[uu] = (q < n && c < C4) ? ld_grad(a.grad_out + (int64_t)b * a.sumD + coff + 4 * c)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          const float w = __shfl_sync(kFull, my_w, q & 31);
-          const int wt = __shfl_sync(kFull, r.weighted, rr);
 #pragma unroll
-          for (int k = 0; k < kKB; ++k) acc.add(q & 1, k, g[uu][k], w, wt);
+          for (int uu = 0; uu < kRedUnroll; ++uu) {
+            const int q = q0 + uu;
+            if (q >= n) break;
+            acc.add<W>(q & 1, g[uu], W ? __shfl_sync(kFull, my_w, q & 31) : 1.f);
+            if ((ends >> q) & 1u) flush(q);
+          }
         }
       }
-    }
-    if (cur >= 0) {
-      float4 v[kKB];
-#pragma unroll
-      for (int k = 0; k < kKB; ++k) v[k] = acc.sum(k);
-      const int64_t off = __shfl_sync(kFull, r.out_off, cur);
-      const int C4c = __shfl_sync(kFull, r.D, cur) >> 2;
-      store_cols(a.row_grads, v, cb, C4c, lane, a.capacity, off);
     }
   }
 }
 
+template <bool W>
 __global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a) {
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
@@ -981,8 +987,8 @@ __global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a)
     if (lane == 0) item = atomicAdd(&a.counters[kCntWork * 2], 1u);
     item = __shfl_sync(kFull, item, 0);
     if ((int32_t)item >= n_items) break;
-    if ((int32_t)item < n_chunks) long_chunk(a, (int32_t)item, lane);
-    else short_batch(a, (int32_t)item - n_chunks, U, lane);
+    if ((int32_t)item < n_chunks) long_chunk<W>(a, (int32_t)item, lane);
+    else short_batch<W>(a, (int32_t)item - n_chunks, U, lane);
   }
 }
 
@@ -1059,7 +1065,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     sa.bag_of = at<int32_t>(ws, L.bag_of);
     sa.psw = a.psw;
     sa.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
-    sa.psw_sorted = (last && a.psw) ? at<float>(ws, L.psw_sorted) : nullptr;
+    sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
     sa.N = (int32_t)N;
     sa.shift = 8 * pass;
     sort_pass_kernel<<<L.sort_ntiles, kSortThreads, 0, s>>>(sa);
@@ -1114,7 +1120,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.grad_out = a.grad_out;
   rd.meta = a.meta;
   rd.bag_sorted = at<int32_t>(ws, L.bag_sorted);
-  rd.psw_sorted = a.psw ? at<float>(ws, L.psw_sorted) : nullptr;
+  rd.psw_sorted = (a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
   rd.unique_rows = a.unique_rows;
   rd.run_starts = run_starts;
   rd.long_list = at<int4>(ws, L.long_list);
@@ -1133,14 +1139,20 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.tau = tu.long_run_threshold;
   rd.chunk = tu.long_chunk;
   rd.slot_floats = L.slot_floats;
-  static int red_grid[64] = {0};
+  static int red_grid[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) dev = 63;
-  if (red_grid[dev] == 0) red_grid[dev] = grid_for((const void*)reduce_kernel, kRedThreads);
+  const bool weighted = rd.psw_sorted != nullptr;
+  if (red_grid[weighted][dev] == 0)
+    red_grid[weighted][dev] =
+        grid_for(weighted ? (const void*)reduce_kernel<true> : (const void*)reduce_kernel<false>, kRedThreads);
   const int64_t want = ((N + 31) / 32 + 7) / 8 + 1;
-  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[dev], want));
-  reduce_kernel<<<rgrid, kRedThreads, 0, s>>>(rd);
+  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[weighted][dev], want));
+  if (weighted)
+    reduce_kernel<true><<<rgrid, kRedThreads, 0, s>>>(rd);
+  else
+    reduce_kernel<false><<<rgrid, kRedThreads, 0, s>>>(rd);
   if (check_launch()) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_reduce");
   return TBE_OK;
