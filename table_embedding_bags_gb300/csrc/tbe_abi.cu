@@ -11,7 +11,7 @@
 namespace tbe {
 
 // Defaults come from the measured sweeps recorded with the benchmark.
-static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/256, /*fwd_unroll=*/8,
+static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/256, /*fwd_unroll=*/4,
                           /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48};
 
 const Tuning& tuning() { return g_tuning; }

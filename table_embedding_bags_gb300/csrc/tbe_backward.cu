@@ -107,6 +107,11 @@ __device__ __forceinline__ uint32_t lookback_window(const uint32_t* words, int32
   return excl;
 }
 
+// Kernels launched with programmatic stream serialisation start while their
+// predecessor drains; this waits until the predecessor grid has completed and
+// its writes are visible (a no-op for a kernel launched without the attribute).
+__device__ __forceinline__ void wait_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T, int64_t row) {
   int lo = 0, hi = T - 1;  // largest t with row_base[t] <= row
   while (lo < hi) {
@@ -326,7 +331,8 @@ struct SortArgs {
   int32_t shift;
 };
 
-__global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs a) {
+__global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortArgs a) {
+  wait_predecessor();
   __shared__ uint32_t s_wcnt[kSortWarps][256];
   __shared__ uint32_t s_start[256];   // tile-local first slot of each digit
   __shared__ int32_t s_gbase[256];    // global position of slot 0 of each digit, minus s_start
@@ -379,6 +385,9 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
       cnt += c;
     }
   }
+  // publish this tile's count of the digit as soon as it is known
+  uint32_t* my_word = a.lookback + (size_t)tile * 256 + tid;
+  st_relaxed(my_word, (tile == 0 ? kFlagInc : kFlagAgg) | cnt);
   // block exclusive scan of the digit counts -> s_start
   uint32_t x = cnt;
 #pragma unroll
@@ -388,7 +397,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
   }
   if (lane == 31) s_scan[warp] = x;
   // global digit base: exclusive scan of this pass's histogram
-  uint32_t h = __ldg(a.hist + tid);
+  const uint32_t h = __ldg(a.hist + tid);
   uint32_t hx = h;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -400,37 +409,8 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
   for (int w = 0; w < warp; ++w) wsum += s_scan[w];
   s_start[tid] = wsum + x - cnt;
   __syncthreads();
-  if (lane == 31) s_scan[warp] = hx;
-  __syncthreads();
-  uint32_t hsum = 0;
-  for (int w = 0; w < warp; ++w) hsum += s_scan[w];
-  const uint32_t gdigit = hsum + hx - h;
-  // decoupled look-back over earlier tiles for this digit
-  uint32_t* my = a.lookback + (size_t)tile * 256 + tid;
-  uint32_t excl = 0;
-  if (tile == 0) {
-    st_relaxed(my, kFlagInc | cnt);
-  } else {
-    st_relaxed(my, kFlagAgg | cnt);
-    // walk back four tiles per round: the four words are requested together
-    bool done = false;
-    for (int32_t pt = tile - 1; pt >= 0 && !done; pt -= 4) {
-      uint32_t v[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = pt - q >= 0 ? ld_relaxed(a.lookback + (size_t)(pt - q) * 256 + tid) : kFlagInc;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (done) break;
-        if (!(v[q] & (kFlagAgg | kFlagInc))) v[q] = wait_flag(a.lookback + (size_t)(pt - q) * 256 + tid, a.status);
-        excl += v[q] & kValMask;
-        if (v[q] & kFlagInc) done = true;
-      }
-    }
-    st_relaxed(my, kFlagInc | ((excl + cnt) & kValMask));
-  }
-  s_gbase[tid] = (int32_t)(gdigit + excl) - (int32_t)s_start[tid];
-  __syncthreads();
-  // place items in tile-local sorted order
+  // place items in tile-local sorted order (only tile-local prefixes are
+  // needed, so this happens before the look-back and frees the item registers)
 #pragma unroll
   for (int k = 0; k < kSortIPT; ++k) {
     const int32_t idx = wbase + k * 32 + lane;
@@ -441,6 +421,35 @@ __global__ void __launch_bounds__(kSortThreads) sort_pass_kernel(const SortArgs 
       s_vals[slot] = val[k];
     }
   }
+  if (lane == 31) s_scan[warp] = hx;
+  __syncthreads();
+  uint32_t hsum = 0;
+  for (int w = 0; w < warp; ++w) hsum += s_scan[w];
+  const uint32_t gdigit = hsum + hx - h;
+  // decoupled look-back over earlier tiles for this digit: the words of up to
+  // 32 predecessors are requested together (each tile owns its own 1 KB of
+  // words, so no line has two writers), then summed back to the nearest
+  // inclusive one
+  uint32_t excl = 0;
+  if (tile > 0) {
+    bool done = false;
+    for (int32_t hi = tile - 1; hi >= 0 && !done; hi -= 32) {
+      uint32_t v[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q)
+        v[q] = hi - q >= 0 ? ld_relaxed(a.lookback + (size_t)(hi - q) * 256 + tid) : kFlagInc;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        if (done) break;
+        uint32_t w = v[q];
+        if (!(w & (kFlagAgg | kFlagInc))) w = wait_flag(a.lookback + (size_t)(hi - q) * 256 + tid, a.status);
+        excl += w & kValMask;
+        if (w & kFlagInc) done = true;
+      }
+    }
+    st_relaxed(my_word, kFlagInc | ((excl + cnt) & kValMask));
+  }
+  s_gbase[tid] = (int32_t)(gdigit + excl) - (int32_t)s_start[tid];
   __syncthreads();
   const int32_t n_tile = min(kSortTile, a.N - tile * kSortTile);
   for (int i = tid; i < n_tile; i += kSortThreads) {
@@ -478,6 +487,7 @@ struct RleArgs {
 };
 
 __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
+  wait_predecessor();
   __shared__ uint32_t s_scan[kRleThreads / 32];
   __shared__ uint32_t s_excl;
   __shared__ int32_t s_tile;
@@ -582,6 +592,7 @@ struct ClsArgs {
 };
 
 __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) {
+  wait_predecessor();
   __shared__ uint32_t s_scan[2][kClsThreads / 32];
   __shared__ unsigned long long s_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -978,6 +989,7 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
 
 template <bool W>
 __global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a) {
+  wait_predecessor();
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
@@ -990,6 +1002,26 @@ __global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a)
     if ((int32_t)item < n_chunks) long_chunk<W>(a, (int32_t)item, lane);
     else short_batch<W>(a, (int32_t)item - n_chunks, U, lane);
   }
+}
+
+// Launch on `s` with programmatic stream serialisation: the kernel may be
+// scheduled while its predecessor drains and calls wait_predecessor() before
+// reading what the predecessor wrote.  Triggers stay implicit (block exit),
+// so it starts only once every block of the predecessor has finished.
+template <typename Arg>
+int launch_pdl(void (*kernel)(Arg), int grid, int threads, cudaStream_t s, const Arg& arg) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, arg) != cudaSuccess) return TBE_ERR_CUDA;
+  return check_launch();
 }
 
 int grid_for(const void* kernel, int threads, size_t smem = 0) {
@@ -1068,8 +1100,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
     sa.N = (int32_t)N;
     sa.shift = 8 * pass;
-    sort_pass_kernel<<<L.sort_ntiles, kSortThreads, 0, s>>>(sa);
-    if (check_launch()) return TBE_ERR_CUDA;
+    if (launch_pdl(sort_pass_kernel, L.sort_ntiles, kSortThreads, s, sa)) return TBE_ERR_CUDA;
     trace_mark(s, "bwd_sort_pass");
     std::swap(kin, kout);
     vin = vout;
@@ -1091,8 +1122,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   ra.N = (int32_t)N;
   ra.ntiles = L.rle_ntiles;
   ra.sentinel = sentinel;
-  rle_kernel<<<L.rle_ntiles, kRleThreads, 0, s>>>(ra);
-  if (check_launch()) return TBE_ERR_CUDA;
+  if (launch_pdl(rle_kernel, L.rle_ntiles, kRleThreads, s, ra)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_rle");
 
   const Tuning& tu = tuning();
@@ -1112,8 +1142,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   ca.tau = tu.long_run_threshold;
   ca.chunk = tu.long_chunk;
   const int cls_blocks = (int)std::min<int64_t>((N + kClsThreads - 1) / kClsThreads, 4 * sm_count());
-  classify_kernel<<<std::max(cls_blocks, 1), kClsThreads, 0, s>>>(ca);
-  if (check_launch()) return TBE_ERR_CUDA;
+  if (launch_pdl(classify_kernel, std::max(cls_blocks, 1), kClsThreads, s, ca)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_classify");
 
   RedArgs rd;
@@ -1149,11 +1178,8 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         grid_for(weighted ? (const void*)reduce_kernel<true> : (const void*)reduce_kernel<false>, kRedThreads);
   const int64_t want = ((N + 31) / 32 + 7) / 8 + 1;
   const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[weighted][dev], want));
-  if (weighted)
-    reduce_kernel<true><<<rgrid, kRedThreads, 0, s>>>(rd);
-  else
-    reduce_kernel<false><<<rgrid, kRedThreads, 0, s>>>(rd);
-  if (check_launch()) return TBE_ERR_CUDA;
+  if (launch_pdl(weighted ? reduce_kernel<true> : reduce_kernel<false>, rgrid, kRedThreads, s, rd))
+    return TBE_ERR_CUDA;
   trace_mark(s, "bwd_reduce");
   return TBE_OK;
 }

@@ -143,7 +143,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 }
 
 template <typename OutT, bool COUNTS_ONLY>
-__global__ void __launch_bounds__(kThreads) hist_kernel(const FwdArgs a, int32_t* counts_out) {
+__global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int32_t* counts_out) {
   extern __shared__ unsigned char smem_raw[];
   const int D = __ldg(&a.meta[0].D);
   const HistLayout L(D);
@@ -314,16 +314,27 @@ template <typename OutT, bool COUNTS_ONLY>
 int launch_hist(const FwdArgs& a, int32_t* counts, int D, cudaStream_t s) {
   const size_t smem = HistLayout(D).total + 1024;  // + alignment slack
   if (cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+                           (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return TBE_ERR_CUDA;
   const int ntiles = (a.B + kM - 1) / kM;
   // CTAs per SM: what shared memory allows, capped so that their TMEM
   // accumulators (<= 256 columns each) fit the 512 columns of an SM
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hist_kernel<OutT, COUNTS_ONLY>, kThreads, smem) !=
-          cudaSuccess ||
-      per_sm < 1)
-    per_sm = 1;
+  // CTAs per SM from the kernel's registers and shared memory (the launch
+  // bounds keep it at <= 128 registers, so two fit the register file)
+  int per_sm = 2;
+  {
+    cudaFuncAttributes fa;
+    int dev = 0, smem_sm = 0;
+    cudaGetDevice(&dev);
+    if (cudaFuncGetAttributes(&fa, hist_kernel<OutT, COUNTS_ONLY>) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess) {
+      const int by_regs = 65536 / std::max(1, fa.numRegs * kThreads);
+      const int by_smem = smem_sm / (int)(smem + 1024);
+      per_sm = std::max(1, std::min(by_regs, by_smem));
+    }
+  }
   const int ncols = D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : 256));
   if (!COUNTS_ONLY) per_sm = std::min(per_sm, 512 / ncols);
   const int grid = std::max(1, std::min(ntiles, sm_count() * per_sm));
