@@ -219,13 +219,22 @@ int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, c
  *   long_run_threshold : runs with at least this many lookups take the
  *                        long-run (chunked, multi-warp) tier; shorter runs
  *                        are reduced by one warp each
- *   long_chunk         : lookups per chunk of a long run
- *   fwd_unroll         : independent row loads in flight per lane group in
- *                        the forward gather (2, 4 or 8)
+ *   long_chunk         : lookups per chunk of a long run (a multiple of 32,
+ *                        or 0: chosen from the batch size, 64..256)
+ *   fwd_unroll         : 16-byte row chunks in flight per lane in the
+ *                        forward gather (4 or 8)
+ *   fwd_lanes_per_row  : most lanes that share one row in the forward gather
+ *                        (1, 2, 4, 8, 16 or 32); fewer lanes pool more bags
+ *                        per warp at once
+ *   red_unroll         : gradient slices in flight per lane in the backward
+ *                        reduction (4: more resident warps, 8: deeper)
  *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
  *                        many as fit)
  *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
  *                        N / B reaches this
+ *   short_item_lookups : lookups per work item of the short-run tier (runs
+ *                        are grouped by 32 and cut into parts of about this
+ *                        many lookups; raised to long_run_threshold if lower)
  * Values outside their ranges are rejected with TBE_ERR_INVALID_ARG. */
 typedef struct tbe_tuning {
   int32_t long_run_threshold;
@@ -233,6 +242,9 @@ typedef struct tbe_tuning {
   int32_t fwd_unroll;
   int32_t fwd_blocks_per_sm;
   int32_t hist_min_mean_bag;
+  int32_t short_item_lookups;
+  int32_t fwd_lanes_per_row;
+  int32_t red_unroll;
 } tbe_tuning;
 int tbe_get_tuning(tbe_tuning* out);
 int tbe_set_tuning(const tbe_tuning* in);

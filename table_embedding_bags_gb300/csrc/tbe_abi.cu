@@ -11,8 +11,10 @@
 namespace tbe {
 
 // Defaults come from the measured sweeps recorded with the benchmark.
-static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/256, /*fwd_unroll=*/4,
-                          /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48};
+static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/0, /*fwd_unroll=*/4,
+                          /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48,
+                          /*short_item_lookups=*/32, /*fwd_lanes_per_row=*/16,
+                          /*red_unroll=*/4};
 
 const Tuning& tuning() { return g_tuning; }
 
@@ -99,21 +101,33 @@ int tbe_get_tuning(tbe_tuning* out) {
   out->fwd_unroll = g_tuning.fwd_unroll;
   out->fwd_blocks_per_sm = g_tuning.fwd_blocks_per_sm;
   out->hist_min_mean_bag = g_tuning.hist_min_mean_bag;
+  out->short_item_lookups = g_tuning.short_item_lookups;
+  out->fwd_lanes_per_row = g_tuning.fwd_lanes_per_row;
+  out->red_unroll = g_tuning.red_unroll;
   return TBE_OK;
 }
 
 int tbe_set_tuning(const tbe_tuning* in) {
   if (!in) return TBE_ERR_INVALID_ARG;
   if (in->long_run_threshold < 1 || in->long_run_threshold > (1 << 20)) return TBE_ERR_INVALID_ARG;
-  if (in->long_chunk < 32 || in->long_chunk > 65536 || (in->long_chunk % 32) != 0) return TBE_ERR_INVALID_ARG;
-  if (in->fwd_unroll != 2 && in->fwd_unroll != 4 && in->fwd_unroll != 8) return TBE_ERR_INVALID_ARG;
+  if (in->long_chunk != 0 && (in->long_chunk < 32 || in->long_chunk > 65536 || (in->long_chunk % 32) != 0))
+    return TBE_ERR_INVALID_ARG;
+  if (in->fwd_unroll != 4 && in->fwd_unroll != 8) return TBE_ERR_INVALID_ARG;
+  if (in->fwd_lanes_per_row < 1 || in->fwd_lanes_per_row > 32 ||
+      (in->fwd_lanes_per_row & (in->fwd_lanes_per_row - 1)) != 0)
+    return TBE_ERR_INVALID_ARG;
   if (in->fwd_blocks_per_sm < 0 || in->fwd_blocks_per_sm > 32) return TBE_ERR_INVALID_ARG;
   if (in->hist_min_mean_bag < 0) return TBE_ERR_INVALID_ARG;
+  if (in->red_unroll != 4 && in->red_unroll != 8) return TBE_ERR_INVALID_ARG;
+  if (in->short_item_lookups < 32 || in->short_item_lookups > (1 << 20)) return TBE_ERR_INVALID_ARG;
   g_tuning.long_run_threshold = in->long_run_threshold;
   g_tuning.long_chunk = in->long_chunk;
   g_tuning.fwd_unroll = in->fwd_unroll;
   g_tuning.fwd_blocks_per_sm = in->fwd_blocks_per_sm;
   g_tuning.hist_min_mean_bag = in->hist_min_mean_bag;
+  g_tuning.short_item_lookups = in->short_item_lookups;
+  g_tuning.fwd_lanes_per_row = in->fwd_lanes_per_row;
+  g_tuning.red_unroll = in->red_unroll;
   return TBE_OK;
 }
 
@@ -292,6 +306,7 @@ int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* i
   a.N = N;
   a.sumD = plan->sumD;
   a.out_vec_ok = plan->out_vec_ok && (((uintptr_t)out & 15) == 0);
+  a.lpr_max = g_tuning.fwd_lanes_per_row;
   bool hist = false;
   if (path == TBE_PATH_HISTOGRAM) {
     if (!hist_eligible(plan, per_sample_weights)) return TBE_ERR_UNSUPPORTED;

@@ -74,35 +74,75 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   return v;
 }
 
-// Waits (bounded) for a published look-back word; returns 0 on time-out.
-__device__ __forceinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status) {
+// Waits (bounded) for a published look-back word; on time-out it reports
+// TBE_DEV_TIMEOUT and returns an inclusive zero so no later tile waits on it.
+// Out of line: waiting is the rare path, and inlined copies would only grow
+// the hot code that every block fetches.
+__device__ __noinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status) {
   for (int it = 0; it < kSpinLimit; ++it) {
     uint32_t v = ld_relaxed(p);
     if (v & (kFlagAgg | kFlagInc)) return v;
     if (it > 64) __nanosleep(100);
   }
   report(status, TBE_DEV_TIMEOUT);
-  return kFlagInc;  // treat as an inclusive zero so no later tile waits on it
+  return kFlagInc;
 }
 
-// Exclusive prefix of tile `tile` from the look-back words of its
-// predecessors, read 32 at a time by one warp: the nearest inclusive word
-// ends the walk, aggregate words before it are added.  Every wait is
-// bounded (wait_flag).
-__device__ __forceinline__ uint32_t lookback_window(const uint32_t* words, int32_t tile, int lane,
-                                                    int32_t* status) {
+// Mask of the window positions 0..q* (q* = nearest predecessor with an
+// inclusive word; all 32 positions when there is none).
+__device__ __forceinline__ uint32_t window_upto(uint32_t inc) {
+  return inc ? (((inc & (0u - inc)) << 1) - 1u) : 0xffffffffu;
+}
+
+// Slow path of one look-back window whose words are not all published: walks
+// predecessors hi, hi-1, ... (at most 32), waiting on each, and stops at the
+// first inclusive word.  Returns (found << 32) | sum.
+__device__ __noinline__ unsigned long long lookback_window_slow(const uint32_t* col, size_t stride, int32_t hi,
+                                                                int32_t* status) {
+  uint32_t sum = 0;
+  for (int q = 0; q < 32 && hi - q >= 0; ++q) {
+    uint32_t w = ld_relaxed(col + (size_t)(hi - q) * stride);
+    if (!(w & (kFlagAgg | kFlagInc))) w = wait_flag(col + (size_t)(hi - q) * stride, status);
+    sum += w & kValMask;
+    if (w & kFlagInc) return (1ull << 32) | sum;
+  }
+  return sum;
+}
+
+// Exclusive prefix of tile `tile` computed by a whole block of kRleThreads
+// threads: thread i reads the word of predecessor tile-1-i (kRleThreads
+// predecessors per round, all requested at once), and the block sums the
+// words up to the nearest inclusive one.  Every thread must call it; `s_lb`
+// is 2 * warps words of shared scratch.  Every wait is bounded (wait_flag).
+template <int kThreads>
+__device__ __forceinline__ uint32_t lookback_block(const uint32_t* words, int32_t tile, int32_t* status,
+                                                   uint32_t* s_lb) {
+  constexpr int kWarps = kThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t excl = 0;
-  for (int32_t end = tile - 1; end >= 0; end -= 32) {
-    const int32_t k = end - lane;
+  for (int32_t top = tile - 1; top >= 0; top -= kThreads) {
+    const int32_t k = top - tid;
     uint32_t v = k >= 0 ? ld_relaxed(words + k) : kFlagInc;
     if (!(v & (kFlagAgg | kFlagInc))) v = wait_flag(words + k, status);
     const unsigned inc = __ballot_sync(kFull, (v & kFlagInc) != 0);
-    const int first = inc ? __ffs(inc) - 1 : 31;  // nearest inclusive predecessor in the window
-    uint32_t x = lane <= first ? (v & kValMask) : 0u;
+    if (lane == 0) s_lb[warp] = inc;
+    __syncthreads();
+    int stop = kThreads - 1;  // block position of the nearest inclusive word
+#pragma unroll
+    for (int w = kWarps - 1; w >= 0; --w)
+      if (s_lb[w]) stop = w * 32 + __ffs(s_lb[w]) - 1;
+    uint32_t x = tid <= stop ? (v & kValMask) : 0u;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
-    excl += x;
-    if (inc) break;
+    if (lane == 0) s_lb[kWarps + warp] = x;
+    __syncthreads();
+    uint32_t sum = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) sum += s_lb[kWarps + w];
+    excl += sum;
+    const bool found = stop < kThreads - 1 || s_lb[kWarps - 1] != 0;
+    __syncthreads();  // s_lb is reused by the next round
+    if (found) break;
   }
   return excl;
 }
@@ -125,19 +165,28 @@ __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t keys_a, keys_b, vals_a, vals_b, bag_of, bag_sorted, psw_sorted, run_starts, long_list, gofs, partials;
+  size_t keys_a, keys_b, vals_a, vals_b, bag_of, bag_sorted, psw_sorted, run_starts, run_table, long_list, sub_list, gofs, partials;
   size_t zero_begin, hist, sort_tiles, rle_tile, counters, zero_end;
   size_t lin_zero_begin, sort_lookback, rle_lookback, combine, lin_zero_end;
   size_t total;
   int npass, sort_ntiles, rle_ntiles;
-  int64_t long_cap, chunk_cap;
-  int32_t slot_floats;
+  int64_t long_cap, chunk_cap, sub_cap;
+  int32_t slot_floats, item_lookups, chunk;
 };
 
 // counters: 8-byte slots; kCntLong holds (long runs << 32) | chunks
-enum Counter { kCntU = 0, kCntInvalid = 1, kCntWork = 2, kCntLong = 4, kNumCounters = 8 };
+enum Counter { kCntU = 0, kCntInvalid = 1, kCntWork = 2, kCntSub = 3, kCntLong = 4, kNumCounters = 8 };
 
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Lookups per long-run chunk: the tuning value, or with 0 a size that keeps
+// a few work items per warp of the reduction (64 for small batches, up to
+// 256 for large ones, where fewer chunks mean less combining).
+static int32_t effective_chunk(const Tuning& tu, int64_t N) {
+  if (tu.long_chunk > 0) return tu.long_chunk;
+  const int64_t per = N / (4 * 32 * (int64_t)sm_count());
+  return (int32_t)std::min<int64_t>(256, std::max<int64_t>(64, per / 32 * 32));
+}
 
 Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   (void)B;
@@ -147,9 +196,13 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.sort_ntiles = (int)((N + kSortTile - 1) / kSortTile);
   L.rle_ntiles = (int)((N + kRleTile - 1) / kRleTile);
   const int64_t tau = std::max(1, tu.long_run_threshold);
-  const int64_t C = tu.long_chunk;
+  L.chunk = effective_chunk(tu, N);
+  const int64_t C = L.chunk;
   L.long_cap = N / tau + 1;
   L.chunk_cap = N / C + L.long_cap + 1;
+  // a part holds at least item_lookups lookups except the last of a batch
+  L.item_lookups = (int32_t)std::max<int64_t>(tu.short_item_lookups, tau);
+  L.sub_cap = (N + 31) / 32 + N / L.item_lookups + 1;
   L.slot_floats = (p.maxD + 3) / 4 * 4;
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t o = off; off += up256(bytes); return o; };
@@ -161,7 +214,9 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.bag_sorted = take(4 * (size_t)N);
   L.psw_sorted = take(4 * (size_t)N);
   L.run_starts = take(4 * (size_t)(N + 1));
+  L.run_table = take(4 * (size_t)N);
   L.long_list = take(16 * (size_t)L.long_cap);
+  L.sub_list = take(8 * (size_t)L.sub_cap);
   L.gofs = take(8 * (size_t)(p.T + 1));
   L.partials = take(4 * (size_t)L.chunk_cap * L.slot_floats);
   L.zero_begin = off;  // cleared by a memset before the first kernel
@@ -428,24 +483,34 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   const uint32_t gdigit = hsum + hx - h;
   // decoupled look-back over earlier tiles for this digit: the words of up to
   // 32 predecessors are requested together (each tile owns its own 1 KB of
-  // words, so no line has two writers), then summed back to the nearest
-  // inclusive one
+  // words, so no line has two writers) and summed, without branches, back to
+  // the nearest inclusive one.  A window with a word not yet published goes
+  // to the out-of-line slow path.
   uint32_t excl = 0;
   if (tile > 0) {
-    bool done = false;
-    for (int32_t hi = tile - 1; hi >= 0 && !done; hi -= 32) {
+    const uint32_t* col = a.lookback + tid;
+    for (int32_t hi = tile - 1; hi >= 0; hi -= 32) {
       uint32_t v[32];
 #pragma unroll
-      for (int q = 0; q < 32; ++q)
-        v[q] = hi - q >= 0 ? ld_relaxed(a.lookback + (size_t)(hi - q) * 256 + tid) : kFlagInc;
+      for (int q = 0; q < 32; ++q) v[q] = hi - q >= 0 ? ld_relaxed(col + (size_t)(hi - q) * 256) : kFlagInc;
+      uint32_t inc = 0, miss = 0;
 #pragma unroll
       for (int q = 0; q < 32; ++q) {
-        if (done) break;
-        uint32_t w = v[q];
-        if (!(w & (kFlagAgg | kFlagInc))) w = wait_flag(a.lookback + (size_t)(hi - q) * 256 + tid, a.status);
-        excl += w & kValMask;
-        if (w & kFlagInc) done = true;
+        inc |= (v[q] >> 31) << q;
+        miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
       }
+      const uint32_t upto = window_upto(inc);
+      if (miss & upto) {
+        const unsigned long long r = lookback_window_slow(col, 256, hi, a.status);
+        excl += (uint32_t)r;
+        if (r >> 32) break;
+        continue;
+      }
+      uint32_t sum = 0;
+#pragma unroll
+      for (int q = 0; q < 32; ++q) sum += ((upto >> q) & 1u) ? (v[q] & kValMask) : 0u;
+      excl += sum;
+      if (inc) break;
     }
     st_relaxed(my_word, kFlagInc | ((excl + cnt) & kValMask));
   }
@@ -467,6 +532,28 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   }
 }
 
+// First row of the table after `tp` (tp = -1: the first table); no further
+// table: the largest key.
+__device__ __forceinline__ int64_t next_table_base(const TableMeta* meta, int32_t T, int tp) {
+  return tp + 1 < T ? __ldg(&meta[tp + 1].row_base) : INT64_MAX;
+}
+
+// A run of key `key` starts at unique index u after keys of table tp: every
+// table in (tp, table(key)] starts with u unique rows below it.  Returns
+// table(key).
+__device__ __noinline__ int cross_tables(const TableMeta* meta, int32_t T, int64_t* unique_count, int tp,
+                                         int64_t key, uint32_t u) {
+  const int tk = table_of_row(meta, T, key);
+  for (int t = tp + 1; t <= tk; ++t) unique_count[t] = u;
+  return tk;
+}
+
+// After the last valid key (table tk): the tables after it, and the end
+// marker T, see all U unique rows below them.
+__device__ __noinline__ void finish_tables(int64_t* unique_count, int32_t T, int tk, uint32_t U) {
+  for (int t = tk + 1; t <= T; ++t) unique_count[t] = U;
+}
+
 // ---------------------------------------------------------------------------
 // 3. run-length segmentation
 // ---------------------------------------------------------------------------
@@ -477,6 +564,7 @@ struct RleArgs {
   int32_t T;
   int64_t* unique_rows;
   int32_t* run_starts;
+  int32_t* run_table;    // table of every run
   uint32_t* lookback;
   uint32_t* tile_counter;
   uint32_t* counters;
@@ -489,6 +577,7 @@ struct RleArgs {
 __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   wait_predecessor();
   __shared__ uint32_t s_scan[kRleThreads / 32];
+  __shared__ uint32_t s_lb[2 * (kRleThreads / 32)];
   __shared__ uint32_t s_excl;
   __shared__ int32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -522,15 +611,14 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
     total += s_scan[w];
   }
   const uint32_t mine = wsum + x - nflag;
-  if (warp == 0) {
+  {
     uint32_t* my = a.lookback + tile;
-    uint32_t excl = 0;
-    if (lane == 0) st_relaxed(my, (tile == 0 ? kFlagInc : kFlagAgg) | total);
-    if (tile > 0) {
-      excl = lookback_window(a.lookback, tile, lane, a.status);
-      if (lane == 0) st_relaxed(my, kFlagInc | ((excl + total) & kValMask));
+    if (tid == 0) st_relaxed(my, (tile == 0 ? kFlagInc : kFlagAgg) | total);
+    const uint32_t excl = tile > 0 ? lookback_block<kRleThreads>(a.lookback, tile, a.status, s_lb) : 0u;
+    if (tid == 0) {
+      if (tile > 0) st_relaxed(my, kFlagInc | ((excl + total) & kValMask));
+      s_excl = excl;
     }
-    if (lane == 0) s_excl = excl;
   }
   if (tid == 0) {
     const uint32_t excl = s_excl;
@@ -544,31 +632,34 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   __syncthreads();
   uint32_t u = s_excl + mine;
   // per-table counts: unique_count[t] = number of unique rows below
-  // table_row_base[t].  A run start whose previous key lies in an earlier
-  // table writes the count for every table boundary in between; the last
-  // valid key writes U for the tables after it.
+  // table_row_base[t].  A run start whose key lies past the table of the
+  // previous valid key writes the count for every table boundary in between;
+  // the last valid key writes U for the tables after it.  The thread tracks
+  // the table of its latest key and the next table's first row, so the
+  // search for a key's table only runs at a boundary (out of line).
   int64_t prevk = (j0 > 0 && j0 - 1 < a.N) ? (int64_t)__ldg(a.keys + j0 - 1) : -1;
   if (prevk >= (int64_t)a.sentinel) prevk = -1;
   const uint32_t knext = (j0 + kRleIPT < a.N) ? __ldg(a.keys + j0 + kRleIPT) : a.sentinel;
   if (j0 == 0 && (a.N == 0 || k[0] >= a.sentinel))  // no valid lookup at all
     for (int t = 0; t <= a.T; ++t) a.unique_count[t] = 0;
+  int tp = prevk < 0 ? -1 : table_of_row(a.meta, a.T, prevk);
+  int64_t next_base = next_table_base(a.meta, a.T, tp);
 #pragma unroll
   for (int q = 0; q < kRleIPT; ++q) {
     const int32_t j = j0 + q;
     if ((flags & (1u << q)) && u < (uint32_t)a.N) {  // u < N unless a wait timed out
       a.unique_rows[u] = (int64_t)k[q];
       a.run_starts[u] = j;
-      const int tk = table_of_row(a.meta, a.T, (int64_t)k[q]);
-      const int tp = prevk < 0 ? -1 : table_of_row(a.meta, a.T, prevk);
-      for (int t = tp + 1; t <= tk; ++t) a.unique_count[t] = u;
+      if ((int64_t)k[q] >= next_base) {
+        tp = cross_tables(a.meta, a.T, a.unique_count, tp, (int64_t)k[q], u);
+        next_base = next_table_base(a.meta, a.T, tp);
+      }
+      a.run_table[u] = tp;
       ++u;
     }
     const uint32_t nk = q + 1 < kRleIPT ? k[q + 1] : knext;
-    if (j < a.N && k[q] < a.sentinel && (j == a.N - 1 || nk >= a.sentinel)) {  // last valid key
-      const int tk = table_of_row(a.meta, a.T, (int64_t)k[q]);
-      for (int t = tk + 1; t <= a.T; ++t) a.unique_count[t] = min(u, (uint32_t)a.N);
-    }
-    if (j < a.N && k[q] < a.sentinel) prevk = (int64_t)k[q];
+    if (j < a.N && k[q] < a.sentinel && (j == a.N - 1 || nk >= a.sentinel))  // last valid key
+      finish_tables(a.unique_count, a.T, tp, min(u, (uint32_t)a.N));
   }
 }
 
@@ -581,7 +672,8 @@ struct ClsArgs {
   const TableMeta* meta;
   int4* long_list;          // {u, first chunk, chunks, length}
   unsigned long long* long_counter;  // (runs << 32) | chunks
-  const uint32_t* counters;
+  uint32_t* counters;
+  int2* sub_list;           // short-run work items {batch, part}
   const int64_t* unique_count;  // [T+1], written by the segmentation kernel
   int64_t* gofs;            // [T+1] float offset of each table's block
   int32_t* status;
@@ -589,12 +681,14 @@ struct ClsArgs {
   int32_t T;
   int32_t tau;
   int32_t chunk;
+  int32_t item_lookups;     // lookups per short-run work item (>= tau)
 };
 
 __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) {
   wait_predecessor();
-  __shared__ uint32_t s_scan[2][kClsThreads / 32];
+  __shared__ uint32_t s_scan[3][kClsThreads / 32];
   __shared__ unsigned long long s_base;
+  __shared__ uint32_t s_sub_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   if (blockIdx.x == 0) {
@@ -637,28 +731,38 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
     if (u < U) len = a.run_starts[u + 1] - a.run_starts[u];
     const bool is_long = u < U && len >= a.tau;
     const uint32_t nch = is_long ? (uint32_t)((len + a.chunk - 1) / a.chunk) : 0u;
+    // this warp's 32 runs are one batch; its short lookups are cut into
+    // parts of item_lookups each (one work item per part)
+    uint32_t short_sum = (u < U && !is_long) ? (uint32_t)len : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) short_sum += __shfl_xor_sync(kFull, short_sum, o);
+    const uint32_t nsub = (short_sum + a.item_lookups - 1) / a.item_lookups;
     uint32_t x0 = is_long, x1 = nch;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y0 = __shfl_up_sync(kFull, x0, o), y1 = __shfl_up_sync(kFull, x1, o);
       if (lane >= o) { x0 += y0; x1 += y1; }
     }
-    if (lane == 31) { s_scan[0][warp] = x0; s_scan[1][warp] = x1; }
+    if (lane == 31) { s_scan[0][warp] = x0; s_scan[1][warp] = x1; s_scan[2][warp] = nsub; }
     __syncthreads();
-    uint32_t w0 = 0, w1 = 0, t0 = 0, t1 = 0;
+    uint32_t w0 = 0, w1 = 0, w2 = 0, t0 = 0, t1 = 0, t2 = 0;
     for (int w = 0; w < kClsThreads / 32; ++w) {
-      if (w < warp) { w0 += s_scan[0][w]; w1 += s_scan[1][w]; }
+      if (w < warp) { w0 += s_scan[0][w]; w1 += s_scan[1][w]; w2 += s_scan[2][w]; }
       t0 += s_scan[0][w];
       t1 += s_scan[1][w];
+      t2 += s_scan[2][w];
     }
     if (tid == 0 && t0 > 0)
       s_base = atomicAdd(a.long_counter, ((unsigned long long)t0 << 32) | (unsigned long long)t1);
+    if (tid == 32 && t2 > 0) s_sub_base = atomicAdd(&a.counters[kCntSub * 2], t2);
     __syncthreads();
     if (is_long) {
       const uint32_t lpos = (uint32_t)(s_base >> 32) + w0 + x0 - 1;
       const uint32_t cpos = (uint32_t)(s_base & 0xffffffffu) + w1 + x1 - nch;
       a.long_list[lpos] = make_int4(u, (int)cpos, (int)nch, len);
     }
+    for (uint32_t k = lane; k < nsub; k += 32)
+      a.sub_list[s_sub_base + w2 + k] = make_int2((u0 >> 5) + warp, (int)k);
     __syncthreads();
   }
 }
@@ -673,6 +777,7 @@ struct RedArgs {
   const float* psw_sorted;    // weight of every sorted lookup (null: unweighted)
   const int64_t* unique_rows;
   const int32_t* run_starts;
+  const int32_t* run_table;
   const int4* long_list;
   const unsigned long long* long_counter;
   uint32_t* counters;
@@ -682,8 +787,9 @@ struct RedArgs {
   const int64_t* gofs;
   float* row_grads;
   int32_t* status;
+  const int2* sub_list;       // short-run work items {batch, part}
   int64_t capacity;
-  int32_t T, B, sumD, tau, chunk, slot_floats;
+  int32_t T, B, sumD, tau, chunk, slot_floats, item_lookups;
 };
 
 // Where run u's row gradient goes and how wide it is.
@@ -695,8 +801,7 @@ struct RunInfo {
 };
 
 __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
-  const int64_t row = a.unique_rows[u];
-  const int32_t t = table_of_row(a.meta, a.T, row);
+  const int32_t t = a.run_table[u];
   RunInfo r;
   r.D = __ldg(&a.meta[t].D);
   r.col_off = __ldg(&a.meta[t].col_off);
@@ -732,7 +837,6 @@ __device__ __forceinline__ float4 ld_grad(const float* p) {
 }
 
 constexpr int kColsPerPass = 128;      // 32 lanes x one float4
-constexpr int kRedUnroll = 8;          // grad_out slices in flight per warp
 
 __device__ __forceinline__ int32_t clamp_bag(int32_t b, int32_t B) {
   return (uint32_t)b < (uint32_t)B ? b : 0;  // defensive: b < B always holds for valid inputs
@@ -759,12 +863,11 @@ __device__ __forceinline__ void fetch_lookup(const RedArgs& a, int32_t j, bool o
 // Sum of sorted lookups [j0, j1) of one run (columns [cb, cb + 128)).  The
 // bags of the next 32 lookups are requested while the current 32 gradient
 // slices are in flight.
-template <bool W>
+template <bool W, int UNR>
 __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int32_t j1, int cb, int lane,
                             Acc& acc) {
   const int C4 = r.D >> 2;
   const int c = (cb >> 2) + lane;
-  const bool full_cols = C4 - (cb >> 2) >= 32;  // uniform: every lane owns a column chunk
   const float* gcol = a.grad_out + r.col_off + 4 * c;
   int32_t nxt_b;
   float nxt_w;
@@ -774,28 +877,17 @@ __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int3
     const int32_t my_b = nxt_b;
     const float my_w = nxt_w;
     fetch_lookup<W>(a, jb + 32 + lane, jb + 32 + lane < j1, r.weighted, nxt_b, nxt_w);
-    if (n == 32 && full_cols) {  // full group: no predicates
+#pragma unroll 1
+    for (int q0 = 0; q0 < n; q0 += UNR) {
+      float4 g[UNR];
 #pragma unroll
-      for (int q0 = 0; q0 < 32; q0 += kRedUnroll) {
-        float4 g[kRedUnroll];
-#pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u)
-          g[u] = ld_grad(gcol + (int64_t)__shfl_sync(kFull, my_b, q0 + u) * a.sumD);
-#pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u) acc.add<W>(u & 1, g[u], W ? __shfl_sync(kFull, my_w, q0 + u) : 1.f);
+      for (int u = 0; u < UNR; ++u) {
+        const int q = q0 + u;
+        const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+        g[u] = (q < n && c < C4) ? ld_grad(gcol + (int64_t)b * a.sumD) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-    } else {
-      for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
-        float4 g[kRedUnroll];
 #pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u) {
-          const int q = q0 + u;
-          const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-          g[u] = (q < n && c < C4) ? ld_grad(gcol + (int64_t)b * a.sumD) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u) acc.add<W>(u & 1, g[u], W ? __shfl_sync(kFull, my_w, (q0 + u) & 31) : 1.f);
-      }
+      for (int u = 0; u < UNR; ++u) acc.add<W>(u & 1, g[u], W ? __shfl_sync(kFull, my_w, (q0 + u) & 31) : 1.f);
     }
   }
 }
@@ -806,7 +898,7 @@ __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int3
 // children-1 after a device-scope fence) sums the children in index order
 // and writes the node's slot, or the row gradient at the root.  The order of
 // every sum is fixed, so the result does not depend on arrival order.
-template <bool W>
+template <bool W, int UNR>
 __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   const unsigned long long lc = *a.long_counter;
   const int32_t n_long = (int32_t)(lc >> 32);
@@ -826,7 +918,7 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   for (int cb = 0; cb < r.D; cb += kColsPerPass) {
     Acc acc;
     acc.zero();
-    sum_lookups<W>(a, r, j0, j1, cb, lane, acc);
+    sum_lookups<W, UNR>(a, r, j0, j1, cb, lane, acc);
     const float4 v = acc.sum();
     const int c = (cb >> 2) + lane;
     if (nch == 1)
@@ -874,12 +966,16 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   }
 }
 
-// Batch of 32 consecutive runs; the warp reduces the short ones in run order
-// as one flattened stream of lookups (lane l holds the metadata of run
-// 32*batch + l) and stores a run's row gradient at its last lookup.  Long
-// runs of the batch are skipped (their chunks are separate work items).
-template <bool W>
-__device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane) {
+// Part `part` of a batch of 32 consecutive runs.  The short runs of the batch
+// form one flattened stream of lookups in run order (lane l holds the
+// metadata of run 32*batch + l); part k takes the runs whose first lookup
+// falls in [k*L, (k+1)*L) of that stream (L = a.item_lookups >= the
+// threshold, so no part is empty and each has fewer than L + threshold
+// lookups).  The warp reduces the part's stream and stores a run's row
+// gradient at its last lookup.  Long runs are skipped (their chunks are
+// separate work items).
+template <bool W, int UNR>
+__device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32_t U, int lane) {
   const int32_t u = batch * 32 + lane;
   int32_t rs = 0, len = 0;
   RunInfo r{0, 0, 4, 0};
@@ -888,7 +984,18 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
     len = a.run_starts[u + 1] - rs;
     r = run_info(a, u);
   }
-  const int32_t cnt = (u < U && len < a.tau) ? len : 0;
+  int32_t cnt = (u < U && len < a.tau) ? len : 0;
+  {  // keep the runs of this part
+    int32_t x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    const int64_t first = (int64_t)(x - cnt);
+    const int64_t lo = (int64_t)part * a.item_lookups;
+    if (first < lo || first >= lo + a.item_lookups) cnt = 0;
+  }
   int32_t incl = cnt;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -898,8 +1005,8 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
   const int32_t excl = incl - cnt;
   const int32_t total = __shfl_sync(kFull, incl, 31);
   if (total == 0) return;
-  // do all short runs of the batch belong to one table?  (then every lookup
-  // shares the column offset and width)
+  // do all runs of the part belong to one table?  (then every lookup shares
+  // the column offset and width)
   const unsigned act = __ballot_sync(kFull, cnt > 0);
   const int first = __ffs(act) - 1;
   const int32_t coff0 = __shfl_sync(kFull, r.col_off, first);
@@ -908,6 +1015,8 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
   int maxD = cnt > 0 ? r.D : 0;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) maxD = max(maxD, __shfl_xor_sync(kFull, maxD, o));
+  // float4 columns this run's row gradient may store (0: over capacity)
+  const int32_t st_c4 = (cnt > 0 && r.out_off + r.D <= a.capacity) ? (r.D >> 2) : 0;
 
   for (int cb = 0; cb < maxD; cb += kColsPerPass) {
     const int c = (cb >> 2) + lane;
@@ -940,67 +1049,62 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t U, int lane
       const float my_w = nxt_w;
       const unsigned ends = __ballot_sync(kFull, nxt_end);
       if (fb + 32 < total) fetch(fb + 32, nxt_r, nxt_b, nxt_w, nxt_end);
-      auto flush = [&](int q) {  // lookup q ends its run: store the run's row gradient
+      // lookup q ends its run: store the run's row gradient
+      auto flush = [&](int q) {
         const int rr = __shfl_sync(kFull, my_r, q);
         const int64_t off = __shfl_sync(kFull, r.out_off, rr);
-        const int C4r = __shfl_sync(kFull, r.D, rr) >> 2;
-        store_col(a.row_grads, acc.sum(), c, C4r, a.capacity, off);
+        const int32_t c4 = __shfl_sync(kFull, st_c4, rr);
+        if (c < c4) *reinterpret_cast<float4*>(a.row_grads + off + 4 * c) = acc.sum();
         acc.zero();
       };
-      if (one_table && n == 32 && (D0 >> 2) - (cb >> 2) >= 32) {  // fast path
-        const float* gcol = a.grad_out + coff0 + 4 * c;
+#pragma unroll 2
+      for (int q0 = 0; q0 < n; q0 += UNR) {
+        float4 g[UNR];
 #pragma unroll
-        for (int q0 = 0; q0 < 32; q0 += kRedUnroll) {
-          float4 g[kRedUnroll];
-#pragma unroll
-          for (int uu = 0; uu < kRedUnroll; ++uu)
-            g[uu] = ld_grad(gcol + (int64_t)__shfl_sync(kFull, my_b, q0 + uu) * a.sumD);
-#pragma unroll
-          for (int uu = 0; uu < kRedUnroll; ++uu) {
-            acc.add<W>(uu & 1, g[uu], W ? __shfl_sync(kFull, my_w, q0 + uu) : 1.f);
-            if ((ends >> (q0 + uu)) & 1u) flush(q0 + uu);
-          }
-        }
-      } else {
-        for (int q0 = 0; q0 < n; q0 += kRedUnroll) {
-          float4 g[kRedUnroll];
-#pragma unroll
-          for (int uu = 0; uu < kRedUnroll; ++uu) {
-            const int q = q0 + uu;
+        for (int uu = 0; uu < UNR; ++uu) {
+          const int q = q0 + uu;
+          const int32_t b = __shfl_sync(kFull, my_b, q & 31);
+          int32_t coff = coff0, C4 = D0 >> 2;
+          if (!one_table) {  // uniform branch: the lookup's own table
             const int rr = __shfl_sync(kFull, my_r, q & 31);
-            const int32_t b = __shfl_sync(kFull, my_b, q & 31);
-            const int32_t coff = __shfl_sync(kFull, r.col_off, rr);
-            const int32_t C4 = __shfl_sync(kFull, r.D, rr) >> 2;
-            g[uu] = (q < n && c < C4) ? ld_grad(a.grad_out + (int64_t)b * a.sumD + coff + 4 * c)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            coff = __shfl_sync(kFull, r.col_off, rr);
+            C4 = __shfl_sync(kFull, r.D, rr) >> 2;
           }
+          g[uu] = (q < n && c < C4) ? ld_grad(a.grad_out + (int64_t)b * a.sumD + coff + 4 * c)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-          for (int uu = 0; uu < kRedUnroll; ++uu) {
-            const int q = q0 + uu;
-            if (q >= n) break;
-            acc.add<W>(q & 1, g[uu], W ? __shfl_sync(kFull, my_w, q & 31) : 1.f);
-            if ((ends >> q) & 1u) flush(q);
-          }
+        for (int uu = 0; uu < UNR; ++uu) {
+          acc.add<W>(uu & 1, g[uu], W ? __shfl_sync(kFull, my_w, (q0 + uu) & 31) : 1.f);
+          if ((ends >> (q0 + uu)) & 1u) flush(q0 + uu);
         }
       }
     }
   }
 }
 
-template <bool W>
-__global__ void __launch_bounds__(kRedThreads, 3) reduce_kernel(const RedArgs a) {
+// UNR: grad_out slices in flight per lane; MINB: resident blocks per SM the
+// register budget targets.
+template <bool W, int UNR, int MINB>
+__global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs a) {
   wait_predecessor();
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
-  const int32_t n_items = n_chunks + (U + 31) / 32;
-  while (true) {
-    uint32_t item = 0;
-    if (lane == 0) item = atomicAdd(&a.counters[kCntWork * 2], 1u);
-    item = __shfl_sync(kFull, item, 0);
-    if ((int32_t)item >= n_items) break;
-    if ((int32_t)item < n_chunks) long_chunk<W>(a, (int32_t)item, lane);
-    else short_batch<W>(a, (int32_t)item - n_chunks, U, lane);
+  const int32_t n_items = n_chunks + (int32_t)a.counters[kCntSub * 2];
+  // the next work item is claimed while the current one is reduced
+  uint32_t claim = 0;
+  if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * 2], 1u);
+  uint32_t item = __shfl_sync(kFull, claim, 0);
+  while ((int32_t)item < n_items) {
+    if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * 2], 1u);
+    if ((int32_t)item < n_chunks) {
+      long_chunk<W, UNR>(a, (int32_t)item, lane);
+    } else {
+      const int2 rec = a.sub_list[item - n_chunks];
+      short_batch<W, UNR>(a, rec.x, rec.y, U, lane);
+    }
+    item = __shfl_sync(kFull, claim, 0);
   }
 }
 
@@ -1115,6 +1219,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   ra.T = a.T;
   ra.unique_rows = a.unique_rows;
   ra.run_starts = run_starts;
+  ra.run_table = at<int32_t>(ws, L.run_table);
   ra.lookback = at<uint32_t>(ws, L.rle_lookback);
   ra.tile_counter = at<uint32_t>(ws, L.rle_tile);
   ra.counters = counters;
@@ -1140,7 +1245,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   ca.capacity = a.row_grads_capacity;
   ca.T = a.T;
   ca.tau = tu.long_run_threshold;
-  ca.chunk = tu.long_chunk;
+  ca.chunk = L.chunk;
+  ca.item_lookups = L.item_lookups;
+  ca.sub_list = at<int2>(ws, L.sub_list);
   const int cls_blocks = (int)std::min<int64_t>((N + kClsThreads - 1) / kClsThreads, 4 * sm_count());
   if (launch_pdl(classify_kernel, std::max(cls_blocks, 1), kClsThreads, s, ca)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_classify");
@@ -1152,6 +1259,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.psw_sorted = (a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
   rd.unique_rows = a.unique_rows;
   rd.run_starts = run_starts;
+  rd.run_table = at<int32_t>(ws, L.run_table);
   rd.long_list = at<int4>(ws, L.long_list);
   rd.long_counter = long_counter;
   rd.counters = counters;
@@ -1166,20 +1274,23 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.B = a.B;
   rd.sumD = a.sumD;
   rd.tau = tu.long_run_threshold;
-  rd.chunk = tu.long_chunk;
+  rd.chunk = L.chunk;
+  rd.item_lookups = L.item_lookups;
+  rd.sub_list = at<int2>(ws, L.sub_list);
   rd.slot_floats = L.slot_floats;
-  static int red_grid[2][64] = {{0}};
+  const bool weighted = rd.psw_sorted != nullptr;
+  const bool deep = tu.red_unroll == 8;
+  void (*kern)(RedArgs) = weighted ? (deep ? reduce_kernel<true, 8, 3> : reduce_kernel<true, 4, 4>)
+                                   : (deep ? reduce_kernel<false, 8, 3> : reduce_kernel<false, 4, 4>);
+  static int red_grid[4][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) dev = 63;
-  const bool weighted = rd.psw_sorted != nullptr;
-  if (red_grid[weighted][dev] == 0)
-    red_grid[weighted][dev] =
-        grid_for(weighted ? (const void*)reduce_kernel<true> : (const void*)reduce_kernel<false>, kRedThreads);
+  const int variant = (weighted ? 2 : 0) + (deep ? 1 : 0);
+  if (red_grid[variant][dev] == 0) red_grid[variant][dev] = grid_for((const void*)kern, kRedThreads);
   const int64_t want = ((N + 31) / 32 + 7) / 8 + 1;
-  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[weighted][dev], want));
-  if (launch_pdl(weighted ? reduce_kernel<true> : reduce_kernel<false>, rgrid, kRedThreads, s, rd))
-    return TBE_ERR_CUDA;
+  const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[variant][dev], want));
+  if (launch_pdl(kern, rgrid, kRedThreads, s, rd)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_reduce");
   return TBE_OK;
 }

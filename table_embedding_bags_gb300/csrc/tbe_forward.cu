@@ -11,15 +11,18 @@
 // written as zero; repeated ids are simply added again.
 //
 // Design (GB300): each bag is pooled by a virtual warp (VW) of `lpr` lanes,
-// lpr = the power of two >= the row's 16-byte chunks (16 lanes for a 256-byte
-// fp16 row), so a 32-lane warp pools 32/lpr bags at once without any
-// cross-lane reduction.  The VW fetches lpr ids of its bag with one coalesced
-// load and hands them around with width-limited shuffles, then requests U
-// rows (16-byte loads through the read-only path) before consuming the first,
-// keeping U independent index->row chains per lane in flight (the page's
-// "several chains" idea, widened to a whole warp).  Warp tasks (32/lpr bags
-// of one table) are walked grid-stride by a grid sized to the SM count;
-// uniform layouts get a kernel specialised to their one dtype.
+// lpr = the power of two >= the row's 16-byte chunks, capped at a tunable
+// maximum (8 by default), so a warp pools 32/lpr bags at once without any
+// cross-lane reduction and every lane owns KMAX chunks of the row.  The VW
+// fetches a window of 4*lpr ids of its bag with one coalesced request and
+// hands them around with width-limited shuffles, then requests U rows
+// (16-byte loads through the read-only path, U*KMAX chunks per lane) before
+// consuming the first, keeping many independent index->row chains in flight
+// (the page's "several chains" idea, widened to a whole warp).  Warp tasks
+// (32/lpr bags of one table) are walked grid-stride by a grid sized to the SM
+// count, and the bag bounds of a warp's next task are requested while it
+// pools the current one.  Uniform layouts get a kernel specialised to their
+// one dtype.
 #include <algorithm>
 
 #include "tbe_internal.cuh"
@@ -39,14 +42,36 @@ __device__ __forceinline__ TableMeta load_meta(const TableMeta* p) {
   return m;
 }
 
-// Pools one bag with a virtual warp (VW) of `lpr` lanes: every lane owns
-// KMAX 16-byte chunks of the row, the VW's lanes fetch `lpr` ids of the bag
-// with one coalesced load and hand them around with width-limited
-// shuffles, and U rows are requested before the first is consumed.
-// KMAX: chunks per lane (1 when the row has <= 32 chunks).
-template <int DT, int KMAX, int U, typename OutT>
-__device__ __forceinline__ void pool_bag_vw(const FwdArgs& a, const TableMeta& m, int lpr, int32_t g,
-                                            int b, int lane) {
+constexpr int kIdsPerLane = 4;  // id window of a VW: kIdsPerLane * lpr ids
+
+// One id window of a bag held by the lanes of its VW: lane `sub` holds ids
+// base + sub + k*lpr (k < kIdsPerLane).  Ids outside the table are -1 (rows
+// < 2^31, so every valid id fits 32 bits).
+struct IdWin {
+  int32_t id[kIdsPerLane];
+  float w[kIdsPerLane];
+};
+
+template <bool WT>
+__device__ __forceinline__ void load_window(const FwdArgs& a, const TableMeta& m, int lpr, int sub, int64_t base,
+                                            int nwin, IdWin& iw) {
+  const bool weighted = WT && m.weighted;
+#pragma unroll
+  for (int k = 0; k < kIdsPerLane; ++k) {  // the whole window in one request
+    const int idx = k * lpr + sub;
+    const int64_t raw = idx < nwin ? ld_stream_i64(a.indices + base + idx) : 0;
+    iw.id[k] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
+    iw.w[k] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
+  }
+}
+
+// Pools bag (t, b) = [start, end) with a virtual warp of `lpr` lanes (lsh =
+// log2 lpr).  Lane `sub` owns chunks sub + k*lpr (k < KMAX) of each column
+// block of lpr*KMAX chunks; U rows are requested before the first is used.
+template <int DT, int KMAX, int U, bool WT, typename OutT>
+__device__ __forceinline__ void pool_bag(const FwdArgs& a, const TableMeta& m, int lsh, int b, int lane,
+                                         int64_t start, int64_t end) {
+  const int lpr = 1 << lsh;
   constexpr int E = Chunk<DT>::kElems;           // elements per chunk
   constexpr int NS = (DT == TBE_F32) ? 2 : 1;    // interleaved accumulator sets (fp32 tables)
   const int C = m.D / E;                          // chunks per row
@@ -54,29 +79,13 @@ __device__ __forceinline__ void pool_bag_vw(const FwdArgs& a, const TableMeta& m
   const unsigned vmask = lpr == 32 ? kFull : (((1u << lpr) - 1u) << (lane & ~(lpr - 1)));
   const char* tbl = reinterpret_cast<const char*>(a.weights) + m.w_off;
   const int64_t row_bytes = (int64_t)C * 16;
-  const bool weighted = (a.psw != nullptr) && m.weighted;
+  const bool weighted = WT && m.weighted;  // WT: the call has per-sample weights
   OutT* out_row = reinterpret_cast<OutT*>(a.out) + (int64_t)b * a.sumD + m.col_off;
-  const bool vec = a.out_vec_ok;
+  const int win = kIdsPerLane * lpr;
+  bool bad = false;
 
-  // bag bounds: offsets must start at 0, never decrease and end at N; a
-  // broken bag is reported and pooled as empty (every access stays in [0, N))
-  int64_t o = 0;
-  if (sub < 2 && lpr >= 2) o = ld_stream_i64(a.offsets + g + sub);
-  int64_t start, end;
-  if (lpr >= 2) {
-    start = __shfl_sync(vmask, o, 0, lpr);
-    end = __shfl_sync(vmask, o, 1, lpr);
-  } else {
-    start = ld_stream_i64(a.offsets + g);
-    end = ld_stream_i64(a.offsets + g + 1);
-  }
-  const int32_t nb = a.T * a.B;
-  if (start < 0 || end < start || end > a.N || (g == 0 && start != 0) || (g == nb - 1 && end != a.N)) {
-    if (sub == 0) report(a.status, TBE_DEV_BAD_OFFSETS);
-    start = end = 0;
-  }
-
-  for (int cb = 0; cb < C; cb += 32 * KMAX) {  // column blocks (rows wider than 32*KMAX chunks)
+#pragma unroll 1
+  for (int cb = 0; cb < C; cb += lpr * KMAX) {  // column blocks (wide rows only)
     float acc[NS][KMAX][E];
 #pragma unroll
     for (int s = 0; s < NS; ++s)
@@ -85,26 +94,30 @@ __device__ __forceinline__ void pool_bag_vw(const FwdArgs& a, const TableMeta& m
 #pragma unroll
         for (int e = 0; e < E; ++e) acc[s][k][e] = 0.f;
 
-    for (int64_t base = start; base < end; base += lpr) {
-      const int n = (int)min((int64_t)lpr, end - base);
-      int64_t my_id = 0;
-      float my_w = 1.f;
-      if (sub < n) {
-        my_id = ld_stream_i64(a.indices + base + sub);
-        if (weighted) my_w = ld_stream_f32(a.psw + base + sub);
-      }
-      const bool my_ok = (uint64_t)my_id < (uint64_t)m.rows;
-      if (__any_sync(vmask, sub < n && !my_ok) && sub == 0 && cb == 0) report(a.status, TBE_DEV_BAD_INDEX);
-      for (int j0 = 0; j0 < n; j0 += U) {
+#pragma unroll 1
+    for (int64_t base = start; base < end; base += win) {
+      const int nwin = (int)min((int64_t)win, end - base);
+      IdWin iw;
+      load_window<WT>(a, m, lpr, sub, base, nwin, iw);
+#pragma unroll 1
+      for (int j0 = 0; j0 < nwin; j0 += U) {
         uint4 v[U][KMAX];
         float w[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int j = j0 + u;
-          const int64_t id = __shfl_sync(vmask, my_id, j, lpr);
-          const bool ok = __shfl_sync(vmask, (int)my_ok, j, lpr) && (j < n);
-          w[u] = __shfl_sync(vmask, my_w, j, lpr);
-          const char* row = tbl + id * row_bytes;
+          const int kk = j >> lsh;  // window slot of id j (uniform in the VW)
+          int32_t src = iw.id[0];
+          float wsrc = iw.w[0];
+#pragma unroll
+          for (int k = 1; k < kIdsPerLane; ++k)
+            if (kk == k) { src = iw.id[k]; wsrc = iw.w[k]; }
+          const int32_t id = __shfl_sync(vmask, src, j & (lpr - 1), lpr);
+          w[u] = WT ? __shfl_sync(vmask, wsrc, j & (lpr - 1), lpr) : 1.f;
+          const bool live = j < nwin;
+          const bool ok = live && id >= 0;
+          bad |= live && !ok;  // reported, contributes nothing
+          const char* row = tbl + (int64_t)id * row_bytes;
 #pragma unroll
           for (int k = 0; k < KMAX; ++k) {
             const int c = cb + sub + k * lpr;
@@ -120,7 +133,7 @@ __device__ __forceinline__ void pool_bag_vw(const FwdArgs& a, const TableMeta& m
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               // weighted: the product is rounded to fp32, then added
-              const float term = weighted ? __fmul_rn(w[u], f[e]) : f[e];
+              const float term = (WT && weighted) ? __fmul_rn(w[u], f[e]) : f[e];
               acc[u % NS][k][e] = __fadd_rn(acc[u % NS][k][e], term);
             }
           }
@@ -134,26 +147,32 @@ __device__ __forceinline__ void pool_bag_vw(const FwdArgs& a, const TableMeta& m
         float f[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) f[e] = NS == 2 ? __fadd_rn(acc[0][k][e], acc[NS - 1][k][e]) : acc[0][k][e];
-        store_out<OutT>(out_row + (int64_t)c * E, f, E, vec);
+        store_out<OutT>(out_row + (int64_t)c * E, f, E, a.out_vec_ok);
       }
     }
   }
+  if (bad && sub == 0) report(a.status, TBE_DEV_BAD_INDEX);
 }
 
-template <int DT, int U, typename OutT>
-__device__ __forceinline__ void pool_bag_dt(const FwdArgs& a, const TableMeta& m, int lpr, int32_t g, int b,
-                                            int lane) {
+// One chunk per lane when the row fits the VW, else two (with column blocks
+// for rows wider than 64 chunks); U = R / KMAX rows in flight.
+template <int DT, int R, bool WT, typename OutT>
+__device__ __forceinline__ void pool_bag_dt(const FwdArgs& a, const TableMeta& m, int lsh, int b, int lane,
+                                            int64_t start, int64_t end) {
   constexpr int E = Chunk<DT>::kElems;
-  if (m.D / E <= 32)
-    pool_bag_vw<DT, 1, U, OutT>(a, m, lpr, g, b, lane);
+  if (m.D / E <= (1 << lsh))
+    pool_bag<DT, 1, R, WT, OutT>(a, m, lsh, b, lane, start, end);
   else
-    pool_bag_vw<DT, 2, (U > 1 ? U / 2 : 1), OutT>(a, m, lpr, g, b, lane);
+    pool_bag<DT, 2, (R / 2 > 0 ? R / 2 : 1), WT, OutT>(a, m, lsh, b, lane, start, end);
 }
 
-// lanes per row: the power of two >= the row's 16-byte chunks, capped at 32
-__device__ __forceinline__ int lanes_per_row(const TableMeta& m) {
+// lanes per row: p = the power of two >= the row's 16-byte chunks; a VW has
+// min(p, lpr_max) lanes but at least p/2 (at most two chunks per lane) and
+// at most 32
+__device__ __forceinline__ int lanes_per_row(const TableMeta& m, int lpr_max) {
   const int C = (m.D * (m.dtype == TBE_F32 ? 4 : 2)) >> 4;
-  return C >= 32 ? 32 : (1 << (32 - __clz(C - 1)));
+  const int p = C <= 1 ? 1 : (1 << (32 - __clz(C - 1)));
+  return min(32, max(min(p, lpr_max), p >> 1));
 }
 
 constexpr int kMaxSmemTables = TBE_MAX_TABLES;
@@ -162,10 +181,57 @@ constexpr int kMaxSmemTables = TBE_MAX_TABLES;
 // b = k*G_t .. k*G_t + G_t - 1 with G_t = 32 / lanes_per_row (one bag per
 // virtual warp).  Every block first builds the running task count of the
 // tables in shared memory, then its warps walk the tasks grid-stride.
-// DTSEL: the one table dtype of the layout with rows of <= 32 chunks, or -1
-// for the generic kernel (any dtype, any width).
-template <typename OutT, int U, int DTSEL>
-__global__ void __launch_bounds__(kThreads, 3) fwd_gather_kernel(const FwdArgs a) {
+// DTSEL: the one table dtype of the layout, or -1 for the generic kernel.
+// R: 16-byte row chunks in flight per lane.
+struct Task {
+  int32_t t, b, lsh;
+  bool live;
+};
+
+__device__ __forceinline__ Task locate_task(const FwdArgs& a, const int32_t* s_pref, int32_t ntasks, int32_t task,
+                                            int lane) {
+  Task k;
+  k.live = false;
+  k.t = k.b = k.lsh = 0;
+  if (task >= ntasks) return k;
+  int lo = 0, hi = a.T - 1;  // table of this task: largest t with s_pref[t] <= task
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pref[mid] <= task) lo = mid; else hi = mid - 1;
+  }
+  k.t = lo;
+  k.lsh = 31 - __clz(lanes_per_row(load_meta(a.meta + lo), a.lpr_max));
+  k.b = (task - s_pref[lo]) * (32 >> k.lsh) + (lane >> k.lsh);
+  k.live = k.b < a.B;  // the table's last task may have idle virtual warps
+  return k;
+}
+
+__device__ __forceinline__ void bag_bounds(const FwdArgs& a, const Task& k, int64_t& start, int64_t& end) {
+  const int64_t g = (int64_t)k.t * a.B + k.b;
+  start = ld_stream_i64(a.offsets + g);
+  end = ld_stream_i64(a.offsets + g + 1);
+}
+
+// Offsets must start at 0, never decrease and end at N; a broken bag is
+// reported and pooled as empty (every access stays in [0, N)).
+__device__ __forceinline__ void check_bounds(const FwdArgs& a, const Task& k, int32_t nb, int lane, int64_t& start,
+                                             int64_t& end) {
+  const int32_t g = k.t * a.B + k.b;
+  if (start < 0 || end < start || end > a.N || (g == 0 && start != 0) || (g == nb - 1 && end != a.N)) {
+    if ((lane & ((1 << k.lsh) - 1)) == 0) report(a.status, TBE_DEV_BAD_OFFSETS);
+    start = end = 0;
+  }
+}
+
+// Resident blocks per SM the register budget targets: R = 8 rows in flight
+// per lane needs more registers than three blocks per SM leave.
+template <int R>
+struct MinBlocks {
+  static constexpr int value = R >= 8 ? 2 : 3;
+};
+
+template <typename OutT, int R, int DTSEL, bool WT>
+__global__ void __launch_bounds__(kThreads, MinBlocks<R>::value) fwd_gather_kernel(const FwdArgs a) {
   __shared__ int32_t s_pref[kMaxSmemTables + 1];
   __shared__ int32_t s_part[kThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -177,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 3) fwd_gather_kernel(const FwdArgs a
       const int t = tid * per + q;
       if (t < a.T) {
         const TableMeta m = load_meta(a.meta + t);
-        const int G = 32 / lanes_per_row(m);
+        const int G = 32 / lanes_per_row(m, a.lpr_max);
         mine += (a.B + G - 1) / G;
       }
     }
@@ -197,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 3) fwd_gather_kernel(const FwdArgs a
       if (t < a.T) {
         s_pref[t] = run;
         const TableMeta m = load_meta(a.meta + t);
-        const int G = 32 / lanes_per_row(m);
+        const int G = 32 / lanes_per_row(m, a.lpr_max);
         run += (a.B + G - 1) / G;
       }
     }
@@ -206,31 +272,37 @@ __global__ void __launch_bounds__(kThreads, 3) fwd_gather_kernel(const FwdArgs a
   }
   const int32_t ntasks = s_pref[a.T];
   const int32_t nw = (int32_t)((gridDim.x * kThreads) >> 5);
-  for (int32_t task = (int32_t)((blockIdx.x * kThreads + tid) >> 5); task < ntasks; task += nw) {
-    int lo = 0, hi = a.T - 1;  // table of this task: largest t with s_pref[t] <= task
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_pref[mid] <= task) lo = mid; else hi = mid - 1;
-    }
-    const int t = lo;
-    const TableMeta m = load_meta(a.meta + t);
-    const int lpr = lanes_per_row(m);
-    const int b = (task - s_pref[t]) * (32 / lpr) + lane / lpr;
-    if (b >= a.B) continue;  // the table's last task may have idle virtual warps
-    const int32_t g = t * a.B + b;
-    if (DTSEL >= 0) {
-      pool_bag_vw<(DTSEL < 0 ? 0 : DTSEL), 1, U, OutT>(a, m, lpr, g, b, lane);
-    } else {
-      switch (m.dtype) {
-        case TBE_F32: pool_bag_dt<TBE_F32, U, OutT>(a, m, lpr, g, b, lane); break;
-        case TBE_F16: pool_bag_dt<TBE_F16, U, OutT>(a, m, lpr, g, b, lane); break;
-        default: pool_bag_dt<TBE_BF16, U, OutT>(a, m, lpr, g, b, lane); break;
+  const int32_t nb = a.T * a.B;
+  // the bounds of the warp's next task are requested while this one is pooled
+  int32_t task = (int32_t)((blockIdx.x * kThreads + tid) >> 5);
+  Task cur = locate_task(a, s_pref, ntasks, task, lane);
+  int64_t cs = 0, ce = 0;
+  if (cur.live) bag_bounds(a, cur, cs, ce);
+  while (task < ntasks) {
+    const Task nxt = locate_task(a, s_pref, ntasks, task + nw, lane);
+    int64_t ns = 0, ne = 0;
+    if (nxt.live) bag_bounds(a, nxt, ns, ne);
+    if (cur.live) {
+      check_bounds(a, cur, nb, lane, cs, ce);
+      const TableMeta m = load_meta(a.meta + cur.t);
+      if (DTSEL >= 0) {
+        pool_bag_dt<(DTSEL < 0 ? 0 : DTSEL), R, WT, OutT>(a, m, cur.lsh, cur.b, lane, cs, ce);
+      } else {
+        switch (m.dtype) {
+          case TBE_F32: pool_bag_dt<TBE_F32, R, WT, OutT>(a, m, cur.lsh, cur.b, lane, cs, ce); break;
+          case TBE_F16: pool_bag_dt<TBE_F16, R, WT, OutT>(a, m, cur.lsh, cur.b, lane, cs, ce); break;
+          default: pool_bag_dt<TBE_BF16, R, WT, OutT>(a, m, cur.lsh, cur.b, lane, cs, ce); break;
+        }
       }
     }
+    cur = nxt;
+    cs = ns;
+    ce = ne;
+    task += nw;
   }
 }
 
-template <typename OutT, int U, int DTSEL>
+template <typename OutT, int R, int DTSEL, bool WT>
 int launch_typed(const FwdArgs& a, cudaStream_t s) {
   static int occ[64] = {0};
   int dev = 0;
@@ -238,7 +310,7 @@ int launch_typed(const FwdArgs& a, cudaStream_t s) {
   if (dev >= 64) dev = 63;
   if (occ[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_gather_kernel<OutT, U, DTSEL>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_gather_kernel<OutT, R, DTSEL, WT>, kThreads, 0) !=
             cudaSuccess ||
         n <= 0)
       n = 1;
@@ -249,30 +321,29 @@ int launch_typed(const FwdArgs& a, cudaStream_t s) {
   int64_t want = (nb + (kThreads / 32) - 1) / (kThreads / 32);
   int64_t cap = (int64_t)sm_count() * per_sm;
   int grid = (int)std::max<int64_t>(1, std::min(want, cap));
-  fwd_gather_kernel<OutT, U, DTSEL><<<grid, kThreads, 0, s>>>(a);
+  fwd_gather_kernel<OutT, R, DTSEL, WT><<<grid, kThreads, 0, s>>>(a);
   return check_launch();
 }
 
-template <typename OutT, int DTSEL>
+template <typename OutT, int DTSEL, bool WT>
 int launch_unroll(const FwdArgs& a, cudaStream_t s) {
-  switch (tuning().fwd_unroll) {
-    case 2:
-    case 4: return launch_typed<OutT, 4, DTSEL>(a, s);
-    default: return launch_typed<OutT, 8, DTSEL>(a, s);
-  }
+  if (tuning().fwd_unroll == 4) return launch_typed<OutT, 4, DTSEL, WT>(a, s);
+  return launch_typed<OutT, 8, DTSEL, WT>(a, s);
+}
+
+template <typename OutT, int DTSEL>
+int launch_weighted(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (a.psw != nullptr && p.any_weighted) return launch_unroll<OutT, DTSEL, true>(a, s);
+  return launch_unroll<OutT, DTSEL, false>(a, s);
 }
 
 template <typename OutT>
 int launch_dtsel(const Plan& p, const FwdArgs& a, cudaStream_t s) {
-  // a uniform layout whose rows fit one chunk per lane gets a kernel with
-  // only that dtype's path (fewer live registers, more resident warps)
-  bool narrow = true;
-  for (int t = 0; t < p.T; ++t)
-    if (p.hmeta[t].D * (p.hmeta[t].dtype == TBE_F32 ? 4 : 2) > 512) narrow = false;
-  if (narrow && p.dtype_mask == (1 << TBE_F16)) return launch_unroll<OutT, TBE_F16>(a, s);
-  if (narrow && p.dtype_mask == (1 << TBE_F32)) return launch_unroll<OutT, TBE_F32>(a, s);
-  if (narrow && p.dtype_mask == (1 << TBE_BF16)) return launch_unroll<OutT, TBE_BF16>(a, s);
-  return launch_unroll<OutT, -1>(a, s);
+  // a uniform layout gets a kernel with only that dtype's path
+  if (p.dtype_mask == (1 << TBE_F16)) return launch_weighted<OutT, TBE_F16>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_F32)) return launch_weighted<OutT, TBE_F32>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_BF16)) return launch_weighted<OutT, TBE_BF16>(p, a, s);
+  return launch_weighted<OutT, -1>(p, a, s);
 }
 
 }  // namespace

@@ -53,6 +53,9 @@ struct Tuning {
   int32_t fwd_unroll;
   int32_t fwd_blocks_per_sm;
   int32_t hist_min_mean_bag;
+  int32_t short_item_lookups;
+  int32_t fwd_lanes_per_row;
+  int32_t red_unroll;
 };
 const Tuning& tuning();
 
@@ -198,6 +201,7 @@ struct FwdArgs {
   int64_t N;
   int32_t sumD;
   int32_t out_vec_ok;
+  int32_t lpr_max;  // lanes per row cap of the gather (a power of two <= 32)
 };
 
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s);

@@ -42,7 +42,7 @@ def test_host_only_calls(lib):
     assert lib.tbe_status_string(tbe.TBE_ERR_WORKSPACE) == b"workspace too small"
     assert b"sm_103a" in lib.tbe_version()
     t = tbe.get_tuning()
-    assert t["long_run_threshold"] >= 1 and t["fwd_unroll"] in (2, 4, 8)
+    assert t["long_run_threshold"] >= 1 and t["fwd_unroll"] in (4, 8)
     with pytest.raises(tbe.TBEError):
         tbe.set_tuning(fwd_unroll=3)
     with pytest.raises(tbe.TBEError):

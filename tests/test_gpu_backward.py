@@ -82,6 +82,16 @@ def test_tiers_and_thresholds(tbe, tuned, tau, chunk):
     check_backward(tbe, make_config("mid_skewed", B=256))
 
 
+@pytest.mark.parametrize("unroll", [4, 8])
+@pytest.mark.parametrize("item", [32, 40, 64, 1000])
+def test_reduce_variants(tbe, tuned, unroll, item):
+    """Both reduction kernels (4 or 8 slices in flight per lane) and short-run
+    work items from one part per batch to many, weighted and unweighted."""
+    tuned(red_unroll=unroll, short_item_lookups=item)
+    check_backward(tbe, make_config("mixed", B=200, rows_scale=0.01))
+    check_backward(tbe, make_config("mid_skewed", B=300))
+
+
 def test_deterministic_bits(tbe, tuned):
     tuned(long_run_threshold=16, long_chunk=32)
     p = make_config("bwd_skew", B=300, rows_scale=0.01)

@@ -76,6 +76,29 @@ def test_shapes_and_dtypes(tbe, out_dt, weighted):
     check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
 
 
+@pytest.mark.parametrize("out_dt", [DT_F32, DT_F16, DT_BF16])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_narrow_rows_long_bags(tbe, out_dt, weighted):
+    """Rows of 16..512 bytes in every dtype, a row width that is not a power
+    of two chunks, bags longer than several id windows, empty bags."""
+    rng = np.random.default_rng(300 + out_dt * 2 + weighted)
+    specs = [(DT_F32, 4), (DT_F32, 16), (DT_F32, 128), (DT_F16, 8), (DT_F16, 24), (DT_F16, 256),
+             (DT_BF16, 64), (DT_BF16, 128), (DT_BF16, 256), (DT_F32, 36)]
+    T, B = len(specs), 45
+    rows = rng.integers(1, 2000, size=T)
+    lens = rng.integers(0, 70, size=(T, B))
+    lens[:, 7] = 0
+    lens[1, 3] = 300
+    lens[5, 44] = 97
+    ids = [rng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
+    N = int(lens.sum())
+    psw = rng.random(N).astype(np.float32) if weighted else None
+    tw = (np.arange(T) % 3 != 0).astype(np.uint8) if weighted else None
+    p = make_problem(T, B, rows=rows, D=[d for _, d in specs], weights_dtype=[s for s, _ in specs],
+                     out_dtype=out_dt, lengths=lens, ids=ids, psw=psw, table_weighted=tw, seed=98)
+    check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
+
+
 def test_repeated_ids_and_empty(tbe):
     p = make_problem(2, 3, rows=[5, 7], D=[8, 4], weights_dtype=[DT_F16, DT_F32], out_dtype=DT_F32,
                      lengths=[[0, 40, 1], [3, 0, 0]], ids=[[2] * 40 + [4], [6, 6, 0]])
@@ -127,11 +150,11 @@ def test_deterministic(tbe):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("unroll", [2, 4, 8])
-def test_unroll_variants(tbe, unroll):
+@pytest.mark.parametrize("unroll,lpr", [(4, 8), (8, 8), (8, 4), (8, 16), (4, 32), (8, 1), (4, 2)])
+def test_unroll_variants(tbe, unroll, lpr):
     old = tbe.get_tuning()
     try:
-        tbe.set_tuning(fwd_unroll=unroll)
+        tbe.set_tuning(fwd_unroll=unroll, fwd_lanes_per_row=lpr)
         p = make_config("mixed", B=64, rows_scale=0.005)
         check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
     finally:
