@@ -44,17 +44,12 @@ constexpr unsigned kFull = 0xffffffffu;
 // tile sizes and look-back flags
 // ---------------------------------------------------------------------------
 constexpr int kLinThreads = 256;
-constexpr int kLinTile = 2048;       // positions per linearize block
-constexpr int kLinOffs = 2048;       // bag offsets staged in shared memory
+constexpr int kLinOffs = 2048;       // bag offsets staged in shared memory (>= the largest tile)
 
 constexpr int kSortThreads = 256;
 constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortIPT = 12;         // keys per thread
-constexpr int kSortTile = kSortThreads * kSortIPT;
 
 constexpr int kRleThreads = 256;
-constexpr int kRleIPT = 8;
-constexpr int kRleTile = kRleThreads * kRleIPT;
 
 constexpr int kClsThreads = 256;
 constexpr int kRedThreads = 256;
@@ -152,6 +147,14 @@ __device__ __forceinline__ uint32_t lookback_block(const uint32_t* words, int32_
 // its writes are visible (a no-op for a kernel launched without the attribute).
 __device__ __forceinline__ void wait_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the next kernel in the stream be scheduled once every block of this
+// one has started: its blocks then wait in wait_predecessor() for this grid
+// to finish instead of being launched after it, which hides the launch gap.
+// Correctness does not depend on it (the wait covers completion and memory).
+__device__ __forceinline__ void release_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T, int64_t row) {
   int lo = 0, hi = T - 1;  // largest t with row_base[t] <= row
   while (lo < hi) {
@@ -169,7 +172,8 @@ struct Layout {
   size_t zero_begin, hist, sort_tiles, rle_tile, counters, zero_end;
   size_t lin_zero_begin, sort_lookback, rle_lookback, combine, lin_zero_end;
   size_t total;
-  int npass, sort_ntiles, rle_ntiles;
+  int npass, sort_ntiles, rle_ntiles, lin_blocks;
+  bool small;  // few tiles per SM: the kernels use half-size tiles
   int64_t long_cap, chunk_cap, sub_cap;
   int32_t slot_floats, item_lookups, chunk;
 };
@@ -193,8 +197,15 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   Layout L{};
   const Tuning& tu = tuning();
   L.npass = (p.key_bits + 7) / 8;
-  L.sort_ntiles = (int)((N + kSortTile - 1) / kSortTile);
-  L.rle_ntiles = (int)((N + kRleTile - 1) / kRleTile);
+  // a batch that gives the big tiles fewer than two per SM uses half-size
+  // tiles, so more SMs (and more warps per SM) take part
+  L.small = N < (int64_t)2 * sm_count() * kSortThreads * 12;
+  const int sort_tile = kSortThreads * (L.small ? 6 : 12);
+  const int lin_tile = kLinThreads * (L.small ? 4 : 8);
+  const int rle_tile = kRleThreads * (L.small ? 4 : 8);
+  L.sort_ntiles = (int)((N + sort_tile - 1) / sort_tile);
+  L.rle_ntiles = (int)((N + rle_tile - 1) / rle_tile);
+  L.lin_blocks = (int)((N + lin_tile - 1) / lin_tile);
   const int64_t tau = std::max(1, tu.long_run_threshold);
   L.chunk = effective_chunk(tu, N);
   const int64_t C = L.chunk;
@@ -288,7 +299,10 @@ __device__ __forceinline__ int32_t bag_search_warp(const int64_t* offsets, int32
   return lo;
 }
 
+template <int IPT>
 __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a) {
+  constexpr int kLinTile = kLinThreads * IPT;
+  release_dependents();
   __shared__ uint32_t s_hist[4][256];
   __shared__ int64_t s_off[kLinOffs];
   __shared__ int32_t s_g0, s_ng;
@@ -318,7 +332,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
   __syncthreads();
   int bad = 0, invalid = 0;
-  constexpr int kIPT = kLinTile / kLinThreads;
+  constexpr int kIPT = IPT;
   int64_t id[kIPT];
 #pragma unroll
   for (int q = 0; q < kIPT; ++q) {  // all of this thread's ids are requested first
@@ -386,8 +400,12 @@ struct SortArgs {
   int32_t shift;
 };
 
+template <int IPT>
 __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortArgs a) {
+  constexpr int kSortIPT = IPT;
+  constexpr int kSortTile = kSortThreads * IPT;
   wait_predecessor();
+  release_dependents();
   __shared__ uint32_t s_wcnt[kSortWarps][256];
   __shared__ uint32_t s_start[256];   // tile-local first slot of each digit
   __shared__ int32_t s_gbase[256];    // global position of slot 0 of each digit, minus s_start
@@ -574,8 +592,12 @@ struct RleArgs {
   uint32_t sentinel;
 };
 
+template <int IPT>
 __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
+  constexpr int kRleIPT = IPT;
+  constexpr int kRleTile = kRleThreads * IPT;
   wait_predecessor();
+  release_dependents();
   __shared__ uint32_t s_scan[kRleThreads / 32];
   __shared__ uint32_t s_lb[2 * (kRleThreads / 32)];
   __shared__ uint32_t s_excl;
@@ -686,6 +708,7 @@ struct ClsArgs {
 
 __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) {
   wait_predecessor();
+  release_dependents();
   __shared__ uint32_t s_scan[3][kClsThreads / 32];
   __shared__ unsigned long long s_base;
   __shared__ uint32_t s_sub_base;
@@ -831,6 +854,15 @@ struct Acc {
                        __fadd_rn(v[0].w, v[1].w));
   }
 };
+
+// acc += w * g (weighted: the product is rounded to fp32, then added)
+template <bool W>
+__device__ __forceinline__ void add_slice(float4& acc, const float4& g, float w) {
+  acc.x = __fadd_rn(acc.x, W ? __fmul_rn(w, g.x) : g.x);
+  acc.y = __fadd_rn(acc.y, W ? __fmul_rn(w, g.y) : g.y);
+  acc.z = __fadd_rn(acc.z, W ? __fmul_rn(w, g.z) : g.z);
+  acc.w = __fadd_rn(acc.w, W ? __fmul_rn(w, g.w) : g.w);
+}
 
 __device__ __forceinline__ float4 ld_grad(const float* p) {
   return __ldg(reinterpret_cast<const float4*>(p));
@@ -1020,8 +1052,8 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
 
   for (int cb = 0; cb < maxD; cb += kColsPerPass) {
     const int c = (cb >> 2) + lane;
-    Acc acc;
-    acc.zero();
+    // one accumulator: short runs are short chains of additions
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     // run, bag and weight of flattened lookup f = fb + lane, and whether it
     // is the last lookup of its run
     auto fetch = [&](int32_t fb, int& my_r, int32_t& my_b, float& my_w, bool& my_end) {
@@ -1054,8 +1086,8 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
         const int rr = __shfl_sync(kFull, my_r, q);
         const int64_t off = __shfl_sync(kFull, r.out_off, rr);
         const int32_t c4 = __shfl_sync(kFull, st_c4, rr);
-        if (c < c4) *reinterpret_cast<float4*>(a.row_grads + off + 4 * c) = acc.sum();
-        acc.zero();
+        if (c < c4) *reinterpret_cast<float4*>(a.row_grads + off + 4 * c) = acc;
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
       };
 #pragma unroll 2
       for (int q0 = 0; q0 < n; q0 += UNR) {
@@ -1075,7 +1107,7 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
         }
 #pragma unroll
         for (int uu = 0; uu < UNR; ++uu) {
-          acc.add<W>(uu & 1, g[uu], W ? __shfl_sync(kFull, my_w, (q0 + uu) & 31) : 1.f);
+          add_slice<W>(acc, g[uu], W ? __shfl_sync(kFull, my_w, (q0 + uu) & 31) : 1.f);
           if ((ends >> (q0 + uu)) & 1u) flush(q0 + uu);
         }
       }
@@ -1088,6 +1120,7 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
 template <bool W, int UNR, int MINB>
 __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs a) {
   wait_predecessor();
+  release_dependents();
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * 2];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
@@ -1174,8 +1207,10 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   la.B = a.B;
   la.npass = L.npass;
   la.sentinel = sentinel;
-  const int lin_blocks = (int)((N + kLinTile - 1) / kLinTile);
-  linearize_kernel<<<lin_blocks, kLinThreads, 0, s>>>(la);
+  if (L.small)
+    linearize_kernel<4><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
+  else
+    linearize_kernel<8><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
   if (check_launch()) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_linearize");
 
@@ -1204,7 +1239,8 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
     sa.N = (int32_t)N;
     sa.shift = 8 * pass;
-    if (launch_pdl(sort_pass_kernel, L.sort_ntiles, kSortThreads, s, sa)) return TBE_ERR_CUDA;
+    if (launch_pdl(L.small ? sort_pass_kernel<6> : sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s, sa))
+      return TBE_ERR_CUDA;
     trace_mark(s, "bwd_sort_pass");
     std::swap(kin, kout);
     vin = vout;
@@ -1227,7 +1263,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   ra.N = (int32_t)N;
   ra.ntiles = L.rle_ntiles;
   ra.sentinel = sentinel;
-  if (launch_pdl(rle_kernel, L.rle_ntiles, kRleThreads, s, ra)) return TBE_ERR_CUDA;
+  if (launch_pdl(L.small ? rle_kernel<4> : rle_kernel<8>, L.rle_ntiles, kRleThreads, s, ra)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_rle");
 
   const Tuning& tu = tuning();

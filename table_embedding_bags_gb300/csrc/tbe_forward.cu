@@ -99,42 +99,41 @@ __device__ __forceinline__ void pool_bag(const FwdArgs& a, const TableMeta& m, i
       const int nwin = (int)min((int64_t)win, end - base);
       IdWin iw;
       load_window<WT>(a, m, lpr, sub, base, nwin, iw);
+#pragma unroll
+      for (int slot = 0; slot < kIdsPerLane; ++slot) {  // window slot: ids slot*lpr .. slot*lpr + lpr - 1
+        const int n = min(lpr, nwin - slot * lpr);
+        if (n <= 0) break;
 #pragma unroll 1
-      for (int j0 = 0; j0 < nwin; j0 += U) {
-        uint4 v[U][KMAX];
-        float w[U];
+        for (int j0 = 0; j0 < n; j0 += U) {
+          uint4 v[U][KMAX];
+          float w[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = j0 + u;
-          const int kk = j >> lsh;  // window slot of id j (uniform in the VW)
-          int32_t src = iw.id[0];
-          float wsrc = iw.w[0];
+          for (int u = 0; u < U; ++u) {
+            const int j = j0 + u;
+            const int32_t id = __shfl_sync(vmask, iw.id[slot], j & (lpr - 1), lpr);
+            w[u] = WT ? __shfl_sync(vmask, iw.w[slot], j & (lpr - 1), lpr) : 1.f;
+            const bool live = j < n;
+            const bool ok = live && id >= 0;
+            bad |= live && !ok;  // reported, contributes nothing
+            const char* row = tbl + (int64_t)id * row_bytes;
 #pragma unroll
-          for (int k = 1; k < kIdsPerLane; ++k)
-            if (kk == k) { src = iw.id[k]; wsrc = iw.w[k]; }
-          const int32_t id = __shfl_sync(vmask, src, j & (lpr - 1), lpr);
-          w[u] = WT ? __shfl_sync(vmask, wsrc, j & (lpr - 1), lpr) : 1.f;
-          const bool live = j < nwin;
-          const bool ok = live && id >= 0;
-          bad |= live && !ok;  // reported, contributes nothing
-          const char* row = tbl + (int64_t)id * row_bytes;
-#pragma unroll
-          for (int k = 0; k < KMAX; ++k) {
-            const int c = cb + sub + k * lpr;
-            v[u][k] = (ok && c < C) ? ld_row16(row + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < KMAX; ++k) {
+              const int c = cb + sub + k * lpr;
+              v[u][k] = (ok && c < C) ? ld_row16(row + (int64_t)c * 16) : make_uint4(0, 0, 0, 0);
+            }
           }
-        }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
+          for (int u = 0; u < U; ++u) {
 #pragma unroll
-          for (int k = 0; k < KMAX; ++k) {
-            float f[E];
-            Chunk<DT>::to_float(v[u][k], f);
+            for (int k = 0; k < KMAX; ++k) {
+              float f[E];
+              Chunk<DT>::to_float(v[u][k], f);
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              // weighted: the product is rounded to fp32, then added
-              const float term = (WT && weighted) ? __fmul_rn(w[u], f[e]) : f[e];
-              acc[u % NS][k][e] = __fadd_rn(acc[u % NS][k][e], term);
+              for (int e = 0; e < E; ++e) {
+                // weighted: the product is rounded to fp32, then added
+                const float term = (WT && weighted) ? __fmul_rn(w[u], f[e]) : f[e];
+                acc[u % NS][k][e] = __fadd_rn(acc[u % NS][k][e], term);
+              }
             }
           }
         }
