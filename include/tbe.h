@@ -229,7 +229,8 @@ int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, c
  *   red_unroll         : gradient slices in flight per lane in the backward
  *                        reduction (4: more resident warps, 8: deeper)
  *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
- *                        many as fit)
+ *                        many as fit; 4 with fwd_unroll 4 selects a build
+ *                        of the kernel with a smaller register budget)
  *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
  *                        N / B reaches this
  *   short_item_lookups : lookups per work item of the short-run tier (runs

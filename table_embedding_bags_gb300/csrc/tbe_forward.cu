@@ -222,15 +222,11 @@ __device__ __forceinline__ void check_bounds(const FwdArgs& a, const Task& k, in
   }
 }
 
-// Resident blocks per SM the register budget targets: R = 8 rows in flight
-// per lane needs more registers than three blocks per SM leave.
-template <int R>
-struct MinBlocks {
-  static constexpr int value = R >= 8 ? 2 : 3;
-};
-
-template <typename OutT, int R, int DTSEL, bool WT>
-__global__ void __launch_bounds__(kThreads, MinBlocks<R>::value) fwd_gather_kernel(const FwdArgs a) {
+// MINB: resident blocks per SM the register budget targets (R = 8 rows in
+// flight per lane needs the registers of two blocks per SM; R = 4 fits three,
+// or four with a few values kept in local memory).
+template <typename OutT, int R, int DTSEL, bool WT, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB) fwd_gather_kernel(const FwdArgs a) {
   __shared__ int32_t s_pref[kMaxSmemTables + 1];
   __shared__ int32_t s_part[kThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -301,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, MinBlocks<R>::value) fwd_gather_kern
   }
 }
 
-template <typename OutT, int R, int DTSEL, bool WT>
+template <typename OutT, int R, int DTSEL, bool WT, int MINB>
 int launch_typed(const FwdArgs& a, cudaStream_t s) {
   static int occ[64] = {0};
   int dev = 0;
@@ -309,7 +305,7 @@ int launch_typed(const FwdArgs& a, cudaStream_t s) {
   if (dev >= 64) dev = 63;
   if (occ[dev] == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_gather_kernel<OutT, R, DTSEL, WT>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_gather_kernel<OutT, R, DTSEL, WT, MINB>, kThreads, 0) !=
             cudaSuccess ||
         n <= 0)
       n = 1;
@@ -320,14 +316,15 @@ int launch_typed(const FwdArgs& a, cudaStream_t s) {
   int64_t want = (nb + (kThreads / 32) - 1) / (kThreads / 32);
   int64_t cap = (int64_t)sm_count() * per_sm;
   int grid = (int)std::max<int64_t>(1, std::min(want, cap));
-  fwd_gather_kernel<OutT, R, DTSEL, WT><<<grid, kThreads, 0, s>>>(a);
+  fwd_gather_kernel<OutT, R, DTSEL, WT, MINB><<<grid, kThreads, 0, s>>>(a);
   return check_launch();
 }
 
 template <typename OutT, int DTSEL, bool WT>
 int launch_unroll(const FwdArgs& a, cudaStream_t s) {
-  if (tuning().fwd_unroll == 4) return launch_typed<OutT, 4, DTSEL, WT>(a, s);
-  return launch_typed<OutT, 8, DTSEL, WT>(a, s);
+  if (tuning().fwd_unroll == 8) return launch_typed<OutT, 8, DTSEL, WT, 2>(a, s);
+  if (tuning().fwd_blocks_per_sm >= 4) return launch_typed<OutT, 4, DTSEL, WT, 4>(a, s);
+  return launch_typed<OutT, 4, DTSEL, WT, 3>(a, s);
 }
 
 template <typename OutT, int DTSEL>

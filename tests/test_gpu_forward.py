@@ -150,11 +150,12 @@ def test_deterministic(tbe):
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-@pytest.mark.parametrize("unroll,lpr", [(4, 8), (8, 8), (8, 4), (8, 16), (4, 32), (8, 1), (4, 2)])
-def test_unroll_variants(tbe, unroll, lpr):
+@pytest.mark.parametrize("unroll,lpr,per_sm", [(4, 8, 0), (8, 8, 0), (8, 4, 0), (8, 16, 0), (4, 32, 0), (8, 1, 0),
+                                            (4, 2, 0), (4, 16, 4), (4, 8, 4)])
+def test_unroll_variants(tbe, unroll, lpr, per_sm):
     old = tbe.get_tuning()
     try:
-        tbe.set_tuning(fwd_unroll=unroll, fwd_lanes_per_row=lpr)
+        tbe.set_tuning(fwd_unroll=unroll, fwd_lanes_per_row=lpr, fwd_blocks_per_sm=per_sm)
         p = make_config("mixed", B=64, rows_scale=0.005)
         check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
     finally:
