@@ -237,6 +237,11 @@ int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, 
   int kb = 1;
   while (kb < 32 && (total_rows >> kb) != 0) ++kb;
   p->key_bits = kb;
+  int64_t max_rows = 0;
+  for (int32_t t = 0; t < T; ++t) max_rows = std::max<int64_t>(max_rows, p->hmeta[t].rows);
+  int sb = 1;
+  while (sb < 32 && (max_rows >> sb) != 0) ++sb;
+  p->seg_bits = sb;
   p->dtype_mask = dtype_mask;
   p->any_weighted = any_weighted;
   if (((int64_t)p->sumD * osz) % 16 != 0) out_vec_ok = 0;

@@ -47,6 +47,8 @@ constexpr int kLinThreads = 256;
 constexpr int kLinOffs = 2048;       // bag offsets staged in shared memory (>= the largest tile)
 
 constexpr int kSortThreads = 256;
+constexpr int kSegMaxT = 64;         // segmented sort: most tables
+constexpr int kSegBk = 512;          // segmented sort: buckets per pass (digits of up to 9 bits)
 constexpr int kSortWarps = kSortThreads / 32;
 
 constexpr int kRleThreads = 256;
@@ -174,6 +176,8 @@ struct Layout {
   size_t total;
   int npass, sort_ntiles, rle_ntiles, lin_blocks;
   bool small;  // few tiles per SM: the kernels use half-size tiles
+  int seg_dbits;  // > 0: segmented sort in two passes of this many bits
+  size_t seg_hist, seg_inv;
   int64_t long_cap, chunk_cap, sub_cap;
   int32_t slot_floats, item_lookups, chunk;
 };
@@ -197,6 +201,9 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   Layout L{};
   const Tuning& tu = tuning();
   L.npass = (p.key_bits + 7) / 8;
+  // few tables whose ids need at most 18 bits: two passes over ids within
+  // each table replace the passes over global rows
+  L.seg_dbits = (p.T < kSegMaxT && p.seg_bits <= 18 && L.npass > 2) ? (p.seg_bits + 1) / 2 : 0;
   // a batch that gives the big tiles fewer than two per SM uses half-size
   // tiles, so more SMs (and more warps per SM) take part
   L.small = N < (int64_t)2 * sm_count() * kSortThreads * 12;
@@ -204,6 +211,10 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   const int lin_tile = kLinThreads * (L.small ? 4 : 8);
   const int rle_tile = kRleThreads * (L.small ? 4 : 8);
   L.sort_ntiles = (int)((N + sort_tile - 1) / sort_tile);
+  if (L.seg_dbits > 0) {  // tiles never span tables: at most one partial tile per table more
+    L.npass = 2;
+    L.sort_ntiles += p.T;
+  }
   L.rle_ntiles = (int)((N + rle_tile - 1) / rle_tile);
   L.lin_blocks = (int)((N + lin_tile - 1) / lin_tile);
   const int64_t tau = std::max(1, tu.long_run_threshold);
@@ -232,12 +243,14 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.partials = take(4 * (size_t)L.chunk_cap * L.slot_floats);
   L.zero_begin = off;  // cleared by a memset before the first kernel
   L.hist = take(4 * 4 * 256);
+  L.seg_hist = take(L.seg_dbits > 0 ? 4 * (size_t)p.T * 2 * kSegBk : 0);
+  L.seg_inv = take(L.seg_dbits > 0 ? 4 * (size_t)p.T : 0);
   L.sort_tiles = take(4 * 4);
   L.rle_tile = take(4);
   L.counters = take(8 * kNumCounters);
   L.zero_end = off;
   L.lin_zero_begin = off;  // cleared by the linearize kernel
-  L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * 256);
+  L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * (L.seg_dbits > 0 ? kSegBk : 256));
   L.rle_lookback = take(4 * (size_t)L.rle_ntiles);
   L.combine = take(4 * (size_t)L.chunk_cap);
   L.lin_zero_end = off;
@@ -267,6 +280,11 @@ struct LinArgs {
   int64_t N;
   int32_t T, B, npass;
   uint32_t sentinel;   // total_rows
+  // segmented sort (seg_dbits > 0): keys are ids within their table (an id
+  // outside the table becomes rows_t), digit counts are per table
+  int32_t seg_dbits;
+  uint32_t* seg_hist;  // [T][2][kSegBk]
+  uint32_t* seg_inv;   // [T] ids outside their table
 };
 
 // largest g in [lo, hi] with offsets[g] <= pos (global memory)
@@ -306,9 +324,11 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   __shared__ uint32_t s_hist[4][256];
   __shared__ int64_t s_off[kLinOffs];
   __shared__ int32_t s_g0, s_ng;
+  __shared__ uint32_t s_inv;
   const int tid = threadIdx.x, lane = tid & 31;
   const int32_t nb = a.T * a.B;
   for (int k = tid; k < 4 * 256; k += kLinThreads) (&s_hist[0][0])[k] = 0;
+  if (tid == 0) s_inv = 0;
   // clear the look-back words and combine counters the later kernels use
   {
     const int64_t gtid = (int64_t)blockIdx.x * kLinThreads + tid;
@@ -327,6 +347,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   if (tid == 0) s_ng = max(s_ng - s_g0 + 1, 1);
   __syncthreads();
   const int32_t g0 = s_g0, ng = s_ng;
+  const int32_t t_first = g0 / max(a.B, 1);
   const bool staged = ng <= kLinOffs;
   if (staged)
     for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
@@ -357,12 +378,28 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     const int32_t t = g / a.B;
     const int32_t b = g - t * a.B;
     const int32_t rows = __ldg(&a.meta[t].rows);
-    uint32_t key = a.sentinel;
-    if ((uint64_t)id[q] < (uint64_t)rows) key = (uint32_t)(__ldg(&a.meta[t].row_base) + id[q]);
-    else { bad = 1; ++invalid; }
+    const bool valid = (uint64_t)id[q] < (uint64_t)rows;
+    if (!valid) { bad = 1; ++invalid; }
+    uint32_t key;
+    if (a.seg_dbits > 0) {
+      key = valid ? (uint32_t)id[q] : (uint32_t)rows;
+      const uint32_t dm = (1u << a.seg_dbits) - 1u;
+      if (t == t_first) {  // the block's first table is counted in shared memory
+        uint32_t* sh = &s_hist[0][0];  // two 512-bucket histograms back to back
+        atomicAdd(&sh[key & dm], 1u);
+        atomicAdd(&sh[kSegBk + ((key >> a.seg_dbits) & dm)], 1u);
+        if (!valid) atomicAdd(&s_inv, 1u);
+      } else {
+        atomicAdd(&a.seg_hist[(size_t)t * 2 * kSegBk + (key & dm)], 1u);
+        atomicAdd(&a.seg_hist[((size_t)t * 2 + 1) * kSegBk + ((key >> a.seg_dbits) & dm)], 1u);
+        if (!valid) atomicAdd(&a.seg_inv[t], 1u);
+      }
+    } else {
+      key = valid ? (uint32_t)(__ldg(&a.meta[t].row_base) + id[q]) : a.sentinel;
+      for (int p = 0; p < a.npass; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xffu], 1u);
+    }
     a.keys[i] = key;
     a.bag_of[i] = b;
-    for (int p = 0; p < a.npass; ++p) atomicAdd(&s_hist[p][(key >> (8 * p)) & 0xffu], 1u);
   }
   // offsets must start at 0, never decrease and end at N
   const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
@@ -374,9 +411,17 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   if (bad & 2) report(a.status, TBE_DEV_BAD_OFFSETS);
   if (invalid) atomicAdd(&a.counters[kCntInvalid * 2], (uint32_t)invalid);
   __syncthreads();
-  for (int k = tid; k < a.npass * 256; k += kLinThreads) {
-    const uint32_t c = (&s_hist[0][0])[k];
-    if (c) atomicAdd(&a.hist[k], c);
+  if (a.seg_dbits > 0) {  // s_hist holds the two 512-bucket histograms of t_first back to back
+    for (int k = tid; k < 2 * kSegBk; k += kLinThreads) {
+      const uint32_t c = (&s_hist[0][0])[k];
+      if (c) atomicAdd(&a.seg_hist[(size_t)t_first * 2 * kSegBk + k], c);
+    }
+    if (tid == 0 && s_inv) atomicAdd(&a.seg_inv[t_first], s_inv);
+  } else {
+    for (int k = tid; k < a.npass * 256; k += kLinThreads) {
+      const uint32_t c = (&s_hist[0][0])[k];
+      if (c) atomicAdd(&a.hist[k], c);
+    }
   }
 }
 
@@ -543,6 +588,266 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
       a.keys_out[dst] = k;
       a.vals_out[dst] = v;
       if (a.bag_sorted) {  // carry each lookup's bag and weight through the same order
+        a.bag_sorted[dst] = __ldg(a.bag_of + v);
+        if (a.psw_sorted) a.psw_sorted[dst] = __ldg(a.psw + v);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2b. segmented radix pass (few tables of at most 2^18 rows)
+// ---------------------------------------------------------------------------
+// The lookups of table t are the contiguous range [offsets[t*B],
+// offsets[(t+1)*B]) and their keys the contiguous range of rows of table t,
+// so sorting every table's range by id sorts the whole batch.  Ids need
+// fewer bits than global rows (17 instead of 20 for 8 tables of 100 K rows),
+// which makes two passes of up to 9 bits enough, and a tile's look-back stops
+// at the first tile of its table.  An id outside its table has key rows_t and
+// sorts to the end of its table; the last pass moves those lookups behind all
+// valid ones (in position order, as the global sort with its sentinel does)
+// and writes the global key table_row_base[t] + id (or the sentinel).
+struct SegSortArgs {
+  const uint32_t* keys_in;  // ids within the table
+  const int32_t* vals_in;   // nullptr: values are the positions themselves
+  uint32_t* keys_out;
+  int32_t* vals_out;
+  const uint32_t* hist;     // [T][2][kSegBk] digit counts per table
+  const uint32_t* inv;      // [T] ids outside their table
+  const int64_t* offsets;
+  const TableMeta* meta;
+  uint32_t* lookback;       // [tiles][kSegBk] of this pass
+  uint32_t* tile_counter;
+  int32_t* status;
+  const int32_t* bag_of;    // last pass only
+  const float* psw;
+  int32_t* bag_sorted;
+  float* psw_sorted;
+  int32_t N, T, B, pass, dbits, last;
+  uint32_t sentinel;        // total_rows
+};
+
+// Inclusive scan over the 256 threads of a block (one value each); `s_w` is
+// 8 words of shared scratch.  Returns the inclusive prefix, `total` gets the
+// block total.  Every thread must call it.
+__device__ __forceinline__ uint32_t block_scan256(uint32_t x, uint32_t* s_w, uint32_t& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_w[warp] = x;
+  __syncthreads();
+  uint32_t before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kSortWarps; ++w) {
+    const uint32_t v = s_w[w];
+    before += w < warp ? v : 0u;
+    total += v;
+  }
+  __syncthreads();  // s_w is reused by the caller's next scan
+  return before + x;
+}
+
+template <int IPT>
+__global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const SegSortArgs a) {
+  constexpr int kTile = kSortThreads * IPT;
+  wait_predecessor();
+  release_dependents();
+  __shared__ uint32_t s_wcnt[kSortWarps][kSegBk];
+  __shared__ uint32_t s_start[kSegBk];  // tile-local first slot of each digit
+  __shared__ int32_t s_gbase[kSegBk];   // table-local position of slot 0 of each digit, minus s_start
+  __shared__ uint32_t s_keys[kTile];
+  __shared__ int32_t s_vals[kTile];
+  __shared__ uint32_t s_w[kSortWarps];
+  __shared__ int64_t s_P[kSegMaxT + 1];  // first lookup of each table
+  __shared__ int32_t s_tp[kSegMaxT + 1]; // first tile of each table
+  __shared__ int32_t s_ip[kSegMaxT + 1]; // ids outside their table before each table
+  __shared__ int32_t s_tile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
+  for (int k = tid; k < kSortWarps * kSegBk; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
+  // table ranges, clamped so that broken offsets still give ranges inside [0, N)
+  if (tid <= a.T) {
+    int64_t P = __ldg(a.offsets + (int64_t)tid * a.B);
+    s_P[tid] = min(max(P, (int64_t)0), (int64_t)a.N);
+  }
+  __syncthreads();
+  if (warp == 0) {  // tiles and invalid ids per table, two tables per lane
+    int32_t nt[2], iv[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = 2 * lane + h;
+      const int64_t n = t < a.T ? max(s_P[t + 1] - s_P[t], (int64_t)0) : 0;
+      nt[h] = (int32_t)((n + kTile - 1) / kTile);
+      iv[h] = t < a.T ? (int32_t)__ldg(a.inv + t) : 0;
+    }
+    int32_t x = nt[0] + nt[1], y = iv[0] + iv[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t xu = __shfl_up_sync(kFull, x, o), yu = __shfl_up_sync(kFull, y, o);
+      if (lane >= o) { x += xu; y += yu; }
+    }
+    const int32_t x0 = x - nt[0] - nt[1], y0 = y - iv[0] - iv[1];
+    if (2 * lane <= a.T) { s_tp[2 * lane] = x0; s_ip[2 * lane] = y0; }
+    if (2 * lane + 1 <= a.T) { s_tp[2 * lane + 1] = x0 + nt[0]; s_ip[2 * lane + 1] = y0 + iv[0]; }
+  }
+  __syncthreads();
+  const int32_t tile = s_tile;
+  if (tile >= s_tp[a.T]) return;  // more blocks are launched than tables need
+  int t = 0;
+  {
+    int lo = 0, hi = a.T - 1;  // largest t with s_tp[t] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_tp[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+  }
+  const int32_t k = tile - s_tp[t];  // tile within the table
+  const int64_t seg_lo = s_P[t];
+  const int32_t n_seg = (int32_t)(s_P[t + 1] - seg_lo);
+  const int32_t base = k * kTile;    // first table-local position of the tile
+  const int32_t n_tile = min(kTile, n_seg - base);
+  const uint32_t dmask = (1u << a.dbits) - 1u;
+  const int shift = a.pass * a.dbits;
+
+  uint32_t key[IPT];
+  int32_t val[IPT];
+  uint32_t rank[IPT];
+  const int32_t wbase = warp * (32 * IPT);
+#pragma unroll
+  for (int q = 0; q < IPT; ++q) {
+    const int32_t li = wbase + q * 32 + lane;
+    const bool ok = li < n_tile;
+    const int64_t gi = seg_lo + base + li;
+    key[q] = ok ? __ldg(a.keys_in + gi) : 0u;
+    val[q] = ok ? (a.vals_in ? __ldg(a.vals_in + gi) : (int32_t)gi) : 0;
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int q = 0; q < IPT; ++q) {  // stable rank inside the warp: items are ordered (q, lane)
+    const int32_t li = wbase + q * 32 + lane;
+    const uint32_t d = li < n_tile ? ((key[q] >> shift) & dmask) : 0xffffu;
+    const uint32_t peers = __match_any_sync(kFull, d);
+    uint32_t before = 0;
+    if (d < kSegBk) before = s_wcnt[warp][d];
+    __syncwarp();
+    if (d < kSegBk) {
+      rank[q] = before + __popc(peers & lt_mask);
+      if ((peers & lt_mask) == 0) s_wcnt[warp][d] = before + __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // per digit (thread tid owns digits tid and tid + 256): warp-exclusive
+  // prefixes and the tile count, published at once
+  uint32_t cnt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int d = tid + h * 256;
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t v = s_wcnt[w][d];
+      s_wcnt[w][d] = c;
+      c += v;
+    }
+    cnt[h] = c;
+  }
+  uint32_t* words = a.lookback + (size_t)tile * kSegBk;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) st_relaxed(words + tid + h * 256, (k == 0 ? kFlagInc : kFlagAgg) | cnt[h]);
+  // tile-local starts and table-local digit bases (exclusive scans over 512 digits)
+  uint32_t tot0, tot1;
+  const uint32_t c0 = block_scan256(cnt[0], s_w, tot0);
+  const uint32_t c1 = block_scan256(cnt[1], s_w, tot1);
+  s_start[tid] = c0 - cnt[0];
+  s_start[tid + 256] = tot0 + c1 - cnt[1];
+  const uint32_t* th = a.hist + ((size_t)t * 2 + a.pass) * kSegBk;
+  const uint32_t h0 = __ldg(th + tid), h1 = __ldg(th + tid + 256);
+  uint32_t ht0, ht1;
+  const uint32_t g0 = block_scan256(h0, s_w, ht0) - h0;
+  const uint32_t g1 = ht0 + block_scan256(h1, s_w, ht1) - h1;
+  __syncthreads();  // s_start complete
+#pragma unroll
+  for (int q = 0; q < IPT; ++q) {  // tile-local sorted order
+    const int32_t li = wbase + q * 32 + lane;
+    if (li < n_tile) {
+      const uint32_t d = (key[q] >> shift) & dmask;
+      const uint32_t slot = s_start[d] + s_wcnt[warp][d] + rank[q];
+      s_keys[slot] = key[q];
+      s_vals[slot] = val[q];
+    }
+  }
+  // look-back over the earlier tiles of this table (k of them), both digits
+  // of the thread in the same 32-tile windows
+  uint32_t excl[2] = {0u, 0u};
+  if (k > 0) {
+    bool done[2] = {false, false};
+    for (int32_t back = 1; back <= k && !(done[0] && done[1]); back += 32) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (done[h]) continue;
+        const uint32_t* col = a.lookback + tid + h * 256;
+        const int32_t hi = tile - back;       // nearest predecessor of this window
+        const int32_t lo_tile = tile - k;     // the table's first tile (inclusive word)
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q)
+          v[q] = hi - q >= lo_tile ? ld_relaxed(col + (size_t)(hi - q) * kSegBk) : kFlagInc;
+        uint32_t inc = 0, miss = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          inc |= (v[q] >> 31) << q;
+          miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
+        }
+        const uint32_t upto = window_upto(inc);
+        if (miss & upto) {
+          const unsigned long long r = lookback_window_slow(col, kSegBk, hi, a.status);
+          excl[h] += (uint32_t)r;
+          if (r >> 32) done[h] = true;
+          continue;
+        }
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) sum += ((upto >> q) & 1u) ? (v[q] & kValMask) : 0u;
+        excl[h] += sum;
+        if (inc) done[h] = true;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) st_relaxed(words + tid + h * 256, kFlagInc | ((excl[h] + cnt[h]) & kValMask));
+  }
+  s_gbase[tid] = (int32_t)(g0 + excl[0]) - (int32_t)s_start[tid];
+  s_gbase[tid + 256] = (int32_t)(g1 + excl[1]) - (int32_t)s_start[tid + 256];
+  __syncthreads();
+  // scatter: table-local position s of slot i is s_gbase[digit] + i
+  const int32_t n_inv_t = s_ip[t + 1] - s_ip[t];
+  const int32_t n_valid_t = n_seg - n_inv_t;
+  const int64_t n_valid = (int64_t)a.N - s_ip[a.T];
+  const uint32_t row_base = a.last ? (uint32_t)__ldg(&a.meta[t].row_base) : 0u;
+  for (int i = tid; i < n_tile; i += kSortThreads) {
+    const uint32_t key_i = s_keys[i];
+    const int32_t sl = s_gbase[(key_i >> shift) & dmask] + i;
+    int64_t dst = seg_lo + sl;
+    uint32_t kout = key_i;
+    if (a.last) {  // valid lookups close up; ids outside their table go behind all of them
+      if (sl < n_valid_t) {
+        dst = seg_lo - s_ip[t] + sl;
+        kout = row_base + key_i;
+      } else {
+        dst = n_valid + s_ip[t] + (sl - n_valid_t);
+        kout = a.sentinel;
+      }
+    }
+    if ((uint64_t)dst < (uint64_t)a.N && (uint32_t)sl < (uint32_t)n_seg) {  // false only for broken inputs
+      const int32_t v = s_vals[i];
+      a.keys_out[dst] = kout;
+      a.vals_out[dst] = v;
+      if (a.bag_sorted) {
         a.bag_sorted[dst] = __ldg(a.bag_of + v);
         if (a.psw_sorted) a.psw_sorted[dst] = __ldg(a.psw + v);
       }
@@ -1207,6 +1512,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   la.B = a.B;
   la.npass = L.npass;
   la.sentinel = sentinel;
+  la.seg_dbits = L.seg_dbits;
+  la.seg_hist = at<uint32_t>(ws, L.seg_hist);
+  la.seg_inv = at<uint32_t>(ws, L.seg_inv);
   if (L.small)
     linearize_kernel<4><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
   else
@@ -1224,6 +1532,38 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     int32_t* vout = last ? final_pos : vbuf[pass & 1];
     if (!last && vout == final_pos) vout = vbuf[(pass + 1) & 1];
     if (vout == vin) vout = (vin == vbuf[0]) ? vbuf[1] : vbuf[0];
+    if (L.seg_dbits > 0) {
+      SegSortArgs ga;
+      ga.keys_in = kin;
+      ga.vals_in = vin;
+      ga.keys_out = kout;
+      ga.vals_out = vout;
+      ga.hist = at<uint32_t>(ws, L.seg_hist);
+      ga.inv = at<uint32_t>(ws, L.seg_inv);
+      ga.offsets = a.offsets;
+      ga.meta = a.meta;
+      ga.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * kSegBk;
+      ga.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
+      ga.status = a.status;
+      ga.bag_of = at<int32_t>(ws, L.bag_of);
+      ga.psw = a.psw;
+      ga.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
+      ga.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+      ga.N = (int32_t)N;
+      ga.T = p.T;
+      ga.B = a.B;
+      ga.pass = pass;
+      ga.dbits = L.seg_dbits;
+      ga.last = last ? 1 : 0;
+      ga.sentinel = sentinel;
+      if (launch_pdl(L.small ? seg_sort_pass_kernel<6> : seg_sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s,
+                     ga))
+        return TBE_ERR_CUDA;
+      trace_mark(s, "bwd_sort_pass");
+      std::swap(kin, kout);
+      vin = vout;
+      continue;
+    }
     SortArgs sa;
     sa.keys_in = kin;
     sa.vals_in = vin;

@@ -37,6 +37,7 @@ struct Plan {
   int32_t maxD;
   int64_t total_rows;
   int32_t key_bits;      // bits needed for a global row or the sentinel total_rows
+  int32_t seg_bits;      // bits needed for an id or the value rows_t, over all tables
   int32_t dtype_mask;    // bit d set if some table has dtype d
   int32_t any_weighted;  // some table is marked weighted
   int32_t out_vec_ok;    // every output segment start is 16-byte aligned

@@ -144,6 +144,37 @@ def test_bad_ids_excluded(tbe):
     check_backward(tbe, p, expect_status=tbe.TBE_DEV_BAD_INDEX)
 
 
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("bad", [False, True])
+def test_segmented_sort(tbe, weighted, bad):
+    """Few tables of at most 2^18 rows with more than 2^16 rows in total: the
+    radix sort runs over ids within each table (two passes); ids outside
+    their table must still end up behind every valid lookup, in position
+    order, exactly as the global sort with its sentinel puts them."""
+    rng = np.random.default_rng(71 + 2 * weighted + bad)
+    rows = [70000, 50000, 100, 3000, 200000]
+    T, B = len(rows), 700
+    lens = rng.integers(0, 40, size=(T, B))
+    lens[2, :] = rng.integers(0, 3, size=B)
+    ids = []
+    for t in range(T):
+        n = int(lens[t].sum())
+        x = (rng.zipf(1.3, size=n) * 7919) % rows[t]
+        if bad:  # ids outside the table: negative and too large
+            k = rng.choice(n, size=max(1, n // 50), replace=False)
+            x[k[::2]] = -3
+            x[k[1::2]] = rows[t] + 5
+        ids.append(x)
+    N = int(lens.sum())
+    psw = rng.random(N).astype(np.float32) if weighted else None
+    tw = np.array([1, 0, 1, 1, 0], np.uint8) if weighted else None
+    D = [64, 32, 128, 16, 64]
+    G = rng.standard_normal((B, sum(D))).astype(np.float32)
+    p = make_problem(T, B, rows=rows, D=D, weights_dtype=[DT_F32] * T, out_dtype=DT_F32, lengths=lens, ids=ids,
+                     psw=psw, table_weighted=tw, grad_out=G)
+    check_backward(tbe, p, expect_status=tbe.TBE_DEV_BAD_INDEX if bad else 0)
+
+
 def test_empty_batches(tbe):
     p = make_problem(2, 8, rows=[5, 7], D=[4, 8], weights_dtype=[DT_F32, DT_F16], out_dtype=DT_F32,
                      lengths=np.zeros((2, 8)), ids=[[], []], grad_out=np.ones((8, 12), np.float32))
