@@ -338,6 +338,15 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   }
   const int64_t p0 = (int64_t)blockIdx.x * kLinTile;
   const int64_t p1 = min(a.N, p0 + kLinTile);
+  // all of this thread's ids are requested first (the bag search below
+  // overlaps their latency)
+  constexpr int kIPT = IPT;
+  int64_t id[kIPT];
+#pragma unroll
+  for (int q = 0; q < kIPT; ++q) {
+    const int64_t i = p0 + q * kLinThreads + tid;
+    id[q] = i < p1 ? ld_stream_i64(a.indices + i) : 0;
+  }
   if (tid < 64) {  // warp 0 finds the bag of p0, warp 1 the bag of p1 - 1
     const int32_t g = bag_search_warp(a.offsets, nb, tid < 32 ? p0 : p1 - 1, lane);
     if (tid == 0) s_g0 = g;
@@ -353,13 +362,6 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
   __syncthreads();
   int bad = 0, invalid = 0;
-  constexpr int kIPT = IPT;
-  int64_t id[kIPT];
-#pragma unroll
-  for (int q = 0; q < kIPT; ++q) {  // all of this thread's ids are requested first
-    const int64_t i = p0 + q * kLinThreads + tid;
-    id[q] = i < p1 ? ld_stream_i64(a.indices + i) : 0;
-  }
 #pragma unroll
   for (int q = 0; q < kIPT; ++q) {
     const int64_t i = p0 + q * kLinThreads + tid;
@@ -913,7 +915,11 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   const int32_t tile = s_tile;
   const int32_t j0 = tile * kRleTile + tid * kRleIPT;
   uint32_t k[kRleIPT];
+  // the key before and the key after this thread's keys are requested with them
   uint32_t prev = (j0 > 0 && j0 - 1 < a.N) ? __ldg(a.keys + j0 - 1) : 0xffffffffu;
+  const uint32_t knext = (j0 + kRleIPT < a.N) ? __ldg(a.keys + j0 + kRleIPT) : a.sentinel;
+  int64_t prevk = (j0 > 0 && j0 - 1 < a.N) ? (int64_t)prev : -1;
+  if (prevk >= (int64_t)a.sentinel) prevk = -1;
   uint32_t flags = 0, nflag = 0;
 #pragma unroll
   for (int q = 0; q < kRleIPT; ++q) {
@@ -924,6 +930,10 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
     flags |= (uint32_t)f << q;
     nflag += f;
   }
+  // table of the key before this thread's keys and the next table's first
+  // row (their loads overlap the look-back below)
+  int tp = prevk < 0 ? -1 : table_of_row(a.meta, a.T, prevk);
+  int64_t next_base = next_table_base(a.meta, a.T, tp);
   uint32_t x = nflag;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -964,13 +974,8 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   // the last valid key writes U for the tables after it.  The thread tracks
   // the table of its latest key and the next table's first row, so the
   // search for a key's table only runs at a boundary (out of line).
-  int64_t prevk = (j0 > 0 && j0 - 1 < a.N) ? (int64_t)__ldg(a.keys + j0 - 1) : -1;
-  if (prevk >= (int64_t)a.sentinel) prevk = -1;
-  const uint32_t knext = (j0 + kRleIPT < a.N) ? __ldg(a.keys + j0 + kRleIPT) : a.sentinel;
   if (j0 == 0 && (a.N == 0 || k[0] >= a.sentinel))  // no valid lookup at all
     for (int t = 0; t <= a.T; ++t) a.unique_count[t] = 0;
-  int tp = prevk < 0 ? -1 : table_of_row(a.meta, a.T, prevk);
-  int64_t next_base = next_table_base(a.meta, a.T, tp);
 #pragma unroll
   for (int q = 0; q < kRleIPT; ++q) {
     const int32_t j = j0 + q;
