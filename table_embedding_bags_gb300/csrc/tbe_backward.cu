@@ -191,6 +191,9 @@ struct Layout {
 
 // counters: 8-byte slots; kCntLong holds (long runs << 32) | chunks
 enum Counter { kCntU = 0, kCntInvalid = 1, kCntWork = 2, kCntSub = 3, kCntLong = 4, kNumCounters = 8 };
+// counter k lives at counters[k * kCntStride] (uint32 units): each on its own
+// 128-byte line, so the reducer's claims do not slow reads of the others
+constexpr int kCntStride = 32;
 
 static size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -254,7 +257,7 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.seg_inv = take(L.seg_dbits > 0 ? 4 * (size_t)p.T : 0);
   L.sort_tiles = take(4 * 4);
   L.rle_tile = take(4);
-  L.counters = take(8 * kNumCounters);
+  L.counters = take(4 * (size_t)kCntStride * kNumCounters);
   L.zero_end = off;
   L.lin_zero_begin = off;  // cleared by the linearize kernel
   L.sort_lookback = take(4 * (size_t)L.npass * L.sort_ntiles * (L.seg_dbits > 0 ? kSegBk : 256));
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   }
   if (bad & 1) report(a.status, TBE_DEV_BAD_INDEX);
   if (bad & 2) report(a.status, TBE_DEV_BAD_OFFSETS);
-  if (invalid) atomicAdd(&a.counters[kCntInvalid * 2], (uint32_t)invalid);
+  if (invalid) atomicAdd(&a.counters[kCntInvalid * kCntStride], (uint32_t)invalid);
   __syncthreads();
   if (a.seg_dbits > 0) {  // s_hist holds the two 512-bucket histograms of t_first back to back
     for (int k = tid; k < 2 * kSegBk; k += kLinThreads) {
@@ -968,8 +971,8 @@ __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
     const uint32_t excl = s_excl;
     if (tile == a.ntiles - 1) {
       const uint32_t U = min(excl + total, (uint32_t)a.N);
-      const uint32_t n_valid = (uint32_t)a.N - a.counters[kCntInvalid * 2];
-      a.counters[kCntU * 2] = U;
+      const uint32_t n_valid = (uint32_t)a.N - a.counters[kCntInvalid * kCntStride];
+      a.counters[kCntU * kCntStride] = U;
       a.run_starts[U] = (int32_t)n_valid;
     }
   }
@@ -1030,7 +1033,7 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
   __shared__ unsigned long long s_base;
   __shared__ uint32_t s_sub_base;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t U = (int32_t)a.counters[kCntU * 2];
+  const int32_t U = (int32_t)a.counters[kCntU * kCntStride];
   if (blockIdx.x == 0) {
     // float offset of each table's block of row gradients:
     // gofs[t] = sum_{t' < t} (unique rows of t') * D_t'
@@ -1094,7 +1097,7 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
     }
     if (tid == 0 && t0 > 0)
       s_base = atomicAdd(a.long_counter, ((unsigned long long)t0 << 32) | (unsigned long long)t1);
-    if (tid == 32 && t2 > 0) s_sub_base = atomicAdd(&a.counters[kCntSub * 2], t2);
+    if (tid == 32 && t2 > 0) s_sub_base = atomicAdd(&a.counters[kCntSub * kCntStride], t2);
     __syncthreads();
     if (is_long) {
       const uint32_t lpos = (uint32_t)(s_base >> 32) + w0 + x0 - 1;
@@ -1439,15 +1442,15 @@ __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs
   wait_predecessor();
   release_dependents();
   const int lane = threadIdx.x & 31;
-  const int32_t U = (int32_t)a.counters[kCntU * 2];
+  const int32_t U = (int32_t)a.counters[kCntU * kCntStride];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
-  const int32_t n_items = n_chunks + (int32_t)a.counters[kCntSub * 2];
+  const int32_t n_items = n_chunks + (int32_t)a.counters[kCntSub * kCntStride];
   // the next work item is claimed while the current one is reduced
   uint32_t claim = 0;
-  if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * 2], 1u);
+  if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * kCntStride], 1u);
   uint32_t item = __shfl_sync(kFull, claim, 0);
   while ((int32_t)item < n_items) {
-    if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * 2], 1u);
+    if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * kCntStride], 1u);
     if ((int32_t)item < n_chunks) {
       long_chunk<W, UNR>(a, (int32_t)item, lane);
     } else {
@@ -1619,7 +1622,7 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   trace_mark(s, "bwd_rle");
 
   const Tuning& tu = tuning();
-  unsigned long long* long_counter = reinterpret_cast<unsigned long long*>(counters + kCntLong * 2);
+  unsigned long long* long_counter = reinterpret_cast<unsigned long long*>(counters + kCntLong * kCntStride);
   ClsArgs ca;
   ca.unique_rows = a.unique_rows;
   ca.run_starts = run_starts;
