@@ -461,8 +461,6 @@ template <int IPT>
 __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortArgs a) {
   constexpr int kSortIPT = IPT;
   constexpr int kSortTile = kSortThreads * IPT;
-  wait_predecessor();
-  release_dependents();
   __shared__ uint32_t s_wcnt[kSortWarps][256];
   __shared__ uint32_t s_start[256];   // tile-local first slot of each digit
   __shared__ int32_t s_gbase[256];    // global position of slot 0 of each digit, minus s_start
@@ -471,7 +469,11 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   __shared__ uint32_t s_scan[kSortWarps];
   __shared__ int32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the tile counter was cleared before the first kernel of the backward, so
+  // the tile is claimed while the previous pass drains
   if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
+  wait_predecessor();
+  release_dependents();
   for (int k = tid; k < kSortWarps * 256; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
   __syncthreads();
   const int32_t tile = s_tile;
@@ -592,7 +594,10 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   s_gbase[tid] = (int32_t)(gdigit + excl) - (int32_t)s_start[tid];
   __syncthreads();
   const int32_t n_tile = min(kSortTile, a.N - tile * kSortTile);
-  for (int i = tid; i < n_tile; i += kSortThreads) {
+#pragma unroll
+  for (int r = 0; r < IPT; ++r) {  // unrolled: the gathers of the last pass are all in flight together
+    const int i = tid + r * kSortThreads;
+    if (i >= n_tile) break;
     const uint32_t k = s_keys[i];
     const int32_t dst = s_gbase[(k >> a.shift) & 0xffu] + i;
     if ((uint32_t)dst < (uint32_t)a.N) {  // always true unless a wait timed out
@@ -666,8 +671,6 @@ __device__ __forceinline__ uint32_t block_scan256(uint32_t x, uint32_t* s_w, uin
 template <int IPT>
 __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const SegSortArgs a) {
   constexpr int kTile = kSortThreads * IPT;
-  wait_predecessor();
-  release_dependents();
   __shared__ uint32_t s_wcnt[kSortWarps][kSegBk];
   __shared__ uint32_t s_start[kSegBk];  // tile-local first slot of each digit
   __shared__ int32_t s_gbase[kSegBk];   // table-local position of slot 0 of each digit, minus s_start
@@ -679,6 +682,8 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
   __shared__ int32_t s_ip[kSegMaxT + 1]; // ids outside their table before each table
   __shared__ int32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the tile counter (cleared before the first kernel of the backward) and
+  // the offsets (an input) are read while the previous kernel drains
   if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
   for (int k = tid; k < kSortWarps * kSegBk; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
   // table ranges, clamped so that broken offsets still give ranges inside [0, N)
@@ -686,6 +691,8 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
     int64_t P = __ldg(a.offsets + (int64_t)tid * a.B);
     s_P[tid] = min(max(P, (int64_t)0), (int64_t)a.N);
   }
+  wait_predecessor();
+  release_dependents();
   __syncthreads();
   if (warp == 0) {  // tiles and invalid ids per table, two tables per lane
     int32_t nt[2], iv[2];
@@ -841,7 +848,10 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
   const int32_t n_valid_t = n_seg - n_inv_t;
   const int64_t n_valid = (int64_t)a.N - s_ip[a.T];
   const uint32_t row_base = a.last ? (uint32_t)__ldg(&a.meta[t].row_base) : 0u;
-  for (int i = tid; i < n_tile; i += kSortThreads) {
+#pragma unroll
+  for (int r = 0; r < IPT; ++r) {  // unrolled: the gathers of the last pass are all in flight together
+    const int i = tid + r * kSortThreads;
+    if (i >= n_tile) break;
     const uint32_t key_i = s_keys[i];
     const int32_t sl = s_gbase[(key_i >> shift) & dmask] + i;
     int64_t dst = seg_lo + sl;
@@ -913,14 +923,15 @@ template <int IPT>
 __global__ void __launch_bounds__(kRleThreads) rle_kernel(const RleArgs a) {
   constexpr int kRleIPT = IPT;
   constexpr int kRleTile = kRleThreads * IPT;
-  wait_predecessor();
-  release_dependents();
   __shared__ uint32_t s_scan[kRleThreads / 32];
   __shared__ uint32_t s_lb[2 * (kRleThreads / 32)];
   __shared__ uint32_t s_excl;
   __shared__ int32_t s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the tile counter was cleared before the first kernel of the backward
   if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
+  wait_predecessor();
+  release_dependents();
   __syncthreads();
   const int32_t tile = s_tile;
   const int32_t j0 = tile * kRleTile + tid * kRleIPT;
