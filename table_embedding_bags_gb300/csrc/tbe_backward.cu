@@ -85,6 +85,9 @@ __device__ __noinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status) {
   return kFlagInc;
 }
 
+// Whole-window re-reads before a look-back falls back to waiting word by word.
+constexpr int kWindowRetries = 8;
+
 // Mask of the window positions 0..q* (q* = nearest predecessor with an
 // inclusive word; all 32 positions when there is none).
 __device__ __forceinline__ uint32_t window_upto(uint32_t inc) {
@@ -462,6 +465,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   constexpr int kSortIPT = IPT;
   constexpr int kSortTile = kSortThreads * IPT;
   __shared__ uint32_t s_wcnt[kSortWarps][256];
+  __shared__ uint32_t s_cnt[256];     // tile count of each digit
   __shared__ uint32_t s_start[256];   // tile-local first slot of each digit
   __shared__ int32_t s_gbase[256];    // global position of slot 0 of each digit, minus s_start
   __shared__ uint32_t s_keys[kSortTile];
@@ -475,6 +479,7 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
   wait_predecessor();
   release_dependents();
   for (int k = tid; k < kSortWarps * 256; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
+  s_cnt[tid] = 0;
   __syncthreads();
   const int32_t tile = s_tile;
   const int32_t wbase = tile * kSortTile + warp * (32 * kSortIPT);
@@ -489,6 +494,14 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
     key[k] = ok ? __ldg(a.keys_in + idx) : 0u;
     val[k] = ok ? (a.vals_in ? __ldg(a.vals_in + idx) : idx) : 0;
   }
+  // the tile's digit counts come first and are published at once, so later
+  // tiles find them in their look-back without waiting for this tile's ranking
+#pragma unroll
+  for (int k = 0; k < kSortIPT; ++k)
+    if (wbase + k * 32 + lane < a.N) atomicAdd(&s_cnt[(key[k] >> a.shift) & 0xffu], 1u);
+  __syncthreads();
+  uint32_t* my_word = a.lookback + (size_t)tile * 256 + tid;
+  st_relaxed(my_word, (tile == 0 ? kFlagInc : kFlagAgg) | s_cnt[tid]);
   // stable rank inside the warp: items are ordered (k, lane)
   const uint32_t lt_mask = (1u << lane) - 1u;
 #pragma unroll
@@ -517,9 +530,6 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
       cnt += c;
     }
   }
-  // publish this tile's count of the digit as soon as it is known
-  uint32_t* my_word = a.lookback + (size_t)tile * 256 + tid;
-  st_relaxed(my_word, (tile == 0 ? kFlagInc : kFlagAgg) | cnt);
   // block exclusive scan of the digit counts -> s_start
   uint32_t x = cnt;
 #pragma unroll
@@ -568,15 +578,21 @@ __global__ void __launch_bounds__(kSortThreads, 4) sort_pass_kernel(const SortAr
     const uint32_t* col = a.lookback + tid;
     for (int32_t hi = tile - 1; hi >= 0; hi -= 32) {
       uint32_t v[32];
+      uint32_t inc = 0, miss = 0, upto = 0;
+      for (int retry = 0; retry < kWindowRetries; ++retry) {  // the whole window again while words are missing
 #pragma unroll
-      for (int q = 0; q < 32; ++q) v[q] = hi - q >= 0 ? ld_relaxed(col + (size_t)(hi - q) * 256) : kFlagInc;
-      uint32_t inc = 0, miss = 0;
+        for (int q = 0; q < 32; ++q) v[q] = hi - q >= 0 ? ld_relaxed(col + (size_t)(hi - q) * 256) : kFlagInc;
+        inc = 0;
+        miss = 0;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        inc |= (v[q] >> 31) << q;
-        miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
+        for (int q = 0; q < 32; ++q) {
+          inc |= (v[q] >> 31) << q;
+          miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
+        }
+        upto = window_upto(inc);
+        if (!(miss & upto)) break;
+        __nanosleep(32);
       }
-      const uint32_t upto = window_upto(inc);
       if (miss & upto) {
         const unsigned long long r = lookback_window_slow(col, 256, hi, a.status);
         excl += (uint32_t)r;
@@ -672,6 +688,7 @@ template <int IPT>
 __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const SegSortArgs a) {
   constexpr int kTile = kSortThreads * IPT;
   __shared__ uint32_t s_wcnt[kSortWarps][kSegBk];
+  __shared__ uint32_t s_cnt[kSegBk];    // tile count of each digit
   __shared__ uint32_t s_start[kSegBk];  // tile-local first slot of each digit
   __shared__ int32_t s_gbase[kSegBk];   // table-local position of slot 0 of each digit, minus s_start
   __shared__ uint32_t s_keys[kTile];
@@ -686,6 +703,7 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
   // the offsets (an input) are read while the previous kernel drains
   if (tid == 0) s_tile = (int32_t)atomicAdd(a.tile_counter, 1u);
   for (int k = tid; k < kSortWarps * kSegBk; k += kSortThreads) (&s_wcnt[0][0])[k] = 0;
+  for (int k = tid; k < kSegBk; k += kSortThreads) s_cnt[k] = 0;
   // table ranges, clamped so that broken offsets still give ranges inside [0, N)
   if (tid <= a.T) {
     int64_t P = __ldg(a.offsets + (int64_t)tid * a.B);
@@ -745,6 +763,16 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
     key[q] = ok ? __ldg(a.keys_in + gi) : 0u;
     val[q] = ok ? (a.vals_in ? __ldg(a.vals_in + gi) : (int32_t)gi) : 0;
   }
+  // the tile's digit counts come first and are published at once, so later
+  // tiles of the table find them in their look-back without waiting for this
+  // tile's ranking
+#pragma unroll
+  for (int q = 0; q < IPT; ++q)
+    if (wbase + q * 32 + lane < n_tile) atomicAdd(&s_cnt[(key[q] >> shift) & dmask], 1u);
+  __syncthreads();
+  uint32_t* words = a.lookback + (size_t)tile * kSegBk;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) st_relaxed(words + tid + h * 256, (k == 0 ? kFlagInc : kFlagAgg) | s_cnt[tid + h * 256]);
   const uint32_t lt_mask = (1u << lane) - 1u;
 #pragma unroll
   for (int q = 0; q < IPT; ++q) {  // stable rank inside the warp: items are ordered (q, lane)
@@ -776,9 +804,6 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
     }
     cnt[h] = c;
   }
-  uint32_t* words = a.lookback + (size_t)tile * kSegBk;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) st_relaxed(words + tid + h * 256, (k == 0 ? kFlagInc : kFlagAgg) | cnt[h]);
   // tile-local starts and table-local digit bases (exclusive scans over 512 digits)
   uint32_t tot0, tot1;
   const uint32_t c0 = block_scan256(cnt[0], s_w, tot0);
@@ -814,16 +839,22 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
         const int32_t hi = tile - back;       // nearest predecessor of this window
         const int32_t lo_tile = tile - k;     // the table's first tile (inclusive word)
         uint32_t v[32];
+        uint32_t inc = 0, miss = 0, upto = 0;
+        for (int retry = 0; retry < kWindowRetries; ++retry) {  // the whole window again while words are missing
 #pragma unroll
-        for (int q = 0; q < 32; ++q)
-          v[q] = hi - q >= lo_tile ? ld_relaxed(col + (size_t)(hi - q) * kSegBk) : kFlagInc;
-        uint32_t inc = 0, miss = 0;
+          for (int q = 0; q < 32; ++q)
+            v[q] = hi - q >= lo_tile ? ld_relaxed(col + (size_t)(hi - q) * kSegBk) : kFlagInc;
+          inc = 0;
+          miss = 0;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          inc |= (v[q] >> 31) << q;
-          miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
+          for (int q = 0; q < 32; ++q) {
+            inc |= (v[q] >> 31) << q;
+            miss |= (uint32_t)((v[q] >> 30) == 0u) << q;
+          }
+          upto = window_upto(inc);
+          if (!(miss & upto)) break;
+          __nanosleep(32);
         }
-        const uint32_t upto = window_upto(inc);
         if (miss & upto) {
           const unsigned long long r = lookback_window_slow(col, kSegBk, hi, a.status);
           excl[h] += (uint32_t)r;
