@@ -228,6 +228,9 @@ int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, c
  *                        per warp at once
  *   red_unroll         : gradient slices in flight per lane in the backward
  *                        reduction (4: more resident warps, 8: deeper)
+ *   fwd_ring           : 1 = rows of at most 512 bytes are copied into a ring
+ *                        of shared memory (16 rows in flight per lane group);
+ *                        0 = rows are loaded into registers
  *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
  *                        many as fit; 4 with fwd_unroll 4 selects a build
  *                        of the kernel with a smaller register budget)
@@ -246,6 +249,7 @@ typedef struct tbe_tuning {
   int32_t short_item_lookups;
   int32_t fwd_lanes_per_row;
   int32_t red_unroll;
+  int32_t fwd_ring;
 } tbe_tuning;
 int tbe_get_tuning(tbe_tuning* out);
 int tbe_set_tuning(const tbe_tuning* in);

@@ -48,7 +48,8 @@ class Tuning(ctypes.Structure):
     _fields_ = [("long_run_threshold", ctypes.c_int32), ("long_chunk", ctypes.c_int32),
                 ("fwd_unroll", ctypes.c_int32), ("fwd_blocks_per_sm", ctypes.c_int32),
                 ("hist_min_mean_bag", ctypes.c_int32), ("short_item_lookups", ctypes.c_int32),
-                ("fwd_lanes_per_row", ctypes.c_int32), ("red_unroll", ctypes.c_int32)]
+                ("fwd_lanes_per_row", ctypes.c_int32), ("red_unroll", ctypes.c_int32),
+                ("fwd_ring", ctypes.c_int32)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -14,7 +14,7 @@ namespace tbe {
 static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/0, /*fwd_unroll=*/4,
                           /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48,
                           /*short_item_lookups=*/32, /*fwd_lanes_per_row=*/16,
-                          /*red_unroll=*/4};
+                          /*red_unroll=*/4, /*fwd_ring=*/1};
 
 const Tuning& tuning() { return g_tuning; }
 
@@ -104,6 +104,7 @@ int tbe_get_tuning(tbe_tuning* out) {
   out->short_item_lookups = g_tuning.short_item_lookups;
   out->fwd_lanes_per_row = g_tuning.fwd_lanes_per_row;
   out->red_unroll = g_tuning.red_unroll;
+  out->fwd_ring = g_tuning.fwd_ring;
   return TBE_OK;
 }
 
@@ -119,6 +120,7 @@ int tbe_set_tuning(const tbe_tuning* in) {
   if (in->fwd_blocks_per_sm < 0 || in->fwd_blocks_per_sm > 32) return TBE_ERR_INVALID_ARG;
   if (in->hist_min_mean_bag < 0) return TBE_ERR_INVALID_ARG;
   if (in->red_unroll != 4 && in->red_unroll != 8) return TBE_ERR_INVALID_ARG;
+  if (in->fwd_ring != 0 && in->fwd_ring != 1) return TBE_ERR_INVALID_ARG;
   if (in->short_item_lookups < 32 || in->short_item_lookups > (1 << 20)) return TBE_ERR_INVALID_ARG;
   g_tuning.long_run_threshold = in->long_run_threshold;
   g_tuning.long_chunk = in->long_chunk;
@@ -128,6 +130,7 @@ int tbe_set_tuning(const tbe_tuning* in) {
   g_tuning.short_item_lookups = in->short_item_lookups;
   g_tuning.fwd_lanes_per_row = in->fwd_lanes_per_row;
   g_tuning.red_unroll = in->red_unroll;
+  g_tuning.fwd_ring = in->fwd_ring;
   return TBE_OK;
 }
 

@@ -297,6 +297,254 @@ __global__ void __launch_bounds__(kThreads, MINB) fwd_gather_kernel(const FwdArg
   }
 }
 
+// ---------------------------------------------------------------------------
+// Ring variant (rows of at most 512 bytes): rows are copied asynchronously
+// (cp.async, 16 bytes per lane, cached in L1) into a ring of kRing slots of
+// shared memory per lane, so each lane group keeps kRing rows of its bag in
+// flight without holding registers for them; lane `sub` copies and later
+// reads only its own chunk of each row (no cross-lane ordering needed, the
+// per-thread cp.async.wait_group suffices).  The bag's id window sits in
+// shared memory, so both the copy of row j + kRing and the sum of row j read
+// their id by index.
+// ---------------------------------------------------------------------------
+constexpr int kRing = 16;      // 16-byte slots per lane
+constexpr int kRingLanes = 16; // most lanes per row: two bags per warp at least
+constexpr int kRingStride = kThreads * 16;  // bytes between a thread's ring slots
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// all but the N most recent groups of this thread have landed
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+// KMAX chunks of each row per lane (1, or 2 for rows of 17..32 chunks); the
+// ring's kRing slots per lane hold RD = kRing / KMAX rows.
+template <int DT, int KMAX, bool WT, typename OutT>
+__device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta& m, int lsh, int b, int lane,
+                                              int64_t start, int64_t end, uint32_t ring, int32_t* ids, float* wts) {
+  constexpr int E = Chunk<DT>::kElems;
+  constexpr int RD = kRing / KMAX;  // rows in flight
+  const int lpr = 1 << lsh;
+  const int C = m.D / E;
+  const int sub = lane & (lpr - 1);
+  const unsigned vmask = lpr == 32 ? kFull : (((1u << lpr) - 1u) << (lane & ~(lpr - 1)));
+  const char* tbl = reinterpret_cast<const char*>(a.weights) + m.w_off;
+  const int64_t row_bytes = (int64_t)C * 16;
+  const bool weighted = WT && m.weighted;
+  const int win = kIdsPerLane * lpr;
+  float acc[KMAX][E];  // one accumulator set: rows arrive far slower than adds complete
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+  bool bad = false;
+  auto issue = [&](int j, int slot) {  // row j's chunks of this lane into ring slots slot*KMAX + k
+    const int32_t id = ids[j];
+    if (id >= 0) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int c = sub + k * lpr;
+        if (c < C) cp_async16(ring + (slot * KMAX + k) * kRingStride, tbl + (int64_t)id * row_bytes + c * 16);
+      }
+    }
+  };
+#pragma unroll 1
+  for (int64_t base = start; base < end; base += win) {
+    const int nwin = (int)min((int64_t)win, end - base);
+#pragma unroll
+    for (int k = 0; k < kIdsPerLane; ++k) {  // the window's ids, one coalesced request
+      const int idx = k * lpr + sub;
+      const int64_t raw = idx < nwin ? ld_stream_i64(a.indices + base + idx) : 0;
+      ids[idx] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
+      if (WT) wts[idx] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
+    }
+    __syncwarp(vmask);
+#pragma unroll 1
+    for (int j = 0; j < RD; ++j) {  // the first RD rows
+      if (j < nwin) issue(j, j);
+      cp_commit();
+    }
+#pragma unroll 1
+    for (int j = 0; j < nwin; ++j) {
+      cp_wait<RD - 1>();  // row j has landed
+      const int32_t id = ids[j];
+      bad |= id < 0;
+      const int slot = j & (RD - 1);
+      const float w = WT ? wts[j] : 1.f;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        const int c = sub + k * lpr;
+        float f[E];
+        if (c < C && id >= 0) {
+          Chunk<DT>::to_float(lds128(ring + (slot * KMAX + k) * kRingStride), f);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) f[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          acc[k][e] = __fadd_rn(acc[k][e], (WT && weighted) ? __fmul_rn(w, f[e]) : f[e]);
+      }
+      if (j + RD < nwin) issue(j + RD, slot);  // refill the slot just read
+      cp_commit();
+    }
+    __syncwarp(vmask);  // the ids are rewritten by the next window
+  }
+  OutT* out_row = reinterpret_cast<OutT*>(a.out) + (int64_t)b * a.sumD + m.col_off;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    const int c = sub + k * lpr;
+    if (c < C) {
+      store_out<OutT>(out_row + (int64_t)c * E, acc[k], E, a.out_vec_ok);
+    }
+  }
+  if (__any_sync(vmask, bad) && sub == 0) report(a.status, TBE_DEV_BAD_INDEX);
+}
+
+template <int DT, bool WT, typename OutT>
+__device__ __forceinline__ void pool_ring_dt(const FwdArgs& a, const TableMeta& m, int lsh, int b, int lane,
+                                             int64_t start, int64_t end, uint32_t ring, int32_t* ids, float* wts) {
+  if (m.D / Chunk<DT>::kElems <= (1 << lsh))
+    pool_bag_ring<DT, 1, WT, OutT>(a, m, lsh, b, lane, start, end, ring, ids, wts);
+  else
+    pool_bag_ring<DT, 2, WT, OutT>(a, m, lsh, b, lane, start, end, ring, ids, wts);
+}
+
+// Dynamic shared memory: ring [kRing][kThreads] x 16 B | ids [warps][128] |
+// weights [warps][128] | running task count [T + 1].
+constexpr size_t kRingBytes = (size_t)kRing * kThreads * 16;
+constexpr size_t kRingWinBytes = (size_t)(kThreads / 32) * 128 * 4;
+
+template <typename OutT, int DTSEL, bool WT>
+__global__ void __launch_bounds__(kThreads, 3) fwd_ring_kernel(const FwdArgs a) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  int32_t* s_ids = reinterpret_cast<int32_t*>(dsm + kRingBytes);
+  float* s_wts = reinterpret_cast<float*>(dsm + kRingBytes + kRingWinBytes);
+  int32_t* s_pref = reinterpret_cast<int32_t*>(dsm + kRingBytes + 2 * kRingWinBytes);
+  __shared__ int32_t s_part[kThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  {  // running task count over tables (as fwd_gather_kernel)
+    const int per = (a.T + kThreads - 1) / kThreads;
+    int32_t mine = 0;
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) mine += (a.B + (32 / lanes_per_row(load_meta(a.meta + t), kRingLanes)) - 1) /
+                           (32 / lanes_per_row(load_meta(a.meta + t), kRingLanes));
+    }
+    int32_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    int32_t run = x - mine;
+    for (int w = 0; w < warp; ++w) run += s_part[w];
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) {
+        s_pref[t] = run;
+        const int G = 32 / lanes_per_row(load_meta(a.meta + t), kRingLanes);
+        run += (a.B + G - 1) / G;
+      }
+    }
+    if (tid == kThreads - 1) s_pref[a.T] = run;
+    __syncthreads();
+  }
+  FwdArgs ar = a;
+  ar.lpr_max = kRingLanes;
+  const int32_t ntasks = s_pref[a.T];
+  const int32_t nw = (int32_t)((gridDim.x * kThreads) >> 5);
+  const int32_t nb = a.T * a.B;
+  const uint32_t ring = smem_u32(dsm) + tid * 16;
+  int32_t task = (int32_t)((blockIdx.x * kThreads + tid) >> 5);
+  Task cur = locate_task(ar, s_pref, ntasks, task, lane);
+  int64_t cs = 0, ce = 0;
+  if (cur.live) bag_bounds(ar, cur, cs, ce);
+  while (task < ntasks) {
+    const Task nxt = locate_task(ar, s_pref, ntasks, task + nw, lane);
+    int64_t ns = 0, ne = 0;
+    if (nxt.live) bag_bounds(ar, nxt, ns, ne);
+    if (cur.live) {
+      check_bounds(ar, cur, nb, lane, cs, ce);
+      const TableMeta m = load_meta(a.meta + cur.t);
+      const int vw = lane & ~((1 << cur.lsh) - 1);  // first lane of the virtual warp
+      int32_t* ids = s_ids + warp * 128 + vw * kIdsPerLane;
+      float* wts = s_wts + warp * 128 + vw * kIdsPerLane;
+      if (DTSEL >= 0) {
+        pool_ring_dt<(DTSEL < 0 ? 0 : DTSEL), WT, OutT>(ar, m, cur.lsh, cur.b, lane, cs, ce, ring, ids, wts);
+      } else {
+        switch (m.dtype) {
+          case TBE_F32: pool_ring_dt<TBE_F32, WT, OutT>(ar, m, cur.lsh, cur.b, lane, cs, ce, ring, ids, wts); break;
+          case TBE_F16: pool_ring_dt<TBE_F16, WT, OutT>(ar, m, cur.lsh, cur.b, lane, cs, ce, ring, ids, wts); break;
+          default: pool_ring_dt<TBE_BF16, WT, OutT>(ar, m, cur.lsh, cur.b, lane, cs, ce, ring, ids, wts); break;
+        }
+      }
+    }
+    cur = nxt;
+    cs = ns;
+    ce = ne;
+    task += nw;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the block's shared memory
+}
+
+template <typename OutT, int DTSEL, bool WT>
+int launch_ring(const FwdArgs& a, cudaStream_t s) {
+  const size_t smem = kRingBytes + 2 * kRingWinBytes + 4 * ((size_t)a.T + 1);
+  auto kern = fwd_ring_kernel<OutT, DTSEL, WT>;
+  static size_t configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) dev = 63;
+  if (configured[dev] < smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(96 * 1024 + 4 * (TBE_MAX_TABLES + 1))) !=
+        cudaSuccess)
+      return TBE_ERR_CUDA;
+    configured[dev] = 96 * 1024 + 4 * (TBE_MAX_TABLES + 1);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm <= 0)
+    per_sm = 1;
+  const int64_t want = ((int64_t)a.T * a.B + (kThreads / 32) - 1) / (kThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * per_sm));
+  kern<<<grid, kThreads, smem, s>>>(a);
+  return check_launch();
+}
+
+template <typename OutT, int DTSEL>
+int launch_ring_w(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (a.psw != nullptr && p.any_weighted) return launch_ring<OutT, DTSEL, true>(a, s);
+  return launch_ring<OutT, DTSEL, false>(a, s);
+}
+
+template <typename OutT>
+int launch_ring_dt(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (p.dtype_mask == (1 << TBE_F16)) return launch_ring_w<OutT, TBE_F16>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_F32)) return launch_ring_w<OutT, TBE_F32>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_BF16)) return launch_ring_w<OutT, TBE_BF16>(p, a, s);
+  return launch_ring_w<OutT, -1>(p, a, s);
+}
+
+bool ring_eligible(const Plan& p) {
+  for (int t = 0; t < p.T; ++t)
+    if (p.hmeta[t].D * (p.hmeta[t].dtype == TBE_F32 ? 4 : 2) > 512) return false;
+  return p.T > 0;
+}
+
 template <typename OutT, int R, int DTSEL, bool WT, int MINB>
 int launch_typed(const FwdArgs& a, cudaStream_t s) {
   static int occ[64] = {0};
@@ -345,6 +593,13 @@ int launch_dtsel(const Plan& p, const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (tuning().fwd_ring && ring_eligible(p)) {
+    switch (p.out_dtype) {
+      case TBE_F32: return launch_ring_dt<float>(p, a, s);
+      case TBE_F16: return launch_ring_dt<__half>(p, a, s);
+      default: return launch_ring_dt<__nv_bfloat16>(p, a, s);
+    }
+  }
   switch (p.out_dtype) {
     case TBE_F32: return launch_dtsel<float>(p, a, s);
     case TBE_F16: return launch_dtsel<__half>(p, a, s);

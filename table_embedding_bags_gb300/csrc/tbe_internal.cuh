@@ -57,6 +57,7 @@ struct Tuning {
   int32_t short_item_lookups;
   int32_t fwd_lanes_per_row;
   int32_t red_unroll;
+  int32_t fwd_ring;
 };
 const Tuning& tuning();
 

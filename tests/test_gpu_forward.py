@@ -42,6 +42,16 @@ def check_full(tbe, p, path=None):
     return parity.compare_forward(p, parity.to_f64(out), ref, ref_abs)
 
 
+@pytest.fixture(params=[1, 0], ids=["ring", "registers"])
+def gather_mode(tbe, request):
+    """Runs a test with rows staged through the shared-memory ring (1) and
+    with rows loaded into registers (0)."""
+    old = tbe.get_tuning()
+    tbe.set_tuning(fwd_ring=request.param)
+    yield request.param
+    tbe.set_tuning(**old)
+
+
 @pytest.mark.parametrize("name,B,rows_scale", [
     ("tiny", None, 1.0),
     ("mid_skewed", None, 1.0),
@@ -49,7 +59,7 @@ def check_full(tbe, p, path=None):
     ("small_table", 777, 1.0),
     ("bwd_skew", 301, 0.02),
 ])
-def test_configs_reduced(tbe, name, B, rows_scale):
+def test_configs_reduced(tbe, gather_mode, name, B, rows_scale):
     p = make_config(name, B=B, rows_scale=rows_scale)
     check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
 
@@ -78,7 +88,7 @@ def test_shapes_and_dtypes(tbe, out_dt, weighted):
 
 @pytest.mark.parametrize("out_dt", [DT_F32, DT_F16, DT_BF16])
 @pytest.mark.parametrize("weighted", [False, True])
-def test_narrow_rows_long_bags(tbe, out_dt, weighted):
+def test_narrow_rows_long_bags(tbe, gather_mode, out_dt, weighted):
     """Rows of 16..512 bytes in every dtype, a row width that is not a power
     of two chunks, bags longer than several id windows, empty bags."""
     rng = np.random.default_rng(300 + out_dt * 2 + weighted)
@@ -99,7 +109,7 @@ def test_narrow_rows_long_bags(tbe, out_dt, weighted):
     check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
 
 
-def test_repeated_ids_and_empty(tbe):
+def test_repeated_ids_and_empty(tbe, gather_mode):
     p = make_problem(2, 3, rows=[5, 7], D=[8, 4], weights_dtype=[DT_F16, DT_F32], out_dtype=DT_F32,
                      lengths=[[0, 40, 1], [3, 0, 0]], ids=[[2] * 40 + [4], [6, 6, 0]])
     check_full(tbe, p)
@@ -116,7 +126,7 @@ def test_all_empty_and_zero_batch(tbe):
     assert out.shape == (0, 8) and st == 0
 
 
-def test_bad_ids_reported_and_skipped(tbe):
+def test_bad_ids_reported_and_skipped(tbe, gather_mode):
     p = make_problem(2, 4, rows=[50, 60], D=[16, 8], weights_dtype=[DT_F32, DT_F16], out_dtype=DT_F32,
                      lengths=[[3, 2, 0, 1], [1, 1, 4, 0]], ids=[[1, 50, 3, -2, 7, 9], [59, 60, 1, 2, -1, 99999]])
     out, st, w_host = run_forward(tbe, p)
@@ -127,7 +137,7 @@ def test_bad_ids_reported_and_skipped(tbe):
 
 
 @pytest.mark.parametrize("bad", [[1, 2, 4, 5], [0, 2, 4, 4], [0, 4, 2, 5], [0, 2, 4, 9]])
-def test_bad_offsets_reported(tbe, bad):
+def test_bad_offsets_reported(tbe, gather_mode, bad):
     p = make_problem(1, 3, rows=[50], D=[16], weights_dtype=[DT_F32], out_dtype=DT_F32,
                      lengths=[[2, 2, 1]], ids=[[1, 2, 3, 4, 5]])
     w_dev, _ = parity.weights_pair(p)
@@ -139,7 +149,7 @@ def test_bad_offsets_reported(tbe, bad):
     assert int(st.item()) & tbe.TBE_DEV_BAD_OFFSETS
 
 
-def test_deterministic(tbe):
+def test_deterministic(tbe, gather_mode):
     p = make_config("mid_skewed")
     w_dev, _ = parity.weights_pair(p)
     d = parity.upload(p)
@@ -155,7 +165,7 @@ def test_deterministic(tbe):
 def test_unroll_variants(tbe, unroll, lpr, per_sm):
     old = tbe.get_tuning()
     try:
-        tbe.set_tuning(fwd_unroll=unroll, fwd_lanes_per_row=lpr, fwd_blocks_per_sm=per_sm)
+        tbe.set_tuning(fwd_unroll=unroll, fwd_lanes_per_row=lpr, fwd_blocks_per_sm=per_sm, fwd_ring=0)
         p = make_config("mixed", B=64, rows_scale=0.005)
         check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
     finally:
