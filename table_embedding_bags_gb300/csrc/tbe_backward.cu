@@ -1204,12 +1204,14 @@ struct Acc {
     v[1] = v[0];
   }
   template <bool W>
-  __device__ __forceinline__ void add(int s, const float4& g, float w) {
-    // weighted: the product is rounded to fp32, then added (w = 1 is exact)
-    v[s].x = __fadd_rn(v[s].x, W ? __fmul_rn(w, g.x) : g.x);
-    v[s].y = __fadd_rn(v[s].y, W ? __fmul_rn(w, g.y) : g.y);
-    v[s].z = __fadd_rn(v[s].z, W ? __fmul_rn(w, g.z) : g.z);
-    v[s].w = __fadd_rn(v[s].w, W ? __fmul_rn(w, g.w) : g.w);
+  __device__ __forceinline__ void add(int s, float4 g, float w) {
+    // weighted: the product is rounded to fp32, then added
+    if (W) {
+      mul2(g.x, g.y, w);
+      mul2(g.z, g.w, w);
+    }
+    add2(v[s].x, v[s].y, g.x, g.y);
+    add2(v[s].z, v[s].w, g.z, g.w);
   }
   __device__ __forceinline__ float4 sum() const {
     return make_float4(__fadd_rn(v[0].x, v[1].x), __fadd_rn(v[0].y, v[1].y), __fadd_rn(v[0].z, v[1].z),
@@ -1219,11 +1221,13 @@ struct Acc {
 
 // acc += w * g (weighted: the product is rounded to fp32, then added)
 template <bool W>
-__device__ __forceinline__ void add_slice(float4& acc, const float4& g, float w) {
-  acc.x = __fadd_rn(acc.x, W ? __fmul_rn(w, g.x) : g.x);
-  acc.y = __fadd_rn(acc.y, W ? __fmul_rn(w, g.y) : g.y);
-  acc.z = __fadd_rn(acc.z, W ? __fmul_rn(w, g.z) : g.z);
-  acc.w = __fadd_rn(acc.w, W ? __fmul_rn(w, g.w) : g.w);
+__device__ __forceinline__ void add_slice(float4& acc, float4 g, float w) {
+  if (W) {
+    mul2(g.x, g.y, w);
+    mul2(g.z, g.w, w);
+  }
+  add2(acc.x, acc.y, g.x, g.y);
+  add2(acc.z, acc.w, g.z, g.w);
 }
 
 __device__ __forceinline__ float4 ld_grad(const float* p) {

@@ -128,12 +128,12 @@ __device__ __forceinline__ void pool_bag(const FwdArgs& a, const TableMeta& m, i
             for (int k = 0; k < KMAX; ++k) {
               float f[E];
               Chunk<DT>::to_float(v[u][k], f);
+              if (WT && weighted) {  // the product is rounded to fp32, then added
 #pragma unroll
-              for (int e = 0; e < E; ++e) {
-                // weighted: the product is rounded to fp32, then added
-                const float term = (WT && weighted) ? __fmul_rn(w[u], f[e]) : f[e];
-                acc[u % NS][k][e] = __fadd_rn(acc[u % NS][k][e], term);
+                for (int e = 0; e < E; e += 2) mul2(f[e], f[e + 1], w[u]);
               }
+#pragma unroll
+              for (int e = 0; e < E; e += 2) add2(acc[u % NS][k][e], acc[u % NS][k][e + 1], f[e], f[e + 1]);
             }
           }
         }
@@ -393,9 +393,12 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
 #pragma unroll
           for (int e = 0; e < E; ++e) f[e] = 0.f;
         }
+        if (WT && weighted) {
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-          acc[k][e] = __fadd_rn(acc[k][e], (WT && weighted) ? __fmul_rn(w, f[e]) : f[e]);
+          for (int e = 0; e < E; e += 2) mul2(f[e], f[e + 1], w);  // products rounded, then added
+        }
+#pragma unroll
+        for (int e = 0; e < E; e += 2) add2(acc[k][e], acc[k][e + 1], f[e], f[e + 1]);
       }
       if (j + RD < nwin) issue(j + RD, slot);  // refill the slot just read
       cp_commit();

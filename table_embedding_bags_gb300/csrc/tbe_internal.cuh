@@ -95,6 +95,29 @@ __device__ __forceinline__ float ld_stream_f32(const float* p) {
   return v;
 }
 
+// x += a, y += b as one packed fp32x2 add (two IEEE round-to-nearest adds,
+// bit-identical to two __fadd_rn, half the instructions).
+__device__ __forceinline__ void add2(float& x, float& y, float a, float b) {
+  asm("{\n\t.reg .b64 p, q;\n\t"
+      "mov.b64 p, {%0, %1};\n\t"
+      "mov.b64 q, {%2, %3};\n\t"
+      "add.rn.f32x2 p, p, q;\n\t"
+      "mov.b64 {%0, %1}, p;\n\t}"
+      : "+f"(x), "+f"(y)
+      : "f"(a), "f"(b));
+}
+
+// (a, b) * w as one packed fp32x2 multiply (each product rounded once).
+__device__ __forceinline__ void mul2(float& a, float& b, float w) {
+  asm("{\n\t.reg .b64 p, q;\n\t"
+      "mov.b64 p, {%0, %1};\n\t"
+      "mov.b64 q, {%2, %2};\n\t"
+      "mul.rn.f32x2 p, p, q;\n\t"
+      "mov.b64 {%0, %1}, p;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "f"(w));
+}
+
 // Elements of a 16-byte chunk as floats.
 template <int DT>
 struct Chunk;
