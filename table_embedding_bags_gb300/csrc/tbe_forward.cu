@@ -371,36 +371,44 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
       if (WT) wts[idx] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
     }
     __syncwarp(vmask);
+    // rows go in pairs: one copy group, one wait and one loop trip per pair
 #pragma unroll 1
-    for (int j = 0; j < RD; ++j) {  // the first RD rows
+    for (int j = 0; j < RD; j += 2) {  // the first RD rows
       if (j < nwin) issue(j, j);
+      if (j + 1 < nwin) issue(j + 1, j + 1);
       cp_commit();
     }
 #pragma unroll 1
-    for (int j = 0; j < nwin; ++j) {
-      cp_wait<RD - 1>();  // row j has landed
-      const int32_t id = ids[j];
-      bad |= id < 0;
-      const int slot = j & (RD - 1);
-      const float w = WT ? wts[j] : 1.f;
+    for (int j = 0; j < nwin; j += 2) {
+      cp_wait<RD / 2 - 1>();  // rows j and j + 1 have landed
 #pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-        const int c = sub + k * lpr;
-        float f[E];
-        if (c < C && id >= 0) {
-          Chunk<DT>::to_float(lds128(ring + (slot * KMAX + k) * kRingStride), f);
-        } else {
+      for (int h = 0; h < 2; ++h) {
+        const int jj = j + h;
+        if (jj >= nwin) break;
+        const int32_t id = ids[jj];
+        bad |= id < 0;
+        const int slot = jj & (RD - 1);
+        const float w = WT ? wts[jj] : 1.f;
 #pragma unroll
-          for (int e = 0; e < E; ++e) f[e] = 0.f;
+        for (int k = 0; k < KMAX; ++k) {
+          const int c = sub + k * lpr;
+          float f[E];
+          if (c < C && id >= 0) {
+            Chunk<DT>::to_float(lds128(ring + (slot * KMAX + k) * kRingStride), f);
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) f[e] = 0.f;
+          }
+          if (WT && weighted) {
+#pragma unroll
+            for (int e = 0; e < E; e += 2) mul2(f[e], f[e + 1], w);  // products rounded, then added
+          }
+#pragma unroll
+          for (int e = 0; e < E; e += 2) add2(acc[k][e], acc[k][e + 1], f[e], f[e + 1]);
         }
-        if (WT && weighted) {
-#pragma unroll
-          for (int e = 0; e < E; e += 2) mul2(f[e], f[e + 1], w);  // products rounded, then added
-        }
-#pragma unroll
-        for (int e = 0; e < E; e += 2) add2(acc[k][e], acc[k][e + 1], f[e], f[e + 1]);
       }
-      if (j + RD < nwin) issue(j + RD, slot);  // refill the slot just read
+      if (j + RD < nwin) issue(j + RD, j & (RD - 1));  // refill the two slots just read
+      if (j + 1 + RD < nwin) issue(j + 1 + RD, (j + 1) & (RD - 1));
       cp_commit();
     }
     __syncwarp(vmask);  // the ids are rewritten by the next window
