@@ -308,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, MINB) fwd_gather_kernel(const FwdArg
 // their id by index.
 // ---------------------------------------------------------------------------
 constexpr int kRing = 16;      // 16-byte slots per lane
-constexpr int kRingLanes = 16; // most lanes per row: two bags per warp at least
 constexpr int kRingStride = kThreads * 16;  // bytes between a thread's ring slots
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -451,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 3) fwd_ring_kernel(const FwdArgs a) 
     int32_t mine = 0;
     for (int q = 0; q < per; ++q) {
       const int t = tid * per + q;
-      if (t < a.T) mine += (a.B + (32 / lanes_per_row(load_meta(a.meta + t), kRingLanes)) - 1) /
-                           (32 / lanes_per_row(load_meta(a.meta + t), kRingLanes));
+      if (t < a.T) mine += (a.B + (32 / lanes_per_row(load_meta(a.meta + t), a.lpr_max)) - 1) /
+                           (32 / lanes_per_row(load_meta(a.meta + t), a.lpr_max));
     }
     int32_t x = mine;
 #pragma unroll
@@ -468,15 +467,14 @@ __global__ void __launch_bounds__(kThreads, 3) fwd_ring_kernel(const FwdArgs a) 
       const int t = tid * per + q;
       if (t < a.T) {
         s_pref[t] = run;
-        const int G = 32 / lanes_per_row(load_meta(a.meta + t), kRingLanes);
+        const int G = 32 / lanes_per_row(load_meta(a.meta + t), a.lpr_max);
         run += (a.B + G - 1) / G;
       }
     }
     if (tid == kThreads - 1) s_pref[a.T] = run;
     __syncthreads();
   }
-  FwdArgs ar = a;
-  ar.lpr_max = kRingLanes;
+  const FwdArgs& ar = a;
   const int32_t ntasks = s_pref[a.T];
   const int32_t nw = (int32_t)((gridDim.x * kThreads) >> 5);
   const int32_t nb = a.T * a.B;

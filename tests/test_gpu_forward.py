@@ -172,6 +172,19 @@ def test_unroll_variants(tbe, unroll, lpr, per_sm):
         tbe.set_tuning(**old)
 
 
+@pytest.mark.parametrize("lpr", [1, 4, 8, 32])
+def test_ring_lanes_per_row(tbe, lpr):
+    """The ring gather with one bag per warp up to 32 bags per warp (two
+    chunks per lane where the row is wider than the lanes)."""
+    old = tbe.get_tuning()
+    try:
+        tbe.set_tuning(fwd_lanes_per_row=lpr, fwd_ring=1)
+        check_full(tbe, make_config("mixed", B=64, rows_scale=0.005), path=tbe.TBE_PATH_GATHER)
+        check_full(tbe, make_config("mid_skewed", B=128, rows_scale=0.1), path=tbe.TBE_PATH_GATHER)
+    finally:
+        tbe.set_tuning(**old)
+
+
 def test_host_argument_errors(tbe):
     p = make_config("tiny")
     w_dev, _ = parity.weights_pair(p)
