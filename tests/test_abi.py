@@ -48,6 +48,29 @@ def test_host_only_calls(lib):
     with pytest.raises(tbe.TBEError):
         tbe.set_tuning(long_chunk=33)
     assert tbe.get_tuning() == t
+
+
+@pytest.mark.parametrize("field,bad", [("fwd_lanes_per_row", 3), ("fwd_lanes_per_row", 64), ("fwd_lanes_per_row", 0),
+                                       ("red_unroll", 6), ("fwd_ring", 2), ("short_item_lookups", 31),
+                                       ("fwd_blocks_per_sm", -1), ("long_run_threshold", 0)])
+def test_tuning_rejects_out_of_range(lib, field, bad):
+    t = tbe.get_tuning()
+    with pytest.raises(tbe.TBEError):
+        tbe.set_tuning(**{field: bad})
+    assert tbe.get_tuning() == t  # a rejected call changes nothing
+
+
+def test_tuning_round_trip(lib):
+    t = tbe.get_tuning()
+    assert t["long_chunk"] == 0 and t["fwd_ring"] == 1 and t["red_unroll"] in (4, 8)
+    try:
+        tbe.set_tuning(long_chunk=128, short_item_lookups=64, fwd_lanes_per_row=8, red_unroll=8, fwd_ring=0)
+        u = tbe.get_tuning()
+        assert (u["long_chunk"], u["short_item_lookups"], u["fwd_lanes_per_row"], u["red_unroll"], u["fwd_ring"]) == \
+            (128, 64, 8, 8, 0)
+    finally:
+        tbe.set_tuning(**t)
+    assert tbe.get_tuning() == t
     # null arguments are rejected on the host before any CUDA call
     assert lib.tbe_plan_create(None, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_forward(None, None, None, 0, None, 0, None, None, None, None) == tbe.TBE_ERR_INVALID_ARG
