@@ -250,7 +250,7 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.psw_sorted = take(4 * (size_t)N);
   L.run_starts = take(4 * (size_t)(N + 1));
   L.run_table = take(4 * (size_t)N);
-  L.long_list = take(16 * (size_t)L.long_cap);
+  L.long_list = take(16 * (size_t)L.chunk_cap);  // one record per chunk
   L.sub_list = take(8 * (size_t)L.sub_cap);
   L.gofs = take(8 * (size_t)(p.T + 1));
   L.partials = take(4 * (size_t)L.chunk_cap * L.slot_floats);
@@ -1054,7 +1054,7 @@ struct ClsArgs {
   const int64_t* unique_rows;
   const int32_t* run_starts;
   const TableMeta* meta;
-  int4* long_list;          // {u, first chunk, chunks, length}
+  int4* long_list;          // per chunk: {run u, its first chunk, chunks, length}
   unsigned long long* long_counter;  // (runs << 32) | chunks
   uint32_t* counters;
   int2* sub_list;           // short-run work items {batch, part}
@@ -1141,10 +1141,10 @@ __global__ void __launch_bounds__(kClsThreads) classify_kernel(const ClsArgs a) 
       s_base = atomicAdd(a.long_counter, ((unsigned long long)t0 << 32) | (unsigned long long)t1);
     if (tid == 32 && t2 > 0) s_sub_base = atomicAdd(&a.counters[kCntSub * kCntStride], t2);
     __syncthreads();
-    if (is_long) {
-      const uint32_t lpos = (uint32_t)(s_base >> 32) + w0 + x0 - 1;
+    if (is_long) {  // every chunk of the run gets the run's record, so a chunk finds its run in one load
       const uint32_t cpos = (uint32_t)(s_base & 0xffffffffu) + w1 + x1 - nch;
-      a.long_list[lpos] = make_int4(u, (int)cpos, (int)nch, len);
+      const int4 rec = make_int4(u, (int)cpos, (int)nch, len);
+      for (uint32_t k = 0; k < nch; ++k) a.long_list[cpos + k] = rec;
     }
     for (uint32_t k = lane; k < nsub; k += 32)
       a.sub_list[s_sub_base + w2 + k] = make_int2((u0 >> 5) + warp, (int)k);
@@ -1298,15 +1298,7 @@ __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int3
 // every sum is fixed, so the result does not depend on arrival order.
 template <bool W, int UNR>
 __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
-  const unsigned long long lc = *a.long_counter;
-  const int32_t n_long = (int32_t)(lc >> 32);
-  // long run whose first chunk e0 <= item (first chunks ascend along the list)
-  int lo = 0, hi = n_long - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (a.long_list[mid].y <= item) lo = mid; else hi = mid - 1;
-  }
-  const int4 rec = a.long_list[lo];
+  const int4 rec = a.long_list[item];  // the record of the chunk's run
   const int32_t u = rec.x, e0 = rec.y, nch = rec.z, len = rec.w;
   const int32_t k = item - e0;
   const RunInfo r = run_info(a, u);
