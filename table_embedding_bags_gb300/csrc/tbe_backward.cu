@@ -1185,13 +1185,23 @@ struct RunInfo {
   int32_t weighted;
 };
 
+// Per-table row-gradient offsets and unique-row counts staged in shared
+// memory by every reduce block when the batch has at most kRedSmemT tables
+// (one dependent global load less per work item).
+constexpr int kRedSmemT = 256;
+__shared__ int64_t s_red_gofs[kRedSmemT + 1];
+__shared__ int64_t s_red_uc[kRedSmemT + 1];
+
 __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
   const int32_t t = a.run_table[u];
   RunInfo r;
   r.D = __ldg(&a.meta[t].D);
   r.col_off = __ldg(&a.meta[t].col_off);
   r.weighted = (a.psw_sorted != nullptr) && __ldg(&a.meta[t].weighted);
-  r.out_off = a.gofs[t] + (int64_t)(u - a.unique_count[t]) * r.D;
+  const bool staged = a.T <= kRedSmemT;
+  const int64_t go = staged ? s_red_gofs[t] : a.gofs[t];
+  const int64_t uc = staged ? s_red_uc[t] : a.unique_count[t];
+  r.out_off = go + (int64_t)(u - uc) * r.D;
   return r;
 }
 
@@ -1479,6 +1489,13 @@ template <bool W, int UNR, int MINB>
 __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs a) {
   wait_predecessor();
   release_dependents();
+  if (a.T <= kRedSmemT) {
+    for (int t = threadIdx.x; t <= a.T; t += kRedThreads) {
+      s_red_gofs[t] = a.gofs[t];
+      s_red_uc[t] = a.unique_count[t];
+    }
+    __syncthreads();
+  }
   const int lane = threadIdx.x & 31;
   const int32_t U = (int32_t)a.counters[kCntU * kCntStride];
   const int32_t n_chunks = (int32_t)(*a.long_counter & 0xffffffffu);
