@@ -77,6 +77,9 @@ def load(path: str | None = None):
     lib.orc_backward_indexing.argtypes = [i32, i32, P, P, i64, P, P, P, P, P, P]
     lib.orc_backward_values.restype = ctypes.c_int
     lib.orc_backward_values.argtypes = [i32, i32, P, P, P, P, i64, P, P, P, P, P, P, i64, P, P, P, i32]
+    lib.orc_exact_update.restype = ctypes.c_int
+    lib.orc_exact_update.argtypes = [i32, P, P, P, P, P, i32, ctypes.c_double, ctypes.c_double, P, i64, P, P,
+                                     P, P, P]
     if path == _LIB:
         _lib = lib
     return lib
@@ -229,6 +232,44 @@ def backward_values(layout: dict, offsets, B: int, grad_out, idx: dict, per_samp
                                  _p(ur), _p(rs), _p(sp), _p(runs), runs.shape[0], _p(pos), _p(s),
                                  _p(a), nthreads)
     return st, s[:n], a[:n], pos
+
+
+EXACT_SGD, EXACT_ROWWISE_ADAGRAD = 0, 1
+
+
+def exact_update(layout: dict, weights, kind: int, lr: float, eps: float, rows, grads, g_pos=None,
+                 momentum=None, lib=None):
+    """One exact optimizer step on finished row gradients.
+
+    ``rows``: global rows; ``grads``: flat float64 values, row k's D_t values
+    at ``g_pos[k]`` (default: back to back in the order listed);
+    ``momentum``: fp32 [total_rows] state before the step (Adagrad only).
+    Returns (status, w_new, m_new): the updated weights in double, unrounded,
+    at the same flat positions as ``grads``, and the new momentum of each
+    listed row (zeros for SGD)."""
+    lib = lib or load()
+    T = int(layout["T"])
+    trb = _c(layout["table_row_base"], np.int64)
+    doff = _c(layout["D_offsets"], np.int32)
+    woff = _c(layout["weights_offsets"], np.int64)
+    wdt = _c(layout["weights_dtype"], np.int32)
+    w = _weights_np(weights)
+    r = _c(rows, np.int64)
+    g = _c(grads, np.float64)
+    if g_pos is None:
+        D = np.diff(doff).astype(np.int64)
+        t_of = np.searchsorted(trb, r, side="right") - 1 if r.size else np.zeros(0, np.int64)
+        widths = D[np.clip(t_of, 0, T - 1)] if r.size else np.zeros(0, np.int64)
+        g_pos = np.concatenate([[0], np.cumsum(widths)[:-1]]) if r.size else np.zeros(0, np.int64)
+    gp = _c(g_pos, np.int64)
+    m = _c(momentum, np.float32)
+    if kind == EXACT_ROWWISE_ADAGRAD and m is None:
+        raise ValueError("row-wise Adagrad needs the momentum state")
+    w_new = np.zeros(max(g.size, 1), np.float64)
+    m_new = np.zeros(max(r.size, 1), np.float64)
+    st = lib.orc_exact_update(T, _p(trb), _p(doff), _p(woff), _p(wdt), _p(w), int(kind), float(lr), float(eps),
+                              _p(m), r.size, _p(r), _p(g), _p(gp), _p(w_new), _p(m_new))
+    return st, w_new[:g.size], m_new[:r.size]
 
 
 def problem_forward(p, weights_host, bags=None, nthreads=0, lib=None):

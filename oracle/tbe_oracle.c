@@ -27,6 +27,9 @@
  *     [FBT] "Why the backward is the hard half".
  *   - Weighted backward pairs each lookup with its own weight through a
  *     stable ordering: [FBT] "Using it, and the import that stops you".
+ *   - Exact optimizers (SGD, row-wise Adagrad) applied once per distinct
+ *     row to its finished gradient: [FBT] "Why the backward is the hard
+ *     half".
  *
  * Readings where the page is silent (each is stated beside its use):
  *   ids are table-local; an id outside [0, rows_t) is reported and contributes
@@ -371,4 +374,53 @@ int orc_backward_values(int32_t T, int32_t B, const int64_t* table_row_base,
   }
   free(bag_of);
   return bad ? ORC_BAD_ARG : 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* exact optimizer step on finished row gradients                             */
+/* ------------------------------------------------------------------------- */
+
+/* [FBT] "Why the backward is the hard half": the optimizer runs inside the
+ * backward, once per distinct row, on that row's finished gradient g (the
+ * sum over its run), never once per lookup.  Two kinds:
+ *   kind 0, exact SGD (the plain reading: the step is lr times g):
+ *       W[r] <- W[r] - lr * g
+ *   kind 1, exact row-wise Adagrad (one momentum scalar per row, fed by the
+ *   mean of the squared gradient over the row's D_t columns):
+ *       m[r] <- m[r] + (sum_c g_c^2) / D_t
+ *       W[r] <- W[r] - lr / (sqrt(m[r]) + eps) * g
+ * For each listed row k (global row rows[k], gradient values
+ * grads[g_pos[k] + c], c < D_t) the updated weights are written in double,
+ * unrounded, to w_new[g_pos[k] + c]: the caller rounds to the table dtype
+ * where it needs to.  For Adagrad, momentum[] is the state before the step
+ * (fp32, indexed by global row) and the new value goes to m_new[k].
+ * Returns ORC_BAD_INDEX if a listed row lies outside every table,
+ * ORC_BAD_ARG for an unknown kind. */
+int orc_exact_update(int32_t T, const int64_t* table_row_base, const int32_t* D_offsets,
+                     const int64_t* weights_offsets, const int32_t* weights_dtype,
+                     const uint8_t* weights, int32_t kind, double lr, double eps,
+                     const float* momentum, int64_t n_rows, const int64_t* rows,
+                     const double* grads, const int64_t* g_pos, double* w_new, double* m_new) {
+  if (kind != 0 && kind != 1) return ORC_BAD_ARG;
+  for (int64_t k = 0; k < n_rows; ++k) {
+    int64_t row = rows[k];
+    if (row < 0 || row >= table_row_base[T]) return ORC_BAD_INDEX;
+    int32_t t = 0;
+    while (table_row_base[t + 1] <= row) ++t;
+    int32_t D = D_offsets[t + 1] - D_offsets[t];
+    int64_t id = row - table_row_base[t];
+    const double* g = grads + g_pos[k];
+    double step = lr;
+    if (kind == 1) {
+      double sq = 0.0;
+      for (int32_t c = 0; c < D; ++c) sq += g[c] * g[c];
+      double m = (double)momentum[row] + sq / (double)D;
+      m_new[k] = m;
+      step = lr / (sqrt(m) + eps);
+    }
+    for (int32_t c = 0; c < D; ++c)
+      w_new[g_pos[k] + c] =
+          table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) - step * g[c];
+  }
+  return 0;
 }

@@ -19,6 +19,16 @@ AssertionError on a mismatch.  What pins what:
   search.
 * ``pin_special_cases`` -- all-empty batch, single-id bags, one id repeated
   n times, out-of-range ids, broken offsets.
+* ``pin_optimizer_hand`` -- exact SGD and row-wise Adagrad steps worked by
+  hand (tests/golden/optimizer_example.json), with momentum carried over
+  from an earlier step and with and without eps.
+* ``pin_optimizer_invariants`` -- properties the update must have whatever
+  the data: a first Adagrad step from zero momentum (eps 0) moves each row
+  by exactly lr * sqrt(D_t) in Euclidean norm and is unchanged when the
+  gradient is scaled; duplicating every column leaves momentum and update
+  unchanged (a mean, not a sum); SGD is linear in the gradient; Adagrad
+  whose denominator sqrt(m) + eps equals 1 is SGD; rows outside every
+  table are reported.
 """
 
 from __future__ import annotations
@@ -316,5 +326,108 @@ def pin_special_cases(lib):
         assert st == oracle.BAD_OFFSETS, bad
 
 
+def _flat_tables(tables):
+    return np.array([v for t in tables for row in t for v in row], np.float64)
+
+
+def pin_optimizer_hand(lib):
+    g = json.load(open(os.path.join(GOLDEN, "optimizer_example.json")))
+    _, p = _hand_problem(False)
+    w = materialize_weights(p)
+    lay = p.layout_arrays()
+    rows = np.array(g["rows"], np.int64)
+    grads = np.array([v for r in g["row_grads"] for v in r], np.float64)
+    st, w_new, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, g["sgd"]["lr"], 0.0, rows, grads, lib=lib)
+    assert st == 0
+    np.testing.assert_allclose(w_new, _flat_tables(g["sgd"]["expected_tables"]), rtol=1e-15, atol=0)
+    for case in ("adagrad", "adagrad_eps"):
+        c = g[case]
+        mom = np.array(c["momentum_before"], np.float32)
+        st, w_new, m_new = oracle.exact_update(lay, w, oracle.EXACT_ROWWISE_ADAGRAD, c["lr"], c["eps"], rows,
+                                               grads, momentum=mom, lib=lib)
+        assert st == 0
+        np.testing.assert_array_equal(m_new, c["expected_momentum"])
+        np.testing.assert_allclose(w_new, _flat_tables(c["expected_tables"]), rtol=1e-15, atol=1e-15)
+
+
+def _opt_problem(rng, T=5, dtypes=(DT_F32, DT_F16, DT_BF16)):
+    p = _random_problem(rng, T, 3, list(dtypes), False, max_rows=12)
+    w = materialize_weights(p)
+    lay = p.layout_arrays()
+    total = int(p.table_row_base[-1])
+    rows = np.sort(rng.choice(total, size=min(total, 9), replace=False)).astype(np.int64)
+    D = p.D.astype(np.int64)
+    t_of = np.searchsorted(p.table_row_base, rows, side="right") - 1
+    widths = D[t_of]
+    grads = rng.standard_normal(int(widths.sum()))
+    pos = np.concatenate([[0], np.cumsum(widths)[:-1]]).astype(np.int64)
+    return p, w, lay, rows, grads, widths, pos
+
+
+def pin_optimizer_invariants(lib, trials=20, seed=23):
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        p, w, lay, rows, grads, widths, pos = _opt_problem(rng)
+        total = int(p.table_row_base[-1])
+        zero = np.zeros(total, np.float32)
+        lr = float(rng.uniform(0.01, 2.0))
+        st, w0, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, 0.0, 0.0, rows, grads, lib=lib)
+        assert st == 0  # lr 0: the table as stored, in double
+        # first Adagrad step from zero momentum, eps 0: |dW_row| = lr * sqrt(D_t), scale-free in g
+        st, w1, m1 = oracle.exact_update(lay, w, oracle.EXACT_ROWWISE_ADAGRAD, lr, 0.0, rows, grads,
+                                         momentum=zero, lib=lib)
+        assert st == 0
+        st, w1s, m1s = oracle.exact_update(lay, w, oracle.EXACT_ROWWISE_ADAGRAD, lr, 0.0, rows, 3.5 * grads,
+                                           momentum=zero, lib=lib)
+        np.testing.assert_allclose(w1s, w1, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(m1s, 12.25 * m1, rtol=1e-13)
+        for k, (s0, n) in enumerate(zip(pos, widths)):
+            step = np.linalg.norm(w1[s0:s0 + n] - w0[s0:s0 + n])
+            np.testing.assert_allclose(step, lr * np.sqrt(n), rtol=1e-12)
+        # SGD is linear in the gradient
+        g2 = rng.standard_normal(grads.size)
+        st, wa, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, lr, 0.0, rows, grads, lib=lib)
+        st, wb, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, lr, 0.0, rows, g2, lib=lib)
+        st, wab, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, lr, 0.0, rows, grads + g2, lib=lib)
+        np.testing.assert_allclose(wab - w0, (wa - w0) + (wb - w0), rtol=1e-12, atol=1e-12)
+        assert np.all((wa != w0) == (grads != 0))
+        # Adagrad whose denominator sqrt(m) + eps is 1 takes the SGD step (one row at a time;
+        # a gradient of 0.5 everywhere has mean square 0.25)
+        for k in range(min(3, rows.size)):
+            s0, n = int(pos[k]), int(widths[k])
+            gk = np.zeros(n) + 0.5  # mean square 0.25
+            mom = zero.copy()
+            mom[rows[k]] = 0.75  # m after the step = 1.0 -> sqrt = 1, eps 0 -> factor lr
+            st, wad, mad = oracle.exact_update(lay, w, oracle.EXACT_ROWWISE_ADAGRAD, lr, 0.0, rows[k:k + 1], gk,
+                                               momentum=mom, lib=lib)
+            st, wsg, _ = oracle.exact_update(lay, w, oracle.EXACT_SGD, lr, 0.0, rows[k:k + 1], gk, lib=lib)
+            assert mad[0] == 1.0
+            np.testing.assert_array_equal(wad, wsg)
+            mom[rows[k]] = 0.0  # m after = 0.25 -> sqrt 0.5; eps 0.5 makes the denominator 1 again
+            st, wad2, _ = oracle.exact_update(lay, w, oracle.EXACT_ROWWISE_ADAGRAD, lr, 0.5, rows[k:k + 1], gk,
+                                              momentum=mom, lib=lib)
+            np.testing.assert_array_equal(wad2, wsg)
+    # duplicating every column (W -> [W, W], g -> [g, g]) keeps momentum and update
+    import torch
+
+    tbl = rng.standard_normal((4, 3)).astype(np.float32)
+    one = make_problem(1, 1, rows=[4], D=[3], weights_dtype=[DT_F32], out_dtype=DT_F32, lengths=[[0]], ids=[[]],
+                       host_tables={0: torch.from_numpy(tbl)})
+    two = make_problem(1, 1, rows=[4], D=[6], weights_dtype=[DT_F32], out_dtype=DT_F32, lengths=[[0]], ids=[[]],
+                       host_tables={0: torch.from_numpy(np.concatenate([tbl, tbl], axis=1))})
+    g = rng.standard_normal(3)
+    mom = np.array([0.3, 1.7, 0.0, 2.5], np.float32)
+    st, wo, mo = oracle.exact_update(one.layout_arrays(), materialize_weights(one), oracle.EXACT_ROWWISE_ADAGRAD,
+                                     0.7, 1e-3, [2], g, momentum=mom, lib=lib)
+    st, wt, mt = oracle.exact_update(two.layout_arrays(), materialize_weights(two), oracle.EXACT_ROWWISE_ADAGRAD,
+                                     0.7, 1e-3, [2], np.concatenate([g, g]), momentum=mom, lib=lib)
+    np.testing.assert_allclose(mt, mo, rtol=1e-15)
+    np.testing.assert_allclose(wt, np.concatenate([wo, wo]), rtol=1e-15)
+    # a row outside every table is reported
+    st, _, _ = oracle.exact_update(one.layout_arrays(), materialize_weights(one), oracle.EXACT_SGD, 1.0, 0.0,
+                                   [4], np.ones(3), lib=lib)
+    assert st == oracle.BAD_INDEX
+
+
 ALL_PINS = [pin_hand_example, pin_dense_onehot, pin_invariants, pin_sort_vs_numpy, pin_formats,
-            pin_special_cases]
+            pin_special_cases, pin_optimizer_hand, pin_optimizer_invariants]

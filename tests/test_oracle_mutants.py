@@ -44,6 +44,18 @@ MUTANTS = {
     "histogram_transposed": ("counts[(int64_t)b * rows_t + id] += 1;", "counts[(int64_t)id * B + b] += 1;"),
     "bwd_unsorted_position": ("int32_t pos = sorted_pos[j];", "int32_t pos = (int32_t)j;"),
     "offsets_not_checked": ("if (offsets[g + 1] < offsets[g]) return ORC_BAD_OFFSETS;", ";"),
+    "adagrad_sum_not_mean": ("double m = (double)momentum[row] + sq / (double)D;",
+                             "double m = (double)momentum[row] + sq;"),
+    "adagrad_momentum_reset": ("double m = (double)momentum[row] + sq / (double)D;",
+                               "double m = sq / (double)D;"),
+    "adagrad_momentum_by_id": ("double m = (double)momentum[row] + sq / (double)D;",
+                               "double m = (double)momentum[id] + sq / (double)D;"),
+    "adagrad_eps_inside_sqrt": ("step = lr / (sqrt(m) + eps);", "step = lr / sqrt(m + eps);"),
+    "adagrad_rms_of_update": ("step = lr / (sqrt(m) + eps);", "step = lr / (m + eps);"),
+    "update_sign": ("table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) - step * g[c];",
+                    "table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) + step * g[c];"),
+    "update_reads_first_row": ("table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) - step * g[c];",
+                               "table_elem(weights, weights_offsets[t], weights_dtype[t], D, 0, c) - step * g[c];"),
 }
 
 
