@@ -44,6 +44,7 @@ WORKLOAD_DESC = ("TBE mid-size skewed: T=8 fp16 tables x 100000 rows, D=128, B=2
                  "Poisson(20) (one empty bag per table), ids Zipf(1.05) through a per-table permutation, "
                  "fp16 output, fp32 grad_out; forward + backward (row gradients)")
 N_BATCHES = 4
+OPT_LR, OPT_EPS = 0.01, 1e-8  # exact row-wise Adagrad step timed beside the headline
 FLUSH_BYTES = 256 << 20
 
 
@@ -97,6 +98,17 @@ def effective_bytes(p, unique_per_table):
     U = np.asarray(unique_per_table, np.int64)
     bwd = int(np.sum(lens * (4 * D + 8 + 4 * w)) + offs + np.sum(U * (8 + 4 * D)))
     return fwd, bwd
+
+
+def optimizer_bytes(p, U_total):
+    """Algorithmic bytes of one exact row-wise Adagrad step: per distinct row
+    its id (8), its gradient (4 D), its weights read and written (2 D x the
+    table's element size) and its momentum read and written (8); plus the
+    per-table counts.  The mid-size workload has one width and dtype, so U
+    counts rows of every table alike."""
+    D = int(p.D[0])
+    eb = 4 if int(p.weights_dtype[0]) == 0 else 2
+    return U_total * (8 + 4 * D + 2 * eb * D + 8) + 8 * (p.T + 1)
 
 
 def kernel_bytes(p, U_total, npass):
@@ -330,12 +342,21 @@ def run_ours(args, world, rank, local):
     step_graphs = capture_steps()
     graphs = capture(False)
     traced_graphs = capture(True)
+    # exact row-wise Adagrad step on the backward's outputs (timed on its own,
+    # after the backward of the same batch, outside the headline step)
+    total_rows = int(p0.table_row_base[-1])
+    momentum = torch.zeros(total_rows, dtype=torch.float32, device=dev)
+    upd_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(upd_graph):
+        tbe.tbe_exact_update(plan, weights, bufs, tbe.TBE_OPT_EXACT_ROWWISE_ADAGRAD, OPT_LR, OPT_EPS,
+                             momentum=momentum, dev_status=status)
     for k in range(args.warmup):
         flush(k)
         step_graphs[k % N_BATCHES].replay()
         graphs[k % N_BATCHES][0].replay()
         graphs[k % N_BATCHES][1].replay()
         traced_graphs[k % N_BATCHES][1].replay()
+        upd_graph.replay()
     torch.cuda.synchronize()
 
     if world > 1:
@@ -374,6 +395,17 @@ def run_ours(args, world, rank, local):
         for name, ms in tbe.trace_read():
             stage.setdefault(name, []).append(ms)
     torch.cuda.synchronize()
+    upd_ms = []
+    for k in range(args.steps):  # optimizer step after the backward of the same batch
+        flush(k)
+        graphs[k % N_BATCHES][1].replay()
+        e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        e0.record(stream)
+        upd_graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        upd_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -399,6 +431,14 @@ def run_ours(args, world, rank, local):
     dom = max(per_kernel, key=lambda n: per_kernel[n])
     peak, peak_kind = load_peaks()
     achieved = kb[dom] / (per_kernel[dom] * 1e-3) / 1e9
+
+    upd_bytes = optimizer_bytes(p0, U_mean)
+    upd_mean = float(np.mean(upd_ms))
+    optimizer = dict(kind="exact_rowwise_adagrad", lr=OPT_LR, eps=OPT_EPS, ms=upd_mean,
+                     GBps=upd_bytes / (upd_mean * 1e-3) / 1e9, bytes_per_launch=upd_bytes,
+                     frac=upd_bytes / (upd_mean * 1e-3) / 1e9 / peak, peak=peak, peak_kind=f"{peak_kind} (copy)",
+                     placement="timed alone right after the backward of the same batch (row gradients still in L2, "
+                               "tables and momentum flushed with the step's L2 flush)")
 
     # e2e through the public API with host buffers
     e2e = None
@@ -431,6 +471,7 @@ def run_ours(args, world, rank, local):
         roofline=dict(bound="hbm", kernel=dom, achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                       peak_kind=f"{peak_kind} (copy)", bytes_per_launch=kb[dom], launch_ms=per_kernel[dom],
                       traffic=traffic_from_profiles(dom)),
+        optimizer=optimizer,
         clocks=clocks,
         gpu_launches=args.steps * (1 + 4 + npass),
         launch="one CUDA graph per step (forward then backward); backward kernels chained with programmatic dependent launch",

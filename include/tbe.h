@@ -214,6 +214,46 @@ int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, c
                                   int32_t* dev_status, void* stream);
 
 /*
+ * Exact optimizer step ([FBT] "Why the backward is the hard half": the
+ * update runs once per distinct row, on the row's finished gradient, so it
+ * sees the whole sum).  Applies, in place, to every row a tbe_backward call
+ * on the same stream produced (its outputs are passed unchanged):
+ *   TBE_OPT_EXACT_SGD:
+ *       W[r] <- W[r] - learning_rate * g
+ *   TBE_OPT_EXACT_ROWWISE_ADAGRAD (one FP32 momentum scalar per row):
+ *       m[r] <- m[r] + (sum_c g_c^2) / D_t
+ *       W[r] <- W[r] - learning_rate / (sqrt(m[r]) + eps) * g
+ * with g the row's gradient (D_t floats), computed in FP32 and stored
+ * rounded to nearest-even in the table's dtype.
+ *   weights            : device, the packed table buffer, updated in place
+ *   momentum           : device fp32 [table_row_base[T]], one scalar per
+ *                        global row, updated in place; Adagrad only (may be
+ *                        NULL for SGD)
+ *   unique_rows        : device int64, the backward's distinct rows
+ *   max_unique         : capacity of unique_rows (the backward's N); runs at
+ *                        or beyond it are never read
+ *   row_grads, row_grads_capacity, unique_count : the backward's outputs
+ *   dev_status         : device int32 word or NULL
+ * Data errors skip the row and set a bit: TBE_DEV_BAD_INDEX for a row
+ * outside its table, TBE_DEV_CAPACITY for a gradient beyond
+ * row_grads_capacity or unique_count[T] > max_unique.
+ * Errors: TBE_ERR_INVALID_ARG (nulls, an unknown kind, a learning rate or
+ * eps that is not finite, a negative eps), TBE_ERR_UNSUPPORTED (row_grads
+ * or weights not 16-byte aligned, a table width that is not a multiple
+ * of 4). */
+#define TBE_OPT_EXACT_SGD 0
+#define TBE_OPT_EXACT_ROWWISE_ADAGRAD 1
+typedef struct tbe_optimizer {
+  int32_t kind;
+  float learning_rate;
+  float eps;
+} tbe_optimizer;
+int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                     const int64_t* unique_rows, int64_t max_unique, const float* row_grads,
+                     int64_t row_grads_capacity, const int64_t* unique_count, int32_t* dev_status,
+                     void* stream);
+
+/*
  * Tuning knobs (process-wide; set them before launching work that should
  * use them, not concurrently with launches).
  *   long_run_threshold : runs with at least this many lookups take the

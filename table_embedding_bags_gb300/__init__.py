@@ -23,13 +23,14 @@ TBE_DEV_BAD_INDEX, TBE_DEV_BAD_OFFSETS, TBE_DEV_TIMEOUT, TBE_DEV_CAPACITY = 1, 2
 TBE_F32, TBE_F16, TBE_BF16 = 0, 1, 2
 TBE_PATH_AUTO, TBE_PATH_GATHER, TBE_PATH_HISTOGRAM = 0, 1, 2
 TBE_MAX_TABLES = 4096
+TBE_OPT_EXACT_SGD, TBE_OPT_EXACT_ROWWISE_ADAGRAD = 0, 1
 
 # every symbol include/tbe.h declares
 EXPORTED = [
     "tbe_plan_device_bytes", "tbe_plan_create", "tbe_plan_destroy", "tbe_forward", "tbe_forward_path",
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
-    "tbe_backward_static_workspace",
+    "tbe_backward_static_workspace", "tbe_exact_update",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -53,6 +54,10 @@ class Tuning(ctypes.Structure):
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+class Optimizer(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("learning_rate", ctypes.c_float), ("eps", ctypes.c_float)]
 
 
 _lib = None
@@ -85,6 +90,8 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_backward.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, sz, P, P]
     lib.tbe_backward_static_workspace.restype = ctypes.c_int
     lib.tbe_backward_static_workspace.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, P]
+    lib.tbe_exact_update.restype = ctypes.c_int
+    lib.tbe_exact_update.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, i64, P, i64, P, P, P]
     lib.tbe_get_tuning.restype = ctypes.c_int
     lib.tbe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
     lib.tbe_set_tuning.restype = ctypes.c_int
@@ -262,6 +269,19 @@ def tbe_backward_static_workspace(plan: Plan, grad_out, indices, offsets, B: int
                                            _stream(stream))
     _check(rc, "tbe_backward_static_workspace")
     return bufs
+
+
+def tbe_exact_update(plan: Plan, weights, bufs: BackwardBuffers, kind: int, learning_rate: float, eps: float = 0.0,
+                     momentum=None, dev_status=None, stream=None):
+    """One exact optimizer step, in place on ``weights`` (and ``momentum``
+    for row-wise Adagrad), from the outputs of a tbe_backward call that
+    filled ``bufs`` on the same stream."""
+    opt = Optimizer(int(kind), float(learning_rate), float(eps))
+    rc = load_library().tbe_exact_update(plan.handle, ctypes.byref(opt), _ptr(weights), _ptr(momentum),
+                                         _ptr(bufs.unique_rows), bufs.N, _ptr(bufs.row_grads),
+                                         bufs.row_grads_capacity, _ptr(bufs.unique_count), _ptr(dev_status),
+                                         _stream(stream))
+    _check(rc, "tbe_exact_update")
 
 
 def get_tuning() -> dict:

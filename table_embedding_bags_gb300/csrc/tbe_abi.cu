@@ -2,6 +2,7 @@
 // tuning and stage tracing.  Every entry point only enqueues kernels on the
 // caller's stream; none synchronises or allocates device memory.
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -404,6 +405,43 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
   cudaStream_t s = (cudaStream_t)stream;
   trace_begin(s);
   return launch_backward(*plan, a, s);
+}
+
+int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                     const int64_t* unique_rows, int64_t max_unique, const float* row_grads,
+                     int64_t row_grads_capacity, const int64_t* unique_count, int32_t* dev_status,
+                     void* stream) {
+  if (!plan || !opt || max_unique < 0 || row_grads_capacity < 0) return TBE_ERR_INVALID_ARG;
+  if (opt->kind != TBE_OPT_EXACT_SGD && opt->kind != TBE_OPT_EXACT_ROWWISE_ADAGRAD) return TBE_ERR_INVALID_ARG;
+  if (!std::isfinite(opt->learning_rate) || !std::isfinite(opt->eps) || opt->eps < 0.f)
+    return TBE_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TBE_ERR_CUDA;
+  if (dev != plan->device) return TBE_ERR_INVALID_ARG;
+  if (!unique_count) return TBE_ERR_INVALID_ARG;
+  if (max_unique > 0 && (!weights || !unique_rows || (!row_grads && row_grads_capacity > 0)))
+    return TBE_ERR_INVALID_ARG;
+  if (max_unique > 0 && opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum) return TBE_ERR_INVALID_ARG;
+  if (((uintptr_t)row_grads & 15) || ((uintptr_t)weights & 15)) return TBE_ERR_UNSUPPORTED;
+  for (int t = 0; t < plan->T; ++t)
+    if (plan->hmeta[t].D % 4 != 0) return TBE_ERR_UNSUPPORTED;
+  UpdArgs a;
+  a.weights = static_cast<uint8_t*>(weights);
+  a.meta = plan->dmeta;
+  a.momentum = momentum;
+  a.unique_rows = unique_rows;
+  a.row_grads = row_grads;
+  a.unique_count = unique_count;
+  a.max_unique = max_unique;
+  a.row_grads_capacity = row_grads_capacity;
+  a.status = dev_status;
+  a.T = plan->T;
+  a.kind = opt->kind;
+  a.lr = opt->learning_rate;
+  a.eps = opt->eps;
+  cudaStream_t s = (cudaStream_t)stream;
+  trace_begin(s);
+  return launch_exact_update(*plan, a, s);
 }
 
 }  // extern "C"

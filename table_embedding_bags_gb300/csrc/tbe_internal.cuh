@@ -256,4 +256,22 @@ struct BwdArgs {
 size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N);
 int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s);
 
+struct UpdArgs {
+  uint8_t* weights;
+  const TableMeta* meta;
+  float* momentum;
+  const int64_t* unique_rows;
+  const float* row_grads;
+  const int64_t* unique_count;
+  int64_t max_unique;
+  int64_t row_grads_capacity;
+  int32_t* status;
+  int32_t T;
+  int32_t kind;
+  float lr;
+  float eps;
+};
+
+int launch_exact_update(const Plan& p, const UpdArgs& a, cudaStream_t s);
+
 }  // namespace tbe

@@ -75,3 +75,11 @@ def test_tuning_round_trip(lib):
     assert lib.tbe_plan_create(None, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_forward(None, None, None, 0, None, 0, None, None, None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_backward_workspace_bytes(None, 1, 1) == 0
+
+
+def test_exact_update_rejects_without_plan(lib):
+    opt = tbe.Optimizer(tbe.TBE_OPT_EXACT_SGD, 0.1, 0.0)
+    rc = lib.tbe_exact_update(None, ctypes.byref(opt), None, None, None, 0, None, 0, None, None, None)
+    assert rc == tbe.TBE_ERR_INVALID_ARG
+    rc = lib.tbe_exact_update(None, None, None, None, None, 0, None, 0, None, None, None)
+    assert rc == tbe.TBE_ERR_INVALID_ARG
