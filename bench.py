@@ -340,16 +340,17 @@ def run_ours(args, world, rank, local):
         return out_graphs
 
     step_graphs = capture_steps()
-    graphs = capture(False)
-    traced_graphs = capture(True)
     # exact row-wise Adagrad step on the backward's outputs (timed on its own,
-    # after the backward of the same batch, outside the headline step)
+    # after the backward of the same batch, outside the headline step);
+    # captured before the traced graphs, which must be the last traced capture
     total_rows = int(p0.table_row_base[-1])
     momentum = torch.zeros(total_rows, dtype=torch.float32, device=dev)
     upd_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(upd_graph):
         tbe.tbe_exact_update(plan, weights, bufs, tbe.TBE_OPT_EXACT_ROWWISE_ADAGRAD, OPT_LR, OPT_EPS,
                              momentum=momentum, dev_status=status)
+    graphs = capture(False)
+    traced_graphs = capture(True)
     for k in range(args.warmup):
         flush(k)
         step_graphs[k % N_BATCHES].replay()

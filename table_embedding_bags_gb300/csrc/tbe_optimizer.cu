@@ -11,11 +11,12 @@
 //
 // This kernel runs after the backward on the same stream and reads its
 // outputs as they are: unique_rows, the table-major row_grads blocks and the
-// per-table unique counts.  One warp owns one distinct row at a time (rows
-// are distinct, so no two warps touch the same weights or momentum), lanes
-// cover the row four columns each; Adagrad sums the squares with a warp
-// reduction, then every lane applies w - step * g as one fused multiply-add
-// and stores it rounded to nearest-even in the table's dtype.
+// per-table unique counts.  A warp owns a group of consecutive distinct rows
+// at a time (rows are distinct, so no two warps touch the same weights or
+// momentum) and lanes cover a row four columns each; Adagrad sums the
+// squares with a warp reduction, then every lane applies w - step * g as one
+// fused multiply-add and stores it rounded to nearest-even in the table's
+// dtype.
 //
 // Per block, the per-table counts and the start of each table's gradient
 // block (sum over earlier tables of rows * D) are staged in shared memory.
@@ -81,23 +82,66 @@ struct Quad<TBE_BF16> {
   }
 };
 
-// w <- w - step * g over one row, lanes striding by 32 quads.
-template <int DT>
-__device__ __forceinline__ void apply_row(uint8_t* wrow, const float* g, int D, float step, int lane) {
-  for (int c = lane * 4; c < D; c += 128) {
-    const float4 gv = *reinterpret_cast<const float4*>(g + c);
-    uint8_t* p = wrow + (size_t)c * (Quad<DT>::kBytes / 4);
-    float4 w = Quad<DT>::load(p);
-    w.x = fmaf(-step, gv.x, w.x);
-    w.y = fmaf(-step, gv.y, w.y);
-    w.z = fmaf(-step, gv.z, w.z);
-    w.w = fmaf(-step, gv.w, w.w);
-    Quad<DT>::store(p, w);
-  }
+// Four consecutive elements of a row of any table dtype.
+__device__ __forceinline__ float4 load_quad(int dt, const uint8_t* p) {
+  if (dt == TBE_F32) return Quad<TBE_F32>::load(p);
+  if (dt == TBE_F16) return Quad<TBE_F16>::load(p);
+  return Quad<TBE_BF16>::load(p);
+}
+
+__device__ __forceinline__ void store_quad(int dt, uint8_t* p, float4 v) {
+  if (dt == TBE_F32) Quad<TBE_F32>::store(p, v);
+  else if (dt == TBE_F16) Quad<TBE_F16>::store(p, v);
+  else Quad<TBE_BF16>::store(p, v);
+}
+
+__device__ __forceinline__ float4 fma_quad(float step, float4 g, float4 w) {
+  w.x = fmaf(-step, g.x, w.x);
+  w.y = fmaf(-step, g.y, w.y);
+  w.z = fmaf(-step, g.z, w.z);
+  w.w = fmaf(-step, g.w, w.w);
+  return w;
+}
+
+__device__ __forceinline__ float sum_sq(float4 v, float acc) {
+  acc = fmaf(v.x, v.x, acc);
+  acc = fmaf(v.y, v.y, acc);
+  acc = fmaf(v.z, v.z, acc);
+  return fmaf(v.w, v.w, acc);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// Where one distinct row's update reads and writes.
+struct RowJob {
+  const float* g;   // its gradient (D floats)
+  uint8_t* w;       // its weights
+  int64_t row;      // global row (momentum index)
+  int32_t D;
+  int32_t dtype;
+  bool ok;
+};
+
+// Rows per warp in flight: a warp takes kRowsPerWarp consecutive runs, loads
+// the gradient, weights and momentum of all of them before it computes any
+// (a row of up to 128 columns is one quad per lane), so one DRAM latency is
+// spent per group instead of three per row.  Wider rows go through a
+// column loop afterwards.
+constexpr int kRowsPerWarp = 4;
+
+template <int KIND>
+__device__ __forceinline__ float row_step(const UpdArgs& a, float m_old, float ss, int D, float* m_new) {
+  if (KIND != TBE_OPT_EXACT_ROWWISE_ADAGRAD) return a.lr;
+  *m_new = __fadd_rn(m_old, __fdiv_rn(ss, (float)D));
+  return __fdiv_rn(a.lr, __fadd_rn(__fsqrt_rn(*m_new), a.eps));
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(kUpdThreads) exact_update_kernel(UpdArgs a) {
+__global__ void __launch_bounds__(kUpdThreads, 3) exact_update_kernel(UpdArgs a) {
   extern __shared__ int64_t s_upd[];
   int64_t* s_uc = s_upd;             // [T+1] distinct rows of tables < t
   int64_t* s_go = s_upd + a.T + 1;   // [T+1] float offset of table t's gradient block
@@ -129,48 +173,100 @@ __global__ void __launch_bounds__(kUpdThreads) exact_update_kernel(UpdArgs a) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, TBE_DEV_CAPACITY);
     U = a.max_unique;
   }
-  const int64_t stride = (int64_t)gridDim.x * kUpdWarps;
-  for (int64_t u = (int64_t)blockIdx.x * kUpdWarps + warp; u < U; u += stride) {
-    int lo = 0, hi = a.T - 1;  // the table of run u: the last t with s_uc[t] <= u
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_uc[mid] <= u) lo = mid;
-      else hi = mid - 1;
-    }
-    const TableMeta m = a.meta[lo];
-    const int64_t row = a.unique_rows[u];
-    const int64_t id = row - m.row_base;
-    const int64_t go = s_go[lo] + (u - s_uc[lo]) * (int64_t)m.D;
-    if (id < 0 || id >= m.rows) {
-      if (lane == 0) report(a.status, TBE_DEV_BAD_INDEX);
-      continue;
-    }
-    if (go < 0 || go + m.D > a.row_grads_capacity) {
-      if (lane == 0) report(a.status, TBE_DEV_CAPACITY);
-      continue;
-    }
-    const float* g = a.row_grads + go;
-    float step = a.lr;
-    if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
-      float ss = 0.f;
-      for (int c = lane * 4; c < m.D; c += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(g + c);
-        ss = fmaf(v.x, v.x, ss);
-        ss = fmaf(v.y, v.y, ss);
-        ss = fmaf(v.z, v.z, ss);
-        ss = fmaf(v.w, v.w, ss);
-      }
+  const int64_t stride = (int64_t)gridDim.x * kUpdWarps * kRowsPerWarp;
+  for (int64_t u0 = ((int64_t)blockIdx.x * kUpdWarps + warp) * kRowsPerWarp; u0 < U; u0 += stride) {
+    // the group's distinct rows: lane r < kRowsPerWarp loads run u0 + r's row
+    int64_t my_row = -1;
+    if (lane < kRowsPerWarp && u0 + lane < U) my_row = a.unique_rows[u0 + lane];
+    RowJob job[kRowsPerWarp];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
-      const float m_new = __fadd_rn(a.momentum[row], __fdiv_rn(ss, (float)m.D));
-      __syncwarp();  // every lane has read the old value before lane 0 replaces it
-      if (lane == 0) a.momentum[row] = m_new;
-      step = __fdiv_rn(a.lr, __fadd_rn(__fsqrt_rn(m_new), a.eps));
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      const int64_t u = u0 + r;
+      const int64_t row = __shfl_sync(kFull, my_row, r);
+      job[r].ok = false;
+      job[r].D = 0;
+      job[r].dtype = TBE_F32;
+      job[r].row = row;
+      job[r].g = nullptr;
+      job[r].w = nullptr;
+      if (u >= U) continue;
+      int lo = 0, hi = a.T - 1;  // the table of run u: the last t with s_uc[t] <= u
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_uc[mid] <= u) lo = mid;
+        else hi = mid - 1;
+      }
+      const TableMeta m = a.meta[lo];
+      const int64_t id = row - m.row_base;
+      const int64_t go = s_go[lo] + (u - s_uc[lo]) * (int64_t)m.D;
+      if (id < 0 || id >= m.rows) {
+        if (lane == 0) report(a.status, TBE_DEV_BAD_INDEX);
+        continue;
+      }
+      if (go < 0 || go + m.D > a.row_grads_capacity) {
+        if (lane == 0) report(a.status, TBE_DEV_CAPACITY);
+        continue;
+      }
+      job[r].ok = true;
+      job[r].D = m.D;
+      job[r].dtype = m.dtype;
+      job[r].g = a.row_grads + go;
+      job[r].w = a.weights + m.w_off + id * (int64_t)m.D * (m.dtype == TBE_F32 ? 4 : 2);
     }
-    uint8_t* wrow = a.weights + m.w_off + id * (int64_t)m.D * (m.dtype == TBE_F32 ? 4 : 2);
-    if (m.dtype == TBE_F32) apply_row<TBE_F32>(wrow, g, m.D, step, lane);
-    else if (m.dtype == TBE_F16) apply_row<TBE_F16>(wrow, g, m.D, step, lane);
-    else apply_row<TBE_BF16>(wrow, g, m.D, step, lane);
+    // rows of at most 128 columns: every load of the group first, then the math
+    float4 gv[kRowsPerWarp], wv[kRowsPerWarp];
+    float mo[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      gv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      wv[r] = gv[r];
+      mo[r] = 0.f;
+      const bool narrow = job[r].ok && job[r].D <= 128;
+      if (narrow && lane * 4 < job[r].D) {
+        gv[r] = *reinterpret_cast<const float4*>(job[r].g + lane * 4);
+        wv[r] = load_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8));
+      }
+      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD && narrow) mo[r] = a.momentum[job[r].row];
+    }
+    float ss[kRowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = sum_sq(gv[r], 0.f);
+    if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = warp_sum(ss[r]);
+    }
+    __syncwarp();  // every lane has read the old momentum before lane 0 replaces it
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (!job[r].ok || job[r].D > 128) continue;
+      float m_new = 0.f;
+      const float step = row_step<KIND>(a, mo[r], ss[r], job[r].D, &m_new);
+      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD && lane == 0) a.momentum[job[r].row] = m_new;
+      if (lane * 4 < job[r].D)
+        store_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8),
+                   fma_quad(step, gv[r], wv[r]));
+    }
+    // wider rows: a column loop per row (two passes over the gradient for Adagrad)
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+      if (!job[r].ok || job[r].D <= 128) continue;
+      const int D = job[r].D, dt = job[r].dtype, eb = dt == TBE_F32 ? 4 : 2;
+      float step = a.lr;
+      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
+        float acc = 0.f;
+        for (int c = lane * 4; c < D; c += 128) acc = sum_sq(*reinterpret_cast<const float4*>(job[r].g + c), acc);
+        acc = warp_sum(acc);
+        const float m_old = a.momentum[job[r].row];
+        __syncwarp();
+        float m_new = 0.f;
+        step = row_step<KIND>(a, m_old, acc, D, &m_new);
+        if (lane == 0) a.momentum[job[r].row] = m_new;
+      }
+      for (int c = lane * 4; c < D; c += 128) {
+        uint8_t* p = job[r].w + (size_t)c * eb;
+        store_quad(dt, p, fma_quad(step, *reinterpret_cast<const float4*>(job[r].g + c), load_quad(dt, p)));
+      }
+    }
   }
 }
 
@@ -181,8 +277,14 @@ int launch_kind(const UpdArgs& a, cudaStream_t s) {
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return TBE_ERR_CUDA;
-  int64_t want = (a.max_unique + kUpdWarps - 1) / kUpdWarps;
-  const int64_t cap = 4LL * sm_count();
+  // a grid-stride loop over groups of kRowsPerWarp runs: at most as many
+  // blocks as fit on the GPU at once, fewer for small batches
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kUpdThreads, smem) != cudaSuccess ||
+      per_sm <= 0)
+    per_sm = 1;
+  const int64_t want = (a.max_unique + kUpdWarps * kRowsPerWarp - 1) / (kUpdWarps * kRowsPerWarp);
+  const int64_t cap = (int64_t)per_sm * sm_count();
   const int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
