@@ -210,7 +210,8 @@ def traffic_from_profiles(kernel):
     if not os.path.exists(path):
         return None
     srcs = {"fwd_gather": "tbe_forward.cu", "bwd_reduce": "tbe_backward.cu",
-            "bwd_sort_pass": "tbe_backward.cu", "fwd_histogram": "tbe_histogram.cu"}
+            "bwd_sort_pass": "tbe_backward.cu", "fwd_histogram": "tbe_histogram.cu",
+            "exact_update": "tbe_optimizer.cu"}
     src = srcs.get(kernel)
     if src is None:
         return None
@@ -438,6 +439,7 @@ def run_ours(args, world, rank, local):
     optimizer = dict(kind="exact_rowwise_adagrad", lr=OPT_LR, eps=OPT_EPS, ms=upd_mean,
                      GBps=upd_bytes / (upd_mean * 1e-3) / 1e9, bytes_per_launch=upd_bytes,
                      frac=upd_bytes / (upd_mean * 1e-3) / 1e9 / peak, peak=peak, peak_kind=f"{peak_kind} (copy)",
+                     traffic=traffic_from_profiles("exact_update"),
                      placement="timed alone right after the backward of the same batch (row gradients still in L2, "
                                "tables and momentum flushed with the step's L2 flush)")
 
