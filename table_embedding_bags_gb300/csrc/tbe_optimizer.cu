@@ -42,14 +42,12 @@ struct Quad;
 
 template <>
 struct Quad<TBE_F32> {
-  static constexpr int kBytes = 16;
   __device__ __forceinline__ static float4 load(const uint8_t* p) { return *reinterpret_cast<const float4*>(p); }
   __device__ __forceinline__ static void store(uint8_t* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 };
 
 template <>
 struct Quad<TBE_F16> {
-  static constexpr int kBytes = 8;
   __device__ __forceinline__ static float4 load(const uint8_t* p) {
     const uint2 u = *reinterpret_cast<const uint2*>(p);
     const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
@@ -67,7 +65,6 @@ struct Quad<TBE_F16> {
 
 template <>
 struct Quad<TBE_BF16> {
-  static constexpr int kBytes = 8;
   __device__ __forceinline__ static float4 load(const uint8_t* p) {
     const uint2 u = *reinterpret_cast<const uint2*>(p);  // bf16 -> fp32 is exact: the bits move up
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
@@ -126,11 +123,11 @@ struct RowJob {
   bool ok;
 };
 
-// Rows per warp in flight: a warp takes kRowsPerWarp consecutive runs, loads
-// the gradient, weights and momentum of all of them before it computes any
-// (a row of up to 128 columns is one quad per lane), so one DRAM latency is
-// spent per group instead of three per row.  Wider rows go through a
-// column loop afterwards.
+// Rows per warp in flight: a warp updates kRowsPerWarp rows of its tile at
+// once, loading the gradient, weights and momentum of all of them before it
+// computes any (a row of up to 128 columns is one quad per lane), so one
+// memory latency is spent per group instead of one per row.  Wider rows go
+// through a column loop afterwards.
 constexpr int kRowsPerWarp = 4;
 
 template <int KIND>
@@ -173,100 +170,141 @@ __global__ void __launch_bounds__(kUpdThreads, 3) exact_update_kernel(UpdArgs a)
     if (blockIdx.x == 0 && threadIdx.x == 0) report(a.status, TBE_DEV_CAPACITY);
     U = a.max_unique;
   }
-  const int64_t stride = (int64_t)gridDim.x * kUpdWarps * kRowsPerWarp;
-  for (int64_t u0 = ((int64_t)blockIdx.x * kUpdWarps + warp) * kRowsPerWarp; u0 < U; u0 += stride) {
-    // the group's distinct rows: lane r < kRowsPerWarp loads run u0 + r's row
-    int64_t my_row = -1;
-    if (lane < kRowsPerWarp && u0 + lane < U) my_row = a.unique_rows[u0 + lane];
-    RowJob job[kRowsPerWarp];
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int64_t u = u0 + r;
-      const int64_t row = __shfl_sync(kFull, my_row, r);
-      job[r].ok = false;
-      job[r].D = 0;
-      job[r].dtype = TBE_F32;
-      job[r].row = row;
-      job[r].g = nullptr;
-      job[r].w = nullptr;
-      if (u >= U) continue;
+  // A warp takes a tile of 32 consecutive runs: lane l looks up run t0 + l
+  // (its row id, table, gradient offset and weight row) in one coalesced
+  // pass and leaves the result in the warp's shared-memory slots, then the
+  // warp updates the tile's rows kRowsPerWarp at a time.
+  __shared__ int64_t s_row[kUpdWarps][32], s_gofs[kUpdWarps][32], s_wofs[kUpdWarps][32];
+  __shared__ int32_t s_D[kUpdWarps][32], s_kind[kUpdWarps][32];  // width; dtype | ok << 8
+  const int64_t stride = (int64_t)gridDim.x * kUpdWarps * 32;
+  for (int64_t t0 = ((int64_t)blockIdx.x * kUpdWarps + warp) * 32; t0 < U; t0 += stride) {
+    const int64_t u_me = t0 + lane;
+    bool ok_me = false;
+    int64_t row_me = 0, go_me = 0, wo_me = 0;
+    int32_t D_me = 0, dt_me = TBE_F32;
+    if (u_me < U) {
+      row_me = a.unique_rows[u_me];
       int lo = 0, hi = a.T - 1;  // the table of run u: the last t with s_uc[t] <= u
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (s_uc[mid] <= u) lo = mid;
+        if (s_uc[mid] <= u_me) lo = mid;
         else hi = mid - 1;
       }
       const TableMeta m = a.meta[lo];
-      const int64_t id = row - m.row_base;
-      const int64_t go = s_go[lo] + (u - s_uc[lo]) * (int64_t)m.D;
+      const int64_t id = row_me - m.row_base;
+      go_me = s_go[lo] + (u_me - s_uc[lo]) * (int64_t)m.D;
       if (id < 0 || id >= m.rows) {
-        if (lane == 0) report(a.status, TBE_DEV_BAD_INDEX);
-        continue;
+        report(a.status, TBE_DEV_BAD_INDEX);
+      } else if (go_me < 0 || go_me + m.D > a.row_grads_capacity) {
+        report(a.status, TBE_DEV_CAPACITY);
+      } else {
+        ok_me = true;
+        D_me = m.D;
+        dt_me = m.dtype;
+        wo_me = m.w_off + id * (int64_t)m.D * (m.dtype == TBE_F32 ? 4 : 2);
       }
-      if (go < 0 || go + m.D > a.row_grads_capacity) {
-        if (lane == 0) report(a.status, TBE_DEV_CAPACITY);
-        continue;
+    }
+    s_row[warp][lane] = row_me;
+    s_gofs[warp][lane] = go_me;
+    s_wofs[warp][lane] = wo_me;
+    s_D[warp][lane] = D_me;
+    s_kind[warp][lane] = dt_me | ((int)ok_me << 8);
+    __syncwarp();
+#pragma unroll 1
+    for (int r0 = 0; r0 < 32; r0 += kRowsPerWarp) {
+      if (t0 + r0 >= U) break;
+      RowJob job[kRowsPerWarp];
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        const int src = r0 + r;
+        const int32_t kind = s_kind[warp][src];
+        job[r].ok = (kind >> 8) != 0;
+        job[r].D = s_D[warp][src];
+        job[r].dtype = kind & 0xff;
+        job[r].row = s_row[warp][src];
+        job[r].g = job[r].ok ? a.row_grads + s_gofs[warp][src] : nullptr;
+        job[r].w = job[r].ok ? a.weights + s_wofs[warp][src] : nullptr;
       }
-      job[r].ok = true;
-      job[r].D = m.D;
-      job[r].dtype = m.dtype;
-      job[r].g = a.row_grads + go;
-      job[r].w = a.weights + m.w_off + id * (int64_t)m.D * (m.dtype == TBE_F32 ? 4 : 2);
-    }
-    // rows of at most 128 columns: every load of the group first, then the math
-    float4 gv[kRowsPerWarp], wv[kRowsPerWarp];
-    float mo[kRowsPerWarp];
+      // rows of at most 128 columns: every load of the group first, then the math
+      float4 gv[kRowsPerWarp], wv[kRowsPerWarp];
+      float mo[kRowsPerWarp];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      gv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      wv[r] = gv[r];
-      mo[r] = 0.f;
-      const bool narrow = job[r].ok && job[r].D <= 128;
-      if (narrow && lane * 4 < job[r].D) {
-        gv[r] = *reinterpret_cast<const float4*>(job[r].g + lane * 4);
-        wv[r] = load_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8));
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        gv[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[r] = gv[r];
+        mo[r] = 0.f;
+        const bool narrow = job[r].ok && job[r].D <= 128;
+        if (narrow && lane * 4 < job[r].D) {
+          gv[r] = *reinterpret_cast<const float4*>(job[r].g + lane * 4);
+          wv[r] = load_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8));
+        }
+        if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD && narrow) mo[r] = a.momentum[job[r].row];
       }
-      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD && narrow) mo[r] = a.momentum[job[r].row];
-    }
-    float ss[kRowsPerWarp];
+      float ss[kRowsPerWarp];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = sum_sq(gv[r], 0.f);
-    if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = warp_sum(ss[r]);
-    }
-    __syncwarp();  // every lane has read the old momentum before lane 0 replaces it
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      if (!job[r].ok || job[r].D > 128) continue;
-      float m_new = 0.f;
-      const float step = row_step<KIND>(a, mo[r], ss[r], job[r].D, &m_new);
-      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD && lane == 0) a.momentum[job[r].row] = m_new;
-      if (lane * 4 < job[r].D)
-        store_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8),
-                   fma_quad(step, gv[r], wv[r]));
-    }
-    // wider rows: a column loop per row (two passes over the gradient for Adagrad)
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      if (!job[r].ok || job[r].D <= 128) continue;
-      const int D = job[r].D, dt = job[r].dtype, eb = dt == TBE_F32 ? 4 : 2;
-      float step = a.lr;
+      for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = sum_sq(gv[r], 0.f);
       if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
-        float acc = 0.f;
-        for (int c = lane * 4; c < D; c += 128) acc = sum_sq(*reinterpret_cast<const float4*>(job[r].g + c), acc);
-        acc = warp_sum(acc);
-        const float m_old = a.momentum[job[r].row];
-        __syncwarp();
-        float m_new = 0.f;
-        step = row_step<KIND>(a, m_old, acc, D, &m_new);
-        if (lane == 0) a.momentum[job[r].row] = m_new;
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) ss[r] = warp_sum(ss[r]);
       }
-      for (int c = lane * 4; c < D; c += 128) {
-        uint8_t* p = job[r].w + (size_t)c * eb;
-        store_quad(dt, p, fma_quad(step, *reinterpret_cast<const float4*>(job[r].g + c), load_quad(dt, p)));
+      __syncwarp();  // every lane has read the old momentum before it is replaced
+      // lane r < kRowsPerWarp works out row r's momentum and step (one square
+      // root and two divides per lane instead of per row), then hands the step
+      // round; rows wider than 128 columns are done below
+      float step[kRowsPerWarp];
+      if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
+        float m_sel = 0.f, ss_sel = 0.f;
+        int D_sel = 1;
+        bool mine = false;
+        int64_t row_sel = 0;
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r)
+          if (lane == r) {
+            m_sel = mo[r];
+            ss_sel = ss[r];
+            D_sel = job[r].D > 0 ? job[r].D : 1;
+            mine = job[r].ok && job[r].D <= 128;
+            row_sel = job[r].row;
+          }
+        float m_new = 0.f;
+        const float st = row_step<KIND>(a, m_sel, ss_sel, D_sel, &m_new);
+        if (mine) a.momentum[row_sel] = m_new;
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) step[r] = __shfl_sync(kFull, st, r);
+      } else {
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) step[r] = a.lr;
+      }
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        if (!job[r].ok || job[r].D > 128) continue;
+        if (lane * 4 < job[r].D)
+          store_quad(job[r].dtype, job[r].w + (size_t)lane * (job[r].dtype == TBE_F32 ? 16 : 8),
+                     fma_quad(step[r], gv[r], wv[r]));
+      }
+      // wider rows: a column loop per row (two passes over the gradient for Adagrad)
+#pragma unroll
+      for (int r = 0; r < kRowsPerWarp; ++r) {
+        if (!job[r].ok || job[r].D <= 128) continue;
+        const int D = job[r].D, dt = job[r].dtype, eb = dt == TBE_F32 ? 4 : 2;
+        float step = a.lr;
+        if (KIND == TBE_OPT_EXACT_ROWWISE_ADAGRAD) {
+          float acc = 0.f;
+          for (int c = lane * 4; c < D; c += 128) acc = sum_sq(*reinterpret_cast<const float4*>(job[r].g + c), acc);
+          acc = warp_sum(acc);
+          const float m_old = a.momentum[job[r].row];
+          __syncwarp();
+          float m_new = 0.f;
+          step = row_step<KIND>(a, m_old, acc, D, &m_new);
+          if (lane == 0) a.momentum[job[r].row] = m_new;
+        }
+        for (int c = lane * 4; c < D; c += 128) {
+          uint8_t* p = job[r].w + (size_t)c * eb;
+          store_quad(dt, p, fma_quad(step, *reinterpret_cast<const float4*>(job[r].g + c), load_quad(dt, p)));
+        }
       }
     }
+    __syncwarp();  // the tile's slots are rewritten by the next tile
   }
 }
 
@@ -274,16 +312,16 @@ template <int KIND>
 int launch_kind(const UpdArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(int64_t) * 2 * (size_t)(a.T + 1);
   auto kernel = exact_update_kernel<KIND>;
-  if (smem > 48 * 1024 &&
+  if (smem > 32 * 1024 &&  // beyond the default once the kernel's static slots are counted
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return TBE_ERR_CUDA;
-  // a grid-stride loop over groups of kRowsPerWarp runs: at most as many
+  // a grid-stride loop over tiles of 32 runs per warp: at most as many
   // blocks as fit on the GPU at once, fewer for small batches
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kUpdThreads, smem) != cudaSuccess ||
       per_sm <= 0)
     per_sm = 1;
-  const int64_t want = (a.max_unique + kUpdWarps * kRowsPerWarp - 1) / (kUpdWarps * kRowsPerWarp);
+  const int64_t want = (a.max_unique + kUpdWarps * 32 - 1) / (kUpdWarps * 32);
   const int64_t cap = (int64_t)per_sm * sm_count();
   const int grid = (int)(want < 1 ? 1 : (want > cap ? cap : want));
   cudaLaunchConfig_t cfg = {};
