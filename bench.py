@@ -591,6 +591,22 @@ def run_reference(args):
     )
 
 
+def combine_ranks(tot_s, nbytes, lookups, steps, device):
+    """Whole-job figures of a multi-rank run (an initialised process group):
+    the bytes and lookups of every rank over the slowest rank's timed
+    seconds.  Every rank gets the same result."""
+    import torch
+    import torch.distributed as dist
+
+    slowest = torch.tensor([tot_s], dtype=torch.float64, device=device)
+    units = torch.tensor([nbytes, lookups], dtype=torch.float64, device=device)
+    dist.all_reduce(slowest, op=dist.ReduceOp.MAX)
+    dist.all_reduce(units, op=dist.ReduceOp.SUM)
+    t = float(slowest[0])
+    return dict(value=float(units[0]) / t / 1e9, lookups_per_s_M=float(units[1]) / t / 1e6,
+                ms_per_step=1e3 * t / steps)
+
+
 def main():
     args = parse_args()
     world, rank, local = dist_env()
@@ -610,16 +626,7 @@ def main():
         dist.init_process_group("nccl")
     res, nbytes, tot_s, lookups = run_ours(args, world, rank, local)
     if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([tot_s, nbytes, lookups], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        dist.all_reduce(mx[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        tot_s = float(mx[0])
-        res["value"] = float(t[1]) / tot_s / 1e9
-        res["lookups_per_s_M"] = float(t[2]) / tot_s / 1e6
-        res["ms_per_step"] = 1e3 * tot_s / args.steps
+        res.update(combine_ranks(tot_s, nbytes, lookups, args.steps, device="cuda"))
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
             b, s, n, steps, cores = oracle_steps(args.workload, seconds=args.cpu_seconds)
