@@ -111,7 +111,7 @@ def optimizer_bytes(p, U_total):
     return U_total * (8 + 4 * D + 2 * eb * D + 8) + 8 * (p.T + 1)
 
 
-def kernel_bytes(p, U_total, npass):
+def kernel_bytes(p, U_total):
     """Algorithmic bytes of each backward kernel for one launch (the
     forward gather's are the forward's effective bytes)."""
     N = p.N
@@ -391,11 +391,15 @@ def run_ours(args, world, rank, local):
         fwd_ms.append(e0.elapsed_time(e1))
         bwd_ms.append(e1.elapsed_time(e2))
     torch.cuda.synchronize()
+    bwd_kernels = []  # the backward's kernel launches per step, from its trace
     for k in range(args.steps):  # per-kernel stage times (an event after every kernel)
         flush(k)
         traced_graphs[k % N_BATCHES][1].replay()
-        for name, ms in tbe.trace_read():
+        trace = tbe.trace_read()
+        for name, ms in trace:
             stage.setdefault(name, []).append(ms)
+        bwd_kernels.append(sum(1 for name, _ in trace if name.startswith("bwd_")
+                               and name not in ("bwd_memset", "bwd_empty")))
     torch.cuda.synchronize()
     upd_ms = []
     for k in range(args.steps):  # optimizer step after the backward of the same batch
@@ -422,13 +426,12 @@ def run_ours(args, world, rank, local):
 
     # dominant kernel: the forward gather against each backward kernel (the
     # trace holds one event per launch; the radix passes share one name)
-    npass = (int(p0.table_row_base[-1]).bit_length() + 7) // 8
     per_kernel = {"fwd_gather": float(np.mean(fwd_ms))}
     for name, v in stage.items():
         if name.startswith("bwd_") and name != "bwd_memset":
             per_kernel[name] = float(np.mean(v))
     U_mean = float(np.mean([u.sum() for u in uniq]))
-    kb = kernel_bytes(p0, U_mean, npass)
+    kb = kernel_bytes(p0, U_mean)
     kb["fwd_gather"] = float(np.mean([f for f, _ in eff]))
     dom = max(per_kernel, key=lambda n: per_kernel[n])
     peak, peak_kind = load_peaks()
@@ -476,7 +479,7 @@ def run_ours(args, world, rank, local):
                       traffic=traffic_from_profiles(dom)),
         optimizer=optimizer,
         clocks=clocks,
-        gpu_launches=args.steps * (1 + 4 + npass),
+        gpu_launches=args.steps + sum(bwd_kernels),
         launch="one CUDA graph per step (forward then backward); backward kernels chained with programmatic dependent launch",
     )
     if e2e is not None:
