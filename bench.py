@@ -576,6 +576,12 @@ def oracle_steps(workload, seconds=None, steps=None, nthreads=0):
     return tot_b, tot_s, tot_n, done, nthreads
 
 
+def batch_size(workload):
+    from tbe_inputs import make_config
+
+    return int(make_config(workload, with_grad=False).B)
+
+
 def run_reference(args):
     import oracle
 
@@ -587,7 +593,8 @@ def run_reference(args):
         impl="reference", metric=METRIC, value=v, unit="GB/s", lookups_per_s_M=n / s / 1e6,
         n_gpus=args.gpus, steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * s / steps,
         higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
-        config=dict(workload=WORKLOAD_DESC, global_batch=2048, parallelism="cpu"),
+        config=dict(workload=WORKLOAD_DESC if args.workload == WORKLOAD else args.workload,
+                    global_batch=batch_size(args.workload), parallelism="cpu"),
         cpu_baseline=dict(value=v, unit="GB/s", cores=cores, kind="oracle",
                           sample=f"{steps} full forward+backward batches of the workload (oracle, fp64)"),
         e2e=dict(value=v, unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0),
