@@ -100,6 +100,29 @@ def effective_bytes(p, unique_per_table):
     return fwd, bwd
 
 
+def compulsory_bytes(p, unique_per_table):
+    """Bytes one forward and one backward cannot avoid: every distinct row
+    (forward) and every output-gradient row (backward) once, plus indices,
+    weights, offsets and outputs.
+
+    FWD_c = sum_t U_t*D_t*s_w + 8*N + 4*N_weighted + (T*B+1)*8 + B*sumD*s_out
+    BWD_c = 8*N + 4*N_weighted + (T*B+1)*8 + 4*B*sumD + sum_t U_t*(8 + 4*D_t)
+    """
+    from tbe_inputs import ELEM_BYTES
+
+    lens = np.diff(p.offsets).reshape(p.T, p.B).sum(axis=1).astype(np.int64)
+    sw = np.array([ELEM_BYTES[int(d)] for d in p.weights_dtype], np.int64)
+    D = p.D.astype(np.int64)
+    w = (p.table_weighted.astype(np.int64) if p.per_sample_weights is not None else np.zeros(p.T, np.int64))
+    U = np.asarray(unique_per_table, np.int64)
+    ids = int(np.sum(lens * (8 + 4 * w)))
+    offs = (p.T * p.B + 1) * 8
+    sumD = int(D.sum())
+    fwd = int(np.sum(U * D * sw)) + ids + offs + p.B * sumD * ELEM_BYTES[int(p.out_dtype)]
+    bwd = ids + offs + 4 * p.B * sumD + int(np.sum(U * (8 + 4 * D)))
+    return fwd, bwd
+
+
 def optimizer_bytes(p, U_total):
     """Algorithmic bytes of one exact row-wise Adagrad step: per distinct row
     its id (8), its gradient (4 D), its weights read and written (2 D x the
@@ -421,6 +444,9 @@ def run_ours(args, world, rank, local):
     eff = [effective_bytes(probs[k % N_BATCHES], uniq[k % N_BATCHES]) for k in range(args.steps)]
     fwd_bytes = sum(f for f, _ in eff)
     bwd_bytes = sum(b for _, b in eff)
+    comp = [compulsory_bytes(probs[k % N_BATCHES], uniq[k % N_BATCHES]) for k in range(args.steps)]
+    fwd_comp = sum(f for f, _ in comp)
+    bwd_comp = sum(b for _, b in comp)
     lookups = sum(probs[k % N_BATCHES].N for k in range(args.steps))
     tot_s = sum(step_ms) / 1e3
 
@@ -464,6 +490,11 @@ def run_ours(args, world, rank, local):
                  pct_of_8TBs=100 * bwd_bytes / (sum(bwd_ms) / 1e3) / 1e9 / NOMINAL_HBM_GBS),
         pct_of_8TBs=100 * (fwd_bytes + bwd_bytes) / tot_s / 1e9 / NOMINAL_HBM_GBS,
         pct_of_measured_peak=100 * (fwd_bytes + bwd_bytes) / tot_s / 1e9 / peak,
+        compulsory=dict(GBps=(fwd_comp + bwd_comp) / tot_s / 1e9,
+                        fwd_GBps=fwd_comp / (sum(fwd_ms) / 1e3) / 1e9,
+                        bwd_GBps=bwd_comp / (sum(bwd_ms) / 1e3) / 1e9,
+                        note="each distinct row and each output-gradient row once, plus ids, weights, "
+                             "offsets and outputs (compulsory_bytes)"),
         stages_ms={k: float(np.mean(v)) for k, v in stage.items()},
         n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=float(np.mean(step_ms)),

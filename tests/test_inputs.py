@@ -50,3 +50,22 @@ def test_zipf_is_skewed():
     top = np.sort(counts)[::-1]
     assert top[0] > 0.05 * seg.size  # hottest row takes several percent of lookups
     assert int(p.weights_dtype[0]) == DT_F16
+
+
+def test_bench_byte_counts_on_the_hand_example():
+    """The benchmark's byte accounting, counted by hand on the two-table
+    example: T=2, B=2, fp32 tables of widths 2 and 1, fp32 output, 4 + 3
+    lookups, 3 + 2 distinct rows, 5 offsets."""
+    import bench
+    from oracle_pins import _hand_problem
+
+    _, p = _hand_problem(False)
+    U = [3, 2]
+    # effective: lookups 4*(2*4 + 8) + 3*(1*4 + 8) = 100; offsets 40; output 2*3*4 = 24
+    # backward: lookups 4*(4*2 + 8) + 3*(4*1 + 8) = 100; offsets 40; rows 3*(8+8) + 2*(8+4) = 72
+    assert bench.effective_bytes(p, U) == (164, 212)
+    # compulsory: rows 3*2*4 + 2*1*4 = 32; ids 7*8 = 56; offsets 40; output 24 -> 152
+    # backward: ids 56; offsets 40; G once 4*2*3 = 24; rows 72 -> 192
+    assert bench.compulsory_bytes(p, U) == (152, 192)
+    # Adagrad step, one width: per row 8 + 4*D + 2*4*D + 8 -> D=2: 40 per row; plus (T+1)*8
+    assert bench.optimizer_bytes(p, 5) == 5 * (8 + 8 + 16 + 8) + 24
