@@ -21,6 +21,9 @@
  *    bags that read it (times their per-sample weights).  Short runs are
  *    reduced by one warp each; long runs are cut into chunks whose partial
  *    sums are combined by the last chunk to finish (fence + counter).
+ *  - Exact optimizer ([FBT] "Why the backward is the hard half"): SGD or
+ *    row-wise Adagrad applied once per distinct row to its finished
+ *    gradient, in place on the tables (tbe_exact_update).
  *
  * Conventions for every entry point
  *  - Pointers named dev_* or documented "device" are CUDA device pointers;
