@@ -83,3 +83,56 @@ def test_exact_update_rejects_without_plan(lib):
     assert rc == tbe.TBE_ERR_INVALID_ARG
     rc = lib.tbe_exact_update(None, None, None, None, None, 0, None, 0, None, None, None)
     assert rc == tbe.TBE_ERR_INVALID_ARG
+
+
+def _layout(T, trb, doff, woff, wdt, out_dtype=0):
+    import numpy as np
+
+    keep = [np.ascontiguousarray(trb, np.int64), np.ascontiguousarray(doff, np.int32),
+            np.ascontiguousarray(woff, np.int64), np.ascontiguousarray(wdt, np.int32)]
+    L = tbe._Layout(T, *(a.ctypes.data for a in keep), None, out_dtype)
+    return L, keep
+
+
+# layouts that tbe_plan_create must refuse before it touches the device
+BAD_LAYOUTS = {
+    "no_tables": (dict(T=0, trb=[0], doff=[0], woff=[], wdt=[]), tbe.TBE_ERR_INVALID_ARG),
+    "too_many_tables": (dict(T=tbe.TBE_MAX_TABLES + 1, trb=[0, 1], doff=[0, 4], woff=[0], wdt=[0]),
+                        tbe.TBE_ERR_INVALID_ARG),
+    "row_base_not_zero": (dict(T=1, trb=[5, 10], doff=[0, 4], woff=[0], wdt=[0]), tbe.TBE_ERR_INVALID_ARG),
+    "rows_decrease": (dict(T=2, trb=[0, 10, 4], doff=[0, 4, 8], woff=[0, 256], wdt=[0, 0]),
+                      tbe.TBE_ERR_INVALID_ARG),
+    "zero_width": (dict(T=2, trb=[0, 10, 20], doff=[0, 4, 4], woff=[0, 256], wdt=[0, 0]), tbe.TBE_ERR_INVALID_ARG),
+    "unknown_dtype": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[7]), tbe.TBE_ERR_INVALID_ARG),
+    "unknown_out_dtype": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[0], out_dtype=9),
+                          tbe.TBE_ERR_INVALID_ARG),
+    "row_not_16_bytes": (dict(T=1, trb=[0, 10], doff=[0, 3], woff=[0], wdt=[0]), tbe.TBE_ERR_UNSUPPORTED),
+    "half_row_not_16_bytes": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[1]), tbe.TBE_ERR_UNSUPPORTED),
+    "table_not_aligned": (dict(T=2, trb=[0, 10, 20], doff=[0, 4, 8], woff=[0, 8], wdt=[0, 0]),
+                          tbe.TBE_ERR_UNSUPPORTED),
+    "rows_beyond_int32": (dict(T=1, trb=[0, 1 << 31], doff=[0, 4], woff=[0], wdt=[0]), tbe.TBE_ERR_UNSUPPORTED),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BAD_LAYOUTS))
+def test_plan_create_refuses_bad_layouts(lib, name):
+    kw, want = BAD_LAYOUTS[name]
+    L, _keep = _layout(kw["T"], kw["trb"], kw["doff"], kw["woff"], kw["wdt"], kw.get("out_dtype", 0))
+    meta = (ctypes.c_uint8 * (1 << 20))()
+    base = (ctypes.addressof(meta) + 15) // 16 * 16
+    h = ctypes.c_void_p()
+    rc = lib.tbe_plan_create(ctypes.byref(L), ctypes.c_void_p(base), (1 << 20) - 16, None, ctypes.byref(h))
+    assert rc == want and not h.value
+
+
+def test_plan_create_checks_its_metadata_buffer(lib):
+    L, _keep = _layout(1, [0, 10], [0, 4], [0], [0])
+    meta = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(meta) + 15) // 16 * 16
+    h = ctypes.c_void_p()
+    need = lib.tbe_plan_device_bytes(1)
+    assert lib.tbe_plan_create(ctypes.byref(L), None, need, None, ctypes.byref(h)) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_plan_create(ctypes.byref(L), ctypes.c_void_p(base), need - 1, None,
+                               ctypes.byref(h)) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_plan_create(ctypes.byref(L), ctypes.c_void_p(base + 4), need, None,
+                               ctypes.byref(h)) == tbe.TBE_ERR_INVALID_ARG
