@@ -227,7 +227,9 @@ def _assemble(T, B, lengths_tb, ids_per_table):
 # the five workloads
 # ---------------------------------------------------------------------------
 
-CONFIG_SEEDS = {"tiny": 1001, "mid_skewed": 1002, "mixed": 1003, "small_table": 1004, "bwd_skew": 1005}
+# mid_uniform shares mid_skewed's seed: same tables, lengths and empty bags, uniform ids (the control)
+CONFIG_SEEDS = {"tiny": 1001, "mid_skewed": 1002, "mixed": 1003, "small_table": 1004, "bwd_skew": 1005,
+                "mid_uniform": 1002}
 
 
 def config_names():
@@ -236,7 +238,8 @@ def config_names():
 
 def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch: int = 0,
                 seed: int | None = None, with_grad: bool = True) -> TBEProblem:
-    """Build one of the five named workloads.
+    """Build one of the named workloads (the five of the method's measurements
+    plus a uniform-id control of the mid-size one).
 
     ``B`` and ``rows_scale`` shrink a workload for parity tests; ``batch``
     selects one of several index batches drawn for the same tables.
@@ -264,7 +267,7 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
         ids = [irng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
         weighted = np.zeros(T, np.uint8)
         recipe = "T=3 fp32 rows 100/50/20 D 8/16/4; L~U{0..5} resampled until one bag is empty; uniform ids"
-    elif name == "mid_skewed":
+    elif name in ("mid_skewed", "mid_uniform"):
         T, Bv = 8, (2048 if B is None else B)
         rows = np.full(T, scaled(100_000), np.int64)
         D = np.full(T, 128, np.int32)
@@ -274,10 +277,15 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
         lens = irng.poisson(20.0, size=(T, Bv))
         empty_b = irng.integers(0, Bv, size=T)
         lens[np.arange(T), empty_b] = 0
-        ids = [_zipf_ids(irng, int(rows[t]), 1.05, int(lens[t].sum())) for t in range(T)]
+        if name == "mid_skewed":
+            ids = [_zipf_ids(irng, int(rows[t]), 1.05, int(lens[t].sum())) for t in range(T)]
+            how = "ids Zipf(1.05) through a per-table permutation"
+        else:
+            ids = [irng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
+            how = "uniform ids (control for the skewed workload: same tables and lengths)"
         weighted = np.zeros(T, np.uint8)
         recipe = ("T=8 fp16 100k rows D=128 W~U(-0.05,0.05); B=2048; L~Poisson(20) with one "
-                  "seed-chosen empty bag per table; ids Zipf(1.05) through a per-table permutation; fp16 out")
+                  f"seed-chosen empty bag per table; {how}; fp16 out")
     elif name == "mixed":
         T, Bv = 40, (8192 if B is None else B)
         rows = np.array([scaled(round(math.exp(x))) for x in lay.uniform(math.log(1e4), math.log(1e7), size=T)], np.int64)

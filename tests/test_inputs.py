@@ -17,7 +17,7 @@ def test_config_shapes(name):
         assert np.all((seg >= 0) & (seg < p.rows[t]))
     assert p.grad_out.shape == (p.B, p.total_D) and p.grad_out.dtype == np.float32
     assert np.all(p.weights_offsets % 256 == 0)
-    if name in ("tiny", "mid_skewed"):
+    if name in ("tiny", "mid_skewed", "mid_uniform"):
         assert (np.diff(p.offsets) == 0).any()
     if name == "mixed":
         assert p.per_sample_weights is not None and int(p.table_weighted.sum()) == 20
@@ -69,3 +69,16 @@ def test_bench_byte_counts_on_the_hand_example():
     assert bench.compulsory_bytes(p, U) == (152, 192)
     # Adagrad step, one width: per row 8 + 4*D + 2*4*D + 8 -> D=2: 40 per row; plus (T+1)*8
     assert bench.optimizer_bytes(p, 5) == 5 * (8 + 8 + 16 + 8) + 24
+
+
+def test_uniform_control_matches_the_skewed_workload():
+    """Same tables and bag lengths as the mid-size skewed batch, ids spread
+    evenly: many more distinct rows, no row far above the mean."""
+    a, b = make_config("mid_skewed"), make_config("mid_uniform")
+    assert np.array_equal(a.offsets, b.offsets) and np.array_equal(a.grad_out, b.grad_out)
+    assert np.array_equal(a.rows, b.rows) and np.array_equal(a.weights_offsets, b.weights_offsets)
+    ua = sum(len(np.unique(a.indices[a.offsets[t * a.B]: a.offsets[(t + 1) * a.B]])) for t in range(a.T))
+    ub = sum(len(np.unique(b.indices[b.offsets[t * b.B]: b.offsets[(t + 1) * b.B]])) for t in range(b.T))
+    assert ub > 2 * ua
+    seg = b.indices[b.offsets[0]: b.offsets[b.B]]
+    assert np.bincount(seg, minlength=int(b.rows[0])).max() < 12
