@@ -29,6 +29,7 @@ from .gen import (  # noqa: F401
     DT_BF16,
     DTYPE_NAMES,
     ELEM_BYTES,
+    RUN_BANDS,
     TBEProblem,
     make_problem,
     make_config,

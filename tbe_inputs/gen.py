@@ -213,6 +213,42 @@ def _zipf_ids(rng, rows: int, alpha: float, n: int) -> np.ndarray:
     return perm[r]
 
 
+def _band_ids(rng, rows: int, n: int, lo: int, hi: int) -> np.ndarray:
+    """n ids of one table whose row multiplicities (run lengths in the
+    backward) are drawn uniformly from [lo, hi]; distinct rows are chosen
+    at random and the lookups shuffled.  When the remainder is too short to
+    start another run it joins a run that stays within hi, so at most one
+    run per table falls outside the band."""
+    if n == 0:
+        return np.zeros(0, dtype=np.int64)
+    runs = []
+    left = n
+    while left > 0:
+        k = int(rng.integers(lo, hi + 1))
+        if k > left:
+            k = left
+        runs.append(k)
+        left -= k
+    if len(runs) > 1 and runs[-1] < lo:
+        tail = runs.pop()
+        for j in range(len(runs)):  # fold the short tail into a run with room for it
+            if runs[j] + tail <= hi:
+                runs[j] += tail
+                tail = 0
+                break
+        if tail:
+            runs.append(tail)
+    if len(runs) > rows:
+        raise ValueError("table too small for the requested run lengths")
+    rows_used = rng.choice(rows, size=len(runs), replace=False).astype(np.int64)
+    ids = np.repeat(rows_used, np.asarray(runs, np.int64))
+    return ids[rng.permutation(n)]
+
+
+# run-length bands of the band workloads (lookups per distinct row)
+RUN_BANDS = {"band_short": (1, 3), "band_mid": (32, 255), "band_long": (1024, 4096)}
+
+
 def _assemble(T, B, lengths_tb, ids_per_table):
     """lengths_tb: [T, B] bag lengths; ids_per_table[t]: ids for table t in bag order."""
     lens = lengths_tb.reshape(-1).astype(np.int64)
@@ -229,7 +265,7 @@ def _assemble(T, B, lengths_tb, ids_per_table):
 
 # mid_uniform shares mid_skewed's seed: same tables, lengths and empty bags, uniform ids (the control)
 CONFIG_SEEDS = {"tiny": 1001, "mid_skewed": 1002, "mixed": 1003, "small_table": 1004, "bwd_skew": 1005,
-                "mid_uniform": 1002}
+                "mid_uniform": 1002, "band_short": 1007, "band_mid": 1007, "band_long": 1007}
 
 
 def config_names():
@@ -238,8 +274,10 @@ def config_names():
 
 def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch: int = 0,
                 seed: int | None = None, with_grad: bool = True) -> TBEProblem:
-    """Build one of the named workloads (the five of the method's measurements
-    plus a uniform-id control of the mid-size one).
+    """Build one of the named workloads: the five of the method's
+    measurements, a uniform-id control of the mid-size one, and three
+    run-length bands (every distinct row read 1..3, 32..255 or 1024..4096
+    times) for mapping where the short/long threshold pays.
 
     ``B`` and ``rows_scale`` shrink a workload for parity tests; ``batch``
     selects one of several index batches drawn for the same tables.
@@ -328,6 +366,19 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
         ids = [_zipf_ids(irng, int(rows[t]), 1.2, int(lens[t].sum())) for t in range(T)]
         weighted = np.zeros(T, np.uint8)
         recipe = "T=16 fp32 1M rows D=128 W~U(-0.05,0.05); B=16384; L~Poisson(50); ids Zipf(1.2)+perm; fp32 out"
+    elif name in RUN_BANDS:
+        lo, hi = RUN_BANDS[name]
+        T, Bv = 8, (8192 if B is None else B)
+        rows = np.full(T, scaled(1_000_000), np.int64)
+        D = np.full(T, 128, np.int32)
+        wdt = np.full(T, DT_F32, np.int32)
+        out_dt = DT_F32
+        wdist = [("usym", 0.05)] * T
+        lens = irng.poisson(20.0, size=(T, Bv))
+        ids = [_band_ids(irng, int(rows[t]), int(lens[t].sum()), lo, hi) for t in range(T)]
+        weighted = np.zeros(T, np.uint8)
+        recipe = (f"T=8 fp32 1M rows D=128 W~U(-0.05,0.05); B=8192; L~Poisson(20); every distinct row "
+                  f"read U{{{lo}..{hi}}} times (shuffled over the bags); fp32 out")
     else:
         raise KeyError(name)
 

@@ -82,3 +82,23 @@ def test_uniform_control_matches_the_skewed_workload():
     assert ub > 2 * ua
     seg = b.indices[b.offsets[0]: b.offsets[b.B]]
     assert np.bincount(seg, minlength=int(b.rows[0])).max() < 12
+
+
+@pytest.mark.parametrize("name", ["band_short", "band_mid", "band_long"])
+def test_run_length_bands(name):
+    """Every distinct row of a band workload is read a number of times inside
+    its band (one run per table may fall short: the remainder), and the three
+    bands share their bag lengths."""
+    from tbe_inputs import RUN_BANDS
+
+    lo, hi = RUN_BANDS[name]
+    p = make_config(name, B=512, with_grad=False)
+    q = make_config("band_mid", B=512, with_grad=False)
+    assert np.array_equal(p.offsets, q.offsets)
+    for t in range(p.T):
+        seg = p.indices[p.offsets[t * p.B]: p.offsets[(t + 1) * p.B]]
+        assert np.all((seg >= 0) & (seg < p.rows[t]))
+        _, counts = np.unique(seg, return_counts=True)
+        outside = counts[(counts < lo) | (counts > hi)]
+        assert outside.size <= 1 and np.all(outside < lo), (t, outside)
+        assert counts[(counts >= lo) & (counts <= hi)].sum() >= 0.9 * seg.size or seg.size < 2 * hi
