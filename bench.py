@@ -44,6 +44,7 @@ WORKLOAD_DESC = ("TBE mid-size skewed: T=8 fp16 tables x 100000 rows, D=128, B=2
                  "Poisson(20) (one empty bag per table), ids Zipf(1.05) through a per-table permutation, "
                  "fp16 output, fp32 grad_out; forward + backward (row gradients)")
 N_BATCHES = 4
+DT_NAMES = {0: "f32", 1: "f16", 2: "bf16"}
 OPT_LR, OPT_EPS = 0.01, 1e-8  # exact row-wise Adagrad step timed beside the headline
 FLUSH_BYTES = 256 << 20
 
@@ -61,6 +62,8 @@ def parse_args():
     ap.add_argument("--B", type=int, default=None, help="batch size override (profiling of smaller cases)")
     ap.add_argument("--only", choices=["both", "fwd", "bwd"], default="both")
     ap.add_argument("--path", choices=["auto", "gather", "histogram"], default="auto")
+    ap.add_argument("--tuning", default=None,
+                    help='JSON object of tbe_tuning fields to set first, e.g. \'{"long_run_threshold": 256}\'')
     ap.add_argument("--profile", action="store_true",
                     help="plain launch loop for a profiler: --warmup then --steps eager steps, one JSON line")
     return ap.parse_args()
@@ -123,15 +126,17 @@ def compulsory_bytes(p, unique_per_table):
     return fwd, bwd
 
 
-def optimizer_bytes(p, U_total):
+def optimizer_bytes(p, unique_per_table):
     """Algorithmic bytes of one exact row-wise Adagrad step: per distinct row
     its id (8), its gradient (4 D), its weights read and written (2 D x the
     table's element size) and its momentum read and written (8); plus the
-    per-table counts.  The mid-size workload has one width and dtype, so U
-    counts rows of every table alike."""
-    D = int(p.D[0])
-    eb = 4 if int(p.weights_dtype[0]) == 0 else 2
-    return U_total * (8 + 4 * D + 2 * eb * D + 8) + 8 * (p.T + 1)
+    per-table counts."""
+    from tbe_inputs import ELEM_BYTES
+
+    U = np.asarray(unique_per_table, np.int64)
+    D = p.D.astype(np.int64)
+    sw = np.array([ELEM_BYTES[int(d)] for d in p.weights_dtype], np.int64)
+    return int(np.sum(U * (8 + 4 * D + 2 * sw * D + 8))) + 8 * (p.T + 1)
 
 
 def kernel_bytes(p, U_total):
@@ -217,6 +222,14 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.acc)
 
 
+def apply_tuning(tbe, spec):
+    """Sets the tbe_tuning fields named in the JSON object `spec` (None: the
+    library's defaults) and returns the tuning in effect."""
+    if spec:
+        tbe.set_tuning(**json.loads(spec))
+    return tbe.get_tuning()
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,6 +272,7 @@ def run_profile(args):
     from tbe_inputs import make_config, materialize_weights
 
     tbe.load_library()
+    apply_tuning(tbe, args.tuning)
     p = make_config(args.workload, B=args.B, with_grad=args.only != "fwd")
     plan = tbe.Plan.from_problem(p)
     ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
@@ -293,6 +307,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     tbe.load_library()
+    tuning = apply_tuning(tbe, args.tuning)
     probs = [make_config(args.workload, batch=k) for k in range(N_BATCHES)]
     p0 = probs[0]
     weights = materialize_weights(p0, device=dev)
@@ -463,7 +478,8 @@ def run_ours(args, world, rank, local):
     peak, peak_kind = load_peaks()
     achieved = kb[dom] / (per_kernel[dom] * 1e-3) / 1e9
 
-    upd_bytes = optimizer_bytes(p0, U_mean)
+    upd_bytes = float(np.mean([optimizer_bytes(probs[k % N_BATCHES], uniq[k % N_BATCHES])
+                               for k in range(args.steps)]))
     upd_mean = float(np.mean(upd_ms))
     optimizer = dict(kind="exact_rowwise_adagrad", lr=OPT_LR, eps=OPT_EPS, ms=upd_mean,
                      GBps=upd_bytes / (upd_mean * 1e-3) / 1e9, bytes_per_launch=upd_bytes,
@@ -501,10 +517,12 @@ def run_ours(args, world, rank, local):
         wall_s=t_wall,
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="f32", data="synthetic",
-        config=dict(workload=WORKLOAD_DESC, global_batch=p0.B * world, tables=p0.T,
+        config=dict(workload=WORKLOAD_DESC if args.workload == WORKLOAD else f"{args.workload}: {p0.recipe}",
+                    global_batch=p0.B * world, tables=p0.T,
                     lookups_per_step=int(np.mean([p.N for p in probs])), index_batches=N_BATCHES,
                     l2="flushed before every step (256 MB write + 256 MB read of another buffer, outside the step events)",
-                    table_dtype="f16", accumulate="f32", out_dtype="f16", parallelism=f"replicas x{world}"),
+                    table_dtype="/".join(sorted({DT_NAMES[int(d)] for d in p0.weights_dtype})), accumulate="f32",
+                    out_dtype=DT_NAMES[int(p0.out_dtype)], parallelism=f"replicas x{world}"),
         roofline=dict(bound="hbm", kernel=dom, achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                       peak_kind=f"{peak_kind} (copy)", bytes_per_launch=kb[dom], launch_ms=per_kernel[dom],
                       traffic=traffic_from_profiles(dom)),
@@ -512,6 +530,7 @@ def run_ours(args, world, rank, local):
         clocks=clocks,
         gpu_launches=args.steps + sum(bwd_kernels),
         launch="one CUDA graph per step (forward then backward); backward kernels chained with programmatic dependent launch",
+        tuning=tuning,
     )
     if e2e is not None:
         res["e2e"] = e2e

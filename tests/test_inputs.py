@@ -67,8 +67,8 @@ def test_bench_byte_counts_on_the_hand_example():
     # compulsory: rows 3*2*4 + 2*1*4 = 32; ids 7*8 = 56; offsets 40; output 24 -> 152
     # backward: ids 56; offsets 40; G once 4*2*3 = 24; rows 72 -> 192
     assert bench.compulsory_bytes(p, U) == (152, 192)
-    # Adagrad step, one width: per row 8 + 4*D + 2*4*D + 8 -> D=2: 40 per row; plus (T+1)*8
-    assert bench.optimizer_bytes(p, 5) == 5 * (8 + 8 + 16 + 8) + 24
+    # Adagrad step: per row 8 + 4*D + 2*4*D + 8 -> 40 for D=2, 28 for D=1; plus (T+1)*8
+    assert bench.optimizer_bytes(p, U) == 3 * 40 + 2 * 28 + 24
 
 
 def test_uniform_control_matches_the_skewed_workload():
