@@ -198,10 +198,13 @@ def materialize_weights(p: TBEProblem, device="cpu", chunk_elems: int = 1 << 25)
 # id / length samplers
 # ---------------------------------------------------------------------------
 
-def _zipf_ids(rng, rows: int, alpha: float, n: int) -> np.ndarray:
+def _zipf_ids(rng, rows: int, alpha: float, n: int, permute: bool = True) -> np.ndarray:
     """Bounded Zipf over ranks 1..rows, P(k) ~ k^-alpha, by inverse CDF on the
-    exact cumulative table; rank -> id through a seeded random permutation."""
+    exact cumulative table; rank -> id through a seeded random permutation
+    (permute=False: id = rank - 1, so the hot rows sit next to each other)."""
     perm = rng.permutation(rows).astype(np.int64)
+    if not permute:
+        perm = np.arange(rows, dtype=np.int64)
     if n == 0:
         return np.zeros(0, dtype=np.int64)
     k = np.arange(1, rows + 1, dtype=np.float64)
@@ -265,7 +268,8 @@ def _assemble(T, B, lengths_tb, ids_per_table):
 
 # mid_uniform shares mid_skewed's seed: same tables, lengths and empty bags, uniform ids (the control)
 CONFIG_SEEDS = {"tiny": 1001, "mid_skewed": 1002, "mixed": 1003, "small_table": 1004, "bwd_skew": 1005,
-                "mid_uniform": 1002, "band_short": 1007, "band_mid": 1007, "band_long": 1007}
+                "mid_uniform": 1002, "mid_identity": 1002, "band_short": 1007, "band_mid": 1007,
+                "band_long": 1007}
 
 
 def config_names():
@@ -275,7 +279,8 @@ def config_names():
 def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch: int = 0,
                 seed: int | None = None, with_grad: bool = True) -> TBEProblem:
     """Build one of the named workloads: the five of the method's
-    measurements, a uniform-id control of the mid-size one, and three
+    measurements, a uniform-id control and an unpermuted-Zipf sensitivity
+    case of the mid-size one, and three
     run-length bands (every distinct row read 1..3, 32..255 or 1024..4096
     times) for mapping where the short/long threshold pays.
 
@@ -305,7 +310,7 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
         ids = [irng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
         weighted = np.zeros(T, np.uint8)
         recipe = "T=3 fp32 rows 100/50/20 D 8/16/4; L~U{0..5} resampled until one bag is empty; uniform ids"
-    elif name in ("mid_skewed", "mid_uniform"):
+    elif name in ("mid_skewed", "mid_uniform", "mid_identity"):
         T, Bv = 8, (2048 if B is None else B)
         rows = np.full(T, scaled(100_000), np.int64)
         D = np.full(T, 128, np.int32)
@@ -318,6 +323,9 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
         if name == "mid_skewed":
             ids = [_zipf_ids(irng, int(rows[t]), 1.05, int(lens[t].sum())) for t in range(T)]
             how = "ids Zipf(1.05) through a per-table permutation"
+        elif name == "mid_identity":
+            ids = [_zipf_ids(irng, int(rows[t]), 1.05, int(lens[t].sum()), permute=False) for t in range(T)]
+            how = "ids Zipf(1.05) with rank k at id k-1 (hot rows adjacent; sensitivity case)"
         else:
             ids = [irng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
             how = "uniform ids (control for the skewed workload: same tables and lengths)"

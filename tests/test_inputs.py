@@ -17,7 +17,7 @@ def test_config_shapes(name):
         assert np.all((seg >= 0) & (seg < p.rows[t]))
     assert p.grad_out.shape == (p.B, p.total_D) and p.grad_out.dtype == np.float32
     assert np.all(p.weights_offsets % 256 == 0)
-    if name in ("tiny", "mid_skewed", "mid_uniform"):
+    if name in ("tiny", "mid_skewed", "mid_uniform", "mid_identity"):
         assert (np.diff(p.offsets) == 0).any()
     if name == "mixed":
         assert p.per_sample_weights is not None and int(p.table_weighted.sum()) == 20
@@ -102,3 +102,14 @@ def test_run_length_bands(name):
         outside = counts[(counts < lo) | (counts > hi)]
         assert outside.size <= 1 and np.all(outside < lo), (t, outside)
         assert counts[(counts >= lo) & (counts <= hi)].sum() >= 0.9 * seg.size or seg.size < 2 * hi
+
+
+def test_identity_case_keeps_the_skew_but_not_the_permutation():
+    a, c = make_config("mid_skewed"), make_config("mid_identity")
+    assert np.array_equal(a.offsets, c.offsets)
+    seg_a = a.indices[a.offsets[0]: a.offsets[a.B]]
+    seg_c = c.indices[c.offsets[0]: c.offsets[c.B]]
+    # the most frequent id is rank 1: id 0 without the permutation
+    assert np.bincount(seg_c).argmax() == 0
+    # same number of distinct rows up to sampling noise (the permutation only renames rows)
+    assert abs(len(np.unique(seg_a)) - len(np.unique(seg_c))) < 0.05 * len(np.unique(seg_a))
