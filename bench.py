@@ -632,6 +632,17 @@ def batch_size(workload):
     return int(make_config(workload, with_grad=False).B)
 
 
+def cpu_baseline(workload, seconds, single_steps=2):
+    """The oracle on the host cores: full forward+backward batches for about
+    `seconds` on every core, then `single_steps` batches on one thread."""
+    b, s, n, steps, cores = oracle_steps(workload, seconds=seconds)
+    b1, s1, _, steps1, _ = oracle_steps(workload, steps=single_steps, nthreads=1)
+    return dict(value=b / s / 1e9, unit="GB/s", cores=cores, kind="oracle",
+                sample=f"{steps} full forward+backward batches of the workload ({s:.1f} s of CPU work, fp64 oracle)",
+                single_thread=dict(value=b1 / s1 / 1e9, unit="GB/s", cores=1,
+                                   sample=f"{steps1} batches on one thread ({s1:.1f} s)"))
+
+
 def run_reference(args):
     import oracle
 
@@ -689,10 +700,7 @@ def main():
         res.update(combine_ranks(tot_s, nbytes, lookups, args.steps, device="cuda"))
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            b, s, n, steps, cores = oracle_steps(args.workload, seconds=args.cpu_seconds)
-            res["cpu_baseline"] = dict(value=b / s / 1e9, unit="GB/s", cores=cores, kind="oracle",
-                                       sample=f"{steps} full forward+backward batches of the workload "
-                                              f"({s:.1f} s of CPU work, fp64 oracle)")
+            res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
         print(json.dumps(res), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

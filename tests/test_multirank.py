@@ -76,3 +76,12 @@ def test_reference_arm_runs_on_rank_zero_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    d = bench.cpu_baseline("tiny", seconds=0.05, single_steps=1)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1
+    assert d["single_thread"]["cores"] == 1 and d["single_thread"]["value"] > 0
