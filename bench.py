@@ -308,7 +308,7 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     tbe.load_library()
     tuning = apply_tuning(tbe, args.tuning)
-    probs = [make_config(args.workload, batch=k) for k in range(N_BATCHES)]
+    probs = [make_config(args.workload, batch=k, B=args.B) for k in range(N_BATCHES)]
     p0 = probs[0]
     weights = materialize_weights(p0, device=dev)
     plan = tbe.Plan.from_problem(p0, device=dev)
@@ -324,10 +324,12 @@ def run_ours(args, world, rank, local):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     tbe.trace_enable(True)
+    path = {"auto": tbe.TBE_PATH_AUTO, "gather": tbe.TBE_PATH_GATHER, "histogram": tbe.TBE_PATH_HISTOGRAM}[args.path]
 
     def step(k):
         d = dev_in[k % N_BATCHES]
-        tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status)
+        tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status,
+                        path=path)
         tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p0.B, d["psw"], bufs=bufs,
                          dev_status=status, want_run_starts=False, want_sorted_positions=False)
 
@@ -358,7 +360,8 @@ def run_ours(args, world, rank, local):
             d = dev_in[k]
             gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
             with torch.cuda.graph(gf):
-                tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status)
+                tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status,
+                                path=path)
             with torch.cuda.graph(gb):
                 tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p0.B, d["psw"], bufs=bufs,
                                  dev_status=status, want_run_starts=False, want_sorted_positions=False)
@@ -372,7 +375,8 @@ def run_ours(args, world, rank, local):
             d = dev_in[k]
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status)
+                tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p0.B, d["psw"], out=out, dev_status=status,
+                                path=path)
                 tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p0.B, d["psw"], bufs=bufs,
                                  dev_status=status, want_run_starts=False, want_sorted_positions=False)
             out_graphs.append(g)
@@ -416,7 +420,7 @@ def run_ours(args, world, rank, local):
         step_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    for k in range(args.steps):  # forward / backward split
+    for k in range(args.steps):  # forward / backward split (separate graphs: each carries one graph launch)
         flush(k)
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         gf, gb = graphs[k % N_BATCHES]

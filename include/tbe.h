@@ -271,9 +271,14 @@ int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weigh
  *                        per warp at once
  *   red_unroll         : gradient slices in flight per lane in the backward
  *                        reduction (4: more resident warps, 8: deeper)
- *   fwd_ring           : 1 = rows of at most 512 bytes are copied into a ring
- *                        of shared memory (16 rows in flight per lane group);
- *                        0 = rows are loaded into registers
+ *   fwd_ring           : forward kernel for layouts whose rows are at most
+ *                        512 bytes: 2 = stream (a warp pools a run of
+ *                        consecutive bags as one stream of rows copied into
+ *                        a shared-memory ring), 1 = per-bag ring (16 rows in
+ *                        flight per lane group), 0 = rows loaded into
+ *                        registers, 3 = automatic (stream when every row
+ *                        is at most 256 bytes, else per-bag ring); rows
+ *                        wider than 512 bytes always use the register kernel
  *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
  *                        many as fit; 4 with fwd_unroll 4 selects a build
  *                        of the kernel with a smaller register budget)

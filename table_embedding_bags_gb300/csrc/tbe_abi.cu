@@ -15,7 +15,7 @@ namespace tbe {
 static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/0, /*fwd_unroll=*/4,
                           /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48,
                           /*short_item_lookups=*/32, /*fwd_lanes_per_row=*/16,
-                          /*red_unroll=*/4, /*fwd_ring=*/1};
+                          /*red_unroll=*/4, /*fwd_ring=*/3};
 
 const Tuning& tuning() { return g_tuning; }
 
@@ -121,7 +121,7 @@ int tbe_set_tuning(const tbe_tuning* in) {
   if (in->fwd_blocks_per_sm < 0 || in->fwd_blocks_per_sm > 32) return TBE_ERR_INVALID_ARG;
   if (in->hist_min_mean_bag < 0) return TBE_ERR_INVALID_ARG;
   if (in->red_unroll != 4 && in->red_unroll != 8) return TBE_ERR_INVALID_ARG;
-  if (in->fwd_ring != 0 && in->fwd_ring != 1) return TBE_ERR_INVALID_ARG;
+  if (in->fwd_ring < 0 || in->fwd_ring > 3) return TBE_ERR_INVALID_ARG;
   if (in->short_item_lookups < 32 || in->short_item_lookups > (1 << 20)) return TBE_ERR_INVALID_ARG;
   g_tuning.long_run_threshold = in->long_run_threshold;
   g_tuning.long_chunk = in->long_chunk;
@@ -250,6 +250,14 @@ int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, 
   p->any_weighted = any_weighted;
   if (((int64_t)p->sumD * osz) % 16 != 0) out_vec_ok = 0;
   p->out_vec_ok = out_vec_ok;
+  p->max_row_bytes = 0;
+  for (int32_t t = 0; t < T; ++t)
+    p->max_row_bytes = std::max(p->max_row_bytes, p->hmeta[t].D * elem_size(p->hmeta[t].dtype));
+  p->uniform = 1;
+  for (int32_t t = 1; t < T; ++t)
+    if (p->hmeta[t].D != p->hmeta[0].D || p->hmeta[t].dtype != p->hmeta[0].dtype ||
+        p->hmeta[t].weighted != p->hmeta[0].weighted)
+      p->uniform = 0;
   p->hist_ok = (T == 1 && L->weights_dtype[0] == TBE_F16 && p->hmeta[0].rows >= 1 &&
                 p->hmeta[0].rows <= TBE_HIST_MAX_ROWS && p->hmeta[0].D % 16 == 0 && p->hmeta[0].D <= 256);
   cudaGetDevice(&p->device);
@@ -316,6 +324,7 @@ int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* i
   a.sumD = plan->sumD;
   a.out_vec_ok = plan->out_vec_ok && (((uintptr_t)out & 15) == 0);
   a.lpr_max = g_tuning.fwd_lanes_per_row;
+  a.balance = plan->uniform ? 0 : 1;
   bool hist = false;
   if (path == TBE_PATH_HISTOGRAM) {
     if (!hist_eligible(plan, per_sample_weights)) return TBE_ERR_UNSUPPORTED;

@@ -343,11 +343,14 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
   const int64_t row_bytes = (int64_t)C * 16;
   const bool weighted = WT && m.weighted;
   const int win = kIdsPerLane * lpr;
-  float acc[KMAX][E];  // one accumulator set: rows arrive far slower than adds complete
+  // acc: the running sum, folded into tot every 64 rows so that no serial
+  // chain of fp32 adds is longer than 64 + len/64
+  float acc[KMAX][E], tot[KMAX][E];
 #pragma unroll
   for (int k = 0; k < KMAX; ++k)
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+    for (int e = 0; e < E; ++e) acc[k][e] = tot[k][e] = 0.f;
+  int rows_done = 0;
   bool bad = false;
   auto issue = [&](int j, int slot) {  // row j's chunks of this lane into ring slots slot*KMAX + k
     const int32_t id = ids[j];
@@ -409,6 +412,16 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
       if (j + RD < nwin) issue(j + RD, j & (RD - 1));  // refill the two slots just read
       if (j + 1 + RD < nwin) issue(j + 1 + RD, (j + 1) & (RD - 1));
       cp_commit();
+      rows_done += 2;
+      if ((rows_done & 63) == 0) {
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            add2(tot[k][e], tot[k][e + 1], acc[k][e], acc[k][e + 1]);
+            acc[k][e] = acc[k][e + 1] = 0.f;
+          }
+      }
     }
     __syncwarp(vmask);  // the ids are rewritten by the next window
   }
@@ -417,6 +430,8 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
   for (int k = 0; k < KMAX; ++k) {
     const int c = sub + k * lpr;
     if (c < C) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2) add2(acc[k][e], acc[k][e + 1], tot[k][e], tot[k][e + 1]);
       store_out<OutT>(out_row + (int64_t)c * E, acc[k], E, a.out_vec_ok);
     }
   }
@@ -548,6 +563,427 @@ int launch_ring_dt(const Plan& p, const FwdArgs& a, cudaStream_t s) {
   return launch_ring_w<OutT, -1>(p, a, s);
 }
 
+// ---------------------------------------------------------------------------
+// Stream variant (rows of at most 512 bytes; the default).
+//
+// A warp task is a run of consecutive bags of one table whose length is set
+// per table so that every task holds about the same number of lookups (the
+// table's mean bag length comes from the offsets at its first and last bag,
+// and the target is the batch spread evenly over the grid's warps).  The
+// warp reads the bounds of its bags with one request and lays the task's
+// lookups out as one stream of positions in shared memory: bag k takes
+// plen_k = max(R, len_k rounded up to R) positions, R = 32 / lpr rows per
+// step, so the R rows of a step always belong to one bag and every bag (an
+// empty one too) ends on a step.  Rows are copied with cp.async into a ring
+// of RG groups of four steps per lane and summed group by group (one wait,
+// four shared-memory reads, then the adds); the copies run across bag
+// boundaries, so the next bags' rows are in flight while a bag is finished.
+// Padding positions and ids outside their table are copied with source size
+// 0 (the slot is zero-filled and nothing is read), so the summing code has no
+// per-row tests.  At the last step of a bag the R row groups' sums are added
+// in a fixed butterfly order and group 0 stores the bag.
+// ---------------------------------------------------------------------------
+constexpr int kSThreads = 128;                       // threads per block
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSWin = 256;                           // stream positions staged per warp at once
+constexpr int kSGroup = 4;                           // steps per copy group
+constexpr int kSWinAlloc = kSWin + kSGroup * 32;     // room for the padding tail of the last group
+constexpr int kSRingStride = kSThreads * 16;         // bytes between a thread's ring slots
+constexpr int kSTaskMax = 192;                       // most lookups a task is sized for (one window)
+constexpr int kFoldGroups = 16;                      // groups (64 steps) summed before acc joins the bag total
+constexpr size_t kSSrcBytes = (size_t)kSWarps * kSWinAlloc * 8;
+constexpr size_t kSWtsBytes = (size_t)kSWarps * kSWinAlloc * 4;
+constexpr size_t kSTotBytes = (size_t)kSThreads * 8 * 4;  // folded sums: 8 floats per thread
+
+// A row of zeros (the widest row the stream kernel takes): padding
+// positions and ids outside their table are copied from here.
+__device__ __align__(16) unsigned char g_zero_row[512];
+
+// acc[e] += element e of a 16-byte chunk.  Half types use the mixed-precision
+// add (fp32 + fp16/bf16 -> fp32, one rounding), which equals converting the
+// half exactly to fp32 and adding; fp32 pairs use one packed add.
+template <int DT>
+__device__ __forceinline__ void accum_chunk(float* acc, const uint4& v) {
+  if (DT == TBE_F32) {
+    add2(acc[0], acc[1], __uint_as_float(v.x), __uint_as_float(v.y));
+    add2(acc[2], acc[3], __uint_as_float(v.z), __uint_as_float(v.w));
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (DT == TBE_F16)
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.f16 %0, l, %0;\n\tadd.rn.f32.f16 %1, h, %1;\n\t}"
+            : "+f"(acc[2 * k]), "+f"(acc[2 * k + 1]) : "r"(w[k]));
+      else
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+            : "+f"(acc[2 * k]), "+f"(acc[2 * k + 1]) : "r"(w[k]));
+    }
+  }
+}
+
+struct StreamTask {
+  int32_t t, b0, nb;
+};
+
+__device__ __forceinline__ StreamTask stream_locate(const int32_t* s_pref, const uint8_t* s_bpt, int32_t T,
+                                                    int32_t B, int32_t task) {
+  int lo = 0, hi = T - 1;  // table of the task: largest t with s_pref[t] <= task
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pref[mid] <= task) lo = mid; else hi = mid - 1;
+  }
+  StreamTask k;
+  k.t = lo;
+  const int bpt = s_bpt[lo];
+  k.b0 = (task - s_pref[lo]) * bpt;
+  k.nb = min(bpt, B - k.b0);
+  return k;
+}
+
+// Bounds of bag b0 + lane (lanes below nb), requested for a later task.
+__device__ __forceinline__ void stream_bounds(const FwdArgs& a, const StreamTask& k, int lane, int64_t& st,
+                                              int64_t& en) {
+  st = en = 0;
+  if (lane < k.nb) {
+    const int64_t g = (int64_t)k.t * a.B + k.b0 + lane;
+    st = ld_stream_i64(a.offsets + g);
+    en = ld_stream_i64(a.offsets + g + 1);
+  }
+}
+
+// Number of bags of the task whose inclusive padded end is <= p, i.e. the
+// bag holding stream position p (p < P).  `pincl` of lanes >= nb is P.
+__device__ __forceinline__ int stream_bag_of(int32_t pincl, int32_t p) {
+  int k = 0;
+#pragma unroll
+  for (int step = 16; step > 0; step >>= 1)
+    if (__shfl_sync(kFull, pincl, k + step - 1) <= p) k += step;
+  return k;
+}
+
+// One task: bags b0 .. b0 + nb - 1 of table m; lane k < nb holds the bounds
+// [st, en) of bag b0 + k (already checked).  `ring`: this thread's slot 0;
+// `srcs` / `wts`: the warp's stream window (row addresses and weights).
+template <int DT, bool WT, typename OutT, int RG>
+__device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m, const StreamTask& k, int lane,
+                                            int32_t st, int32_t en, uint32_t ring, unsigned long long* srcs,
+                                            float* wts, float* tot) {
+  constexpr int E = Chunk<DT>::kElems;
+  const int C = m.D / E;  // 16-byte chunks per row (<= 32)
+  const int lsh = C <= 1 ? 0 : 32 - __clz(C - 1);
+  const int lpr = 1 << lsh, rsh = 5 - lsh, R = 1 << rsh;
+  const int grp = lane >> lsh, sub = lane & (lpr - 1);
+  const bool live = sub < C;  // lanes past the row's last chunk copy nothing and store nothing
+  const bool weighted = WT && m.weighted;
+  const char* tbl = reinterpret_cast<const char*>(a.weights) + m.w_off;
+  const uint64_t row_bytes = (uint64_t)C * 16u;
+  const uint64_t zero_row = reinterpret_cast<uint64_t>(g_zero_row);
+  // padded stream: bag k occupies positions [pincl_k - plen_k, pincl_k)
+  const int32_t len = lane < k.nb ? en - st : 0;
+  const int32_t plen = lane < k.nb ? max(R, (len + R - 1) & ~(R - 1)) : 0;
+  int32_t pincl = plen;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(kFull, pincl, o);
+    if (lane >= o) pincl += y;
+  }
+  const int32_t P = __shfl_sync(kFull, pincl, 31);
+  const int32_t pst = pincl - plen;
+  bool bad = false;
+  // acc: the running sum since the bag's start or the last fold; tot (this
+  // thread's column of shared memory, stride kSThreads): the folded part,
+  // valid only while tot_live -- bags longer than kFoldGroups groups
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  bool tot_live = false;
+  int bag = 0;  // bags stored so far
+  OutT* out_ptr = reinterpret_cast<OutT*>(a.out) + (int64_t)k.b0 * a.sumD + m.col_off + sub * E;
+  const unsigned long long* my_srcs = srcs + grp;
+  const float* my_wts = wts + grp;
+  const uint32_t sub16 = (uint32_t)sub * 16u;
+
+#pragma unroll 1
+  for (int32_t win0 = 0; win0 < P; win0 += kSWin) {
+    const int32_t nwin = min(kSWin, P - win0);
+    const int32_t nsteps = nwin >> rsh;
+    const int32_t ngroups = (nsteps + kSGroup - 1) / kSGroup;
+    const int32_t npad = (ngroups * kSGroup) << rsh;  // positions of whole groups (<= kSWinAlloc - 31)
+    // row addresses (and weights) of positions win0 .. win0 + nwin - 1, then
+    // the zero row to npad; 128 positions per round, all loads issued first
+#pragma unroll 1
+    for (int32_t q0 = 0; q0 < npad; q0 += 128) {
+      int64_t raw[4];
+      int32_t iu[4];
+      bool vu[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int32_t q = q0 + u * 32 + lane;
+        const int32_t p = win0 + q;
+        const int kb = stream_bag_of(pincl, min(p, P - 1));
+        const int32_t r = p - __shfl_sync(kFull, pst, kb);
+        const int32_t lk = __shfl_sync(kFull, len, kb);
+        iu[u] = __shfl_sync(kFull, st, kb) + r;
+        vu[u] = q < nwin && r < lk;
+        raw[u] = vu[u] ? ld_stream_i64(a.indices + iu[u]) : 0;
+      }
+      float wv[4];
+      if (WT) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wv[u] = (weighted && vu[u]) ? ld_stream_f32(a.psw + iu[u]) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (q0 + u * 32 < npad) {
+          const bool ok = vu[u] && (uint64_t)raw[u] < (uint64_t)m.rows;
+          bad |= vu[u] && !ok;  // reported; contributes nothing
+          srcs[q0 + u * 32 + lane] = ok ? reinterpret_cast<uint64_t>(tbl) + (uint64_t)raw[u] * row_bytes : zero_row;
+          if (WT) wts[q0 + u * 32 + lane] = ok ? wv[u] : 0.f;
+        }
+      }
+    }
+    __syncwarp();
+    // steps 4g .. 4g + 3 into the ring slots of group g % RG
+    auto issue_group = [&](int32_t g) {
+      const uint32_t dst = ring + (uint32_t)((g % RG) * kSGroup) * kSRingStride;
+      const unsigned long long* s = my_srcs + ((g * kSGroup) << rsh);
+#pragma unroll
+      for (int j = 0; j < kSGroup; ++j)
+        if (live) cp_async16(dst + j * kSRingStride, reinterpret_cast<const char*>(s[j << rsh] + sub16));
+    };
+#pragma unroll
+    for (int g = 0; g < RG; ++g) {
+      if (g < ngroups) issue_group(g);
+      cp_commit();
+    }
+    uint32_t ends = 0;
+#pragma unroll 1
+    for (int32_t g = 0; g < ngroups; ++g) {
+      if ((g & 7) == 0) {  // which of steps 4g .. 4g + 31 end a bag
+        const int32_t sj = g * kSGroup + lane;
+        const int32_t p = win0 + (sj << rsh);
+        const int kb = stream_bag_of(pincl, min(p, P - 1));
+        const int32_t kend = __shfl_sync(kFull, pincl, kb);  // every lane takes part in the shuffle
+        ends = __ballot_sync(kFull, sj < nsteps && p + R == kend);
+      }
+      cp_wait<RG - 1>();  // group g has landed
+      const uint32_t src = ring + (uint32_t)((g % RG) * kSGroup) * kSRingStride;
+      uint4 v[kSGroup];
+#pragma unroll
+      for (int j = 0; j < kSGroup; ++j) v[j] = lds128(src + j * kSRingStride);
+      float w[kSGroup];
+      if (WT && weighted) {
+#pragma unroll
+        for (int j = 0; j < kSGroup; ++j) w[j] = my_wts[(g * kSGroup + j) << rsh];
+      }
+      const uint32_t eg = ends >> ((g & 7) * kSGroup);
+#pragma unroll
+      for (int j = 0; j < kSGroup; ++j) {
+        if (WT && weighted) {
+          float f[E];
+          Chunk<DT>::to_float(v[j], f);
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            mul2(f[e], f[e + 1], w[j]);  // the product is rounded to fp32, then added
+            add2(acc[e], acc[e + 1], f[e], f[e + 1]);
+          }
+        } else {
+          accum_chunk<DT>(acc, v[j]);
+        }
+        if (eg & (1u << j)) {  // last step of a bag: combine the row groups and store
+          float res[E];
+#pragma unroll
+          for (int e = 0; e < E; e += 2) {
+            res[e] = acc[e];
+            res[e + 1] = acc[e + 1];
+            if (tot_live) add2(res[e], res[e + 1], tot[e * kSThreads], tot[(e + 1) * kSThreads]);
+          }
+          for (int o = lpr; o < 32; o <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; e += 2)
+              add2(res[e], res[e + 1], __shfl_xor_sync(kFull, res[e], o), __shfl_xor_sync(kFull, res[e + 1], o));
+          }
+          if (grp == 0 && live) store_out<OutT>(out_ptr + (int64_t)bag * a.sumD, res, E, a.out_vec_ok);
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = 0.f;
+          tot_live = false;
+          ++bag;
+        }
+      }
+      if (g + RG < ngroups) issue_group(g + RG);  // refill the slots just read
+      cp_commit();
+      if ((((win0 >> rsh) / kSGroup + g) & (kFoldGroups - 1)) == kFoldGroups - 1) {  // bound the serial depth of acc
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+          float x = acc[e], y = acc[e + 1];
+          if (tot_live) add2(x, y, tot[e * kSThreads], tot[(e + 1) * kSThreads]);
+          tot[e * kSThreads] = x;
+          tot[(e + 1) * kSThreads] = y;
+          acc[e] = acc[e + 1] = 0.f;
+        }
+        tot_live = true;
+      }
+    }
+    __syncwarp();  // the window is rewritten next
+  }
+  if (__any_sync(kFull, bad) && lane == 0) report(a.status, TBE_DEV_BAD_INDEX);
+}
+
+template <typename OutT, int DTSEL, bool WT, int RG, int MINB>
+__global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdArgs a) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  constexpr size_t kRingB = (size_t)RG * kSGroup * kSThreads * 16;
+  float* s_tot = reinterpret_cast<float*>(dsm + kRingB);
+  unsigned long long* s_srcs = reinterpret_cast<unsigned long long*>(dsm + kRingB + kSTotBytes);
+  float* s_wts = reinterpret_cast<float*>(dsm + kRingB + kSTotBytes + kSSrcBytes);
+  int32_t* s_pref = reinterpret_cast<int32_t*>(dsm + kRingB + kSTotBytes + kSSrcBytes + (WT ? kSWtsBytes : 0));
+  uint8_t* s_bpt = reinterpret_cast<uint8_t*>(s_pref + a.T + 1);
+  __shared__ int32_t s_part[kSWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t nw = (int32_t)(gridDim.x * kSWarps);
+  const int32_t nb_all = a.T * a.B;
+  // lookups per task: the batch spread over the grid's warps, 32 .. kSTaskMax
+  const int64_t per_task = min((int64_t)kSTaskMax, max((int64_t)32, (a.N + nw - 1) / nw));
+  // bags per task at the batch's mean bag length.  Layouts whose tables all
+  // have one shape use it for every table, so a task's bags follow from its
+  // index alone; other layouts size every table's tasks from its own mean bag
+  // length (two offsets per table, read by every block)
+  const int bpt_u = a.N > 0 ? (int)min((int64_t)32, max((int64_t)1, (per_task * nb_all + a.N - 1) / a.N)) : 32;
+  const int32_t tpt_u = (a.B + bpt_u - 1) / bpt_u;
+  int32_t task = (int32_t)blockIdx.x * kSWarps + warp;
+  int32_t ntasks = a.T * tpt_u;
+  if (a.balance) {  // bags per task and first task of every table (block-wide scan, T/128 tables per thread)
+    const int per = (a.T + kSThreads - 1) / kSThreads;
+    int32_t mine = 0;
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) {
+        const int64_t lo = min(max(__ldg(a.offsets + (int64_t)t * a.B), (int64_t)0), a.N);
+        const int64_t hi = min(max(__ldg(a.offsets + (int64_t)(t + 1) * a.B), (int64_t)0), a.N);
+        const int64_t n = hi - lo;
+        const int bpt = n > 0 ? (int)min((int64_t)32, max((int64_t)1, (per_task * a.B + n - 1) / n)) : 32;
+        s_bpt[t] = (uint8_t)bpt;
+        mine += (a.B + bpt - 1) / bpt;
+      }
+    }
+    int32_t x = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) s_part[warp] = x;
+    __syncthreads();
+    int32_t run = x - mine;
+    for (int w = 0; w < warp; ++w) run += s_part[w];
+    for (int q = 0; q < per; ++q) {
+      const int t = tid * per + q;
+      if (t < a.T) {
+        s_pref[t] = run;
+        run += (a.B + s_bpt[t] - 1) / s_bpt[t];
+      }
+    }
+    if (tid == kSThreads - 1) s_pref[a.T] = run;
+    __syncthreads();
+    ntasks = s_pref[a.T];
+  }
+  auto locate = [&](int32_t k) {
+    if (a.balance) return stream_locate(s_pref, s_bpt, a.T, a.B, k);
+    StreamTask r{k / tpt_u, (k % tpt_u) * bpt_u, 0};
+    r.nb = min(bpt_u, a.B - r.b0);
+    return r;
+  };
+  const uint32_t ring = smem_u32(dsm) + tid * 16;
+  unsigned long long* srcs = s_srcs + warp * kSWinAlloc;
+  float* wts = s_wts + warp * kSWinAlloc;
+  StreamTask cur{0, 0, 0};
+  int64_t cs = 0, ce = 0;
+  if (task < ntasks) {
+    cur = locate(task);
+    stream_bounds(a, cur, lane, cs, ce);
+  }
+  while (task < ntasks) {
+    // the next task's bounds are requested while this one is pooled
+    const int32_t next = task + nw;
+    StreamTask nxt{0, 0, 0};
+    int64_t ns = 0, ne = 0;
+    if (next < ntasks) {
+      nxt = locate(next);
+      stream_bounds(a, nxt, lane, ns, ne);
+    }
+    if (lane < cur.nb) {  // offsets must start at 0, never decrease and end at N
+      const int32_t g = cur.t * a.B + cur.b0 + lane;
+      if (cs < 0 || ce < cs || ce > a.N || (g == 0 && cs != 0) || (g == nb_all - 1 && ce != a.N)) {
+        report(a.status, TBE_DEV_BAD_OFFSETS);
+        cs = ce = 0;  // pooled as empty
+      }
+    }
+    const TableMeta m = load_meta(a.meta + cur.t);
+    if (DTSEL >= 0) {
+      stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid);
+    } else {
+      switch (m.dtype) {
+        case TBE_F32: stream_task<TBE_F32, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+        case TBE_F16: stream_task<TBE_F16, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+        default: stream_task<TBE_BF16, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+      }
+    }
+    cur = nxt;
+    cs = ns;
+    ce = ne;
+    task = next;
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the block's shared memory
+}
+
+constexpr int kStreamRG = 2;    // copy groups in the ring (8 steps in flight per lane)
+constexpr int kStreamMinB = 6;  // resident blocks per SM the register budget targets
+
+size_t stream_smem_bytes(bool weighted, int32_t T) {
+  return (size_t)kStreamRG * kSGroup * kSThreads * 16 + kSTotBytes + kSSrcBytes + (weighted ? kSWtsBytes : 0) +
+         5 * ((size_t)T + 1) + 16;
+}
+
+template <typename OutT, int DTSEL, bool WT>
+int launch_stream(const FwdArgs& a, cudaStream_t s) {
+  auto kern = fwd_stream_kernel<OutT, DTSEL, WT, kStreamRG, kStreamMinB>;
+  const size_t smem = stream_smem_bytes(WT, a.T);
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 64) dev = 63;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem_bytes(WT, TBE_MAX_TABLES)) != cudaSuccess)
+      return TBE_ERR_CUDA;
+    configured[dev] = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem) != cudaSuccess || per_sm <= 0)
+    per_sm = 1;
+  if (tuning().fwd_blocks_per_sm > 0) per_sm = std::min(per_sm, tuning().fwd_blocks_per_sm);
+  const int64_t want = ((int64_t)a.T * a.B + kSWarps - 1) / kSWarps;  // a bag per warp at least
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * per_sm));
+  kern<<<grid, kSThreads, smem, s>>>(a);
+  return check_launch();
+}
+
+template <typename OutT, int DTSEL>
+int launch_stream_w(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (a.psw != nullptr && p.any_weighted) return launch_stream<OutT, DTSEL, true>(a, s);
+  return launch_stream<OutT, DTSEL, false>(a, s);
+}
+
+template <typename OutT>
+int launch_stream_dt(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+  if (p.dtype_mask == (1 << TBE_F16)) return launch_stream_w<OutT, TBE_F16>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_F32)) return launch_stream_w<OutT, TBE_F32>(p, a, s);
+  if (p.dtype_mask == (1 << TBE_BF16)) return launch_stream_w<OutT, TBE_BF16>(p, a, s);
+  return launch_stream_w<OutT, -1>(p, a, s);
+}
+
 bool ring_eligible(const Plan& p) {
   for (int t = 0; t < p.T; ++t)
     if (p.hmeta[t].D * (p.hmeta[t].dtype == TBE_F32 ? 4 : 2) > 512) return false;
@@ -601,8 +1037,23 @@ int launch_dtsel(const Plan& p, const FwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Widest row for which fwd_ring 3 (automatic) takes the stream kernel.  The
+// stream kernel keeps 8 steps of R = 512 / row_bytes rows in flight per warp;
+// for 512-byte rows (R = 1) that is half of what the per-bag ring keeps, and
+// the ring is faster there; for rows up to 256 bytes the stream kernel is
+// faster at every batch size measured (2 K .. 33 K lookups per SM).
+constexpr int kStreamMaxRowBytes = 256;
+
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s) {
-  if (tuning().fwd_ring && ring_eligible(p)) {
+  const int mode = tuning().fwd_ring == 3 ? (p.max_row_bytes <= kStreamMaxRowBytes ? 2 : 1) : tuning().fwd_ring;
+  if (mode == 2 && ring_eligible(p)) {
+    switch (p.out_dtype) {
+      case TBE_F32: return launch_stream_dt<float>(p, a, s);
+      case TBE_F16: return launch_stream_dt<__half>(p, a, s);
+      default: return launch_stream_dt<__nv_bfloat16>(p, a, s);
+    }
+  }
+  if (mode == 1 && ring_eligible(p)) {
     switch (p.out_dtype) {
       case TBE_F32: return launch_ring_dt<float>(p, a, s);
       case TBE_F16: return launch_ring_dt<__half>(p, a, s);

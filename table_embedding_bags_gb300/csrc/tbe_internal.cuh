@@ -41,6 +41,8 @@ struct Plan {
   int32_t dtype_mask;    // bit d set if some table has dtype d
   int32_t any_weighted;  // some table is marked weighted
   int32_t out_vec_ok;    // every output segment start is 16-byte aligned
+  int32_t uniform;       // every table has the same width, dtype and weighting
+  int32_t max_row_bytes; // widest row of the layout
   int32_t hist_ok;       // static part of the histogram-path eligibility
   int32_t device;        // device the plan was created on
   const TableMeta* dmeta;  // device copy (caller memory)
@@ -161,8 +163,8 @@ struct Chunk<TBE_BF16> {
   }
 };
 
-// Store n (4 or 8) floats rounded to the output type; `vec` selects 16-byte
-// stores when the destination is 16-byte aligned.
+// Store n (4 or 8) floats rounded to the output type; `vec` selects vector
+// stores (16 bytes, or 8 for four halves) when the destination is aligned.
 template <typename OutT>
 __device__ __forceinline__ void store_out(OutT* dst, const float* f, int n, bool vec);
 
@@ -187,6 +189,9 @@ __device__ __forceinline__ void store_out<__half>(__half* dst, const float* f, i
     v.z = *reinterpret_cast<uint32_t*>(&h2);
     v.w = *reinterpret_cast<uint32_t*>(&h3);
     *reinterpret_cast<uint4*>(dst) = v;
+  } else if (vec && n == 4) {
+    __half2 h0 = __floats2half2_rn(f[0], f[1]), h1 = __floats2half2_rn(f[2], f[3]);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
   } else {
     for (int k = 0; k < n; ++k) dst[k] = __float2half_rn(f[k]);
   }
@@ -204,6 +209,9 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* dst, con
     v.z = *reinterpret_cast<uint32_t*>(&h2);
     v.w = *reinterpret_cast<uint32_t*>(&h3);
     *reinterpret_cast<uint4*>(dst) = v;
+  } else if (vec && n == 4) {
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(f[0], f[1]), h1 = __floats2bfloat162_rn(f[2], f[3]);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<uint32_t*>(&h0), *reinterpret_cast<uint32_t*>(&h1));
   } else {
     for (int k = 0; k < n; ++k) dst[k] = __float2bfloat16_rn(f[k]);
   }
@@ -227,6 +235,7 @@ struct FwdArgs {
   int32_t sumD;
   int32_t out_vec_ok;
   int32_t lpr_max;  // lanes per row cap of the gather (a power of two <= 32)
+  int32_t balance;  // tables differ in shape: size each table's tasks by its own mean bag length
 };
 
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s);

@@ -51,7 +51,7 @@ def test_host_only_calls(lib):
 
 
 @pytest.mark.parametrize("field,bad", [("fwd_lanes_per_row", 3), ("fwd_lanes_per_row", 64), ("fwd_lanes_per_row", 0),
-                                       ("red_unroll", 6), ("fwd_ring", 2), ("short_item_lookups", 31),
+                                       ("red_unroll", 6), ("fwd_ring", 4), ("short_item_lookups", 31),
                                        ("fwd_blocks_per_sm", -1), ("long_run_threshold", 0)])
 def test_tuning_rejects_out_of_range(lib, field, bad):
     t = tbe.get_tuning()
@@ -62,7 +62,7 @@ def test_tuning_rejects_out_of_range(lib, field, bad):
 
 def test_tuning_round_trip(lib):
     t = tbe.get_tuning()
-    assert t["long_chunk"] == 0 and t["fwd_ring"] == 1 and t["red_unroll"] in (4, 8)
+    assert t["long_chunk"] == 0 and t["fwd_ring"] == 3 and t["red_unroll"] in (4, 8)
     try:
         tbe.set_tuning(long_chunk=128, short_item_lookups=64, fwd_lanes_per_row=8, red_unroll=8, fwd_ring=0)
         u = tbe.get_tuning()

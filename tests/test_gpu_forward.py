@@ -42,10 +42,11 @@ def check_full(tbe, p, path=None):
     return parity.compare_forward(p, parity.to_f64(out), ref, ref_abs)
 
 
-@pytest.fixture(params=[1, 0], ids=["ring", "registers"])
+@pytest.fixture(params=[2, 1, 0], ids=["stream", "ring", "registers"])
 def gather_mode(tbe, request):
-    """Runs a test with rows staged through the shared-memory ring (1) and
-    with rows loaded into registers (0)."""
+    """Runs a test with each gather kernel: the stream kernel (2, rows of at
+    most 512 bytes through a cp.async ring, bags of a task back to back), the
+    per-bag shared-memory ring (1) and rows loaded into registers (0)."""
     old = tbe.get_tuning()
     tbe.set_tuning(fwd_ring=request.param)
     yield request.param
@@ -100,6 +101,9 @@ def test_narrow_rows_long_bags(tbe, gather_mode, out_dt, weighted):
     lens[:, 7] = 0
     lens[1, 3] = 300
     lens[5, 44] = 97
+    lens[2, 9] = 1500  # fp32 bags far past the ~160-add depth a single serial fp32 sum guarantees
+    lens[0, 11] = 700
+    lens[9, 20] = 2000
     ids = [rng.integers(0, rows[t], size=int(lens[t].sum())) for t in range(T)]
     N = int(lens.sum())
     psw = rng.random(N).astype(np.float32) if weighted else None
