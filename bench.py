@@ -64,6 +64,10 @@ def parse_args():
     ap.add_argument("--path", choices=["auto", "gather", "histogram"], default="auto")
     ap.add_argument("--tuning", default=None,
                     help='JSON object of tbe_tuning fields to set first, e.g. \'{"long_run_threshold": 256}\'')
+    ap.add_argument("--sweep", choices=["backward", "histogram"], default=None,
+                    help="tuning sweeps: backward = long-run threshold x chunk on the run-length band, mid-size and "
+                         "backward-skew workloads; histogram = histogram path against the gather path over mean bag "
+                         "length x table rows; one JSON line per point")
     ap.add_argument("--profile", action="store_true",
                     help="plain launch loop for a profiler: --warmup then --steps eager steps, one JSON line")
     return ap.parse_args()
@@ -237,12 +241,13 @@ def dist_env():
     return world, rank, local
 
 
-def traffic_from_profiles(kernel):
+def traffic_from_profiles(kernel, workload=WORKLOAD):
     """DRAM bytes per launch measured by ncu for `kernel`, if the committed
-    summary was taken from the current source of that kernel."""
+    record (profiles/dram_traffic.json) was taken from the current source of
+    that kernel."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(path):
         return None
     srcs = {"fwd_gather": "tbe_forward.cu", "bwd_reduce": "tbe_backward.cu",
@@ -252,11 +257,11 @@ def traffic_from_profiles(kernel):
     if src is None:
         return None
     h = hashlib.sha256(open(os.path.join(ROOT, "table_embedding_bags_gb300", "csrc", src), "rb").read()).hexdigest()[:16]
-    for line in open(path):
-        if line.startswith("traffic:"):
-            f = dict(kv.split("=", 1) for kv in line[len("traffic:"):].split())
-            if f.get("kernel") == kernel and f.get("src_sha") == h and f.get("workload") == WORKLOAD:
-                return float(f["bytes_per_launch"])
+    with open(path) as f:
+        entries = json.load(f)["entries"]
+    for e in entries:
+        if e["kernel"] == kernel and e["src_sha"] == h and e["workload"] == workload:
+            return float(e["bytes_per_launch"])
     return None
 
 
@@ -296,6 +301,119 @@ def run_profile(args):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     return dict(profile=True, workload=args.workload, B=p.B, N=p.N, only=args.only, path=args.path,
                 steps=args.steps, wall_ms_per_step=1e3 * (time.perf_counter() - t0) / max(args.steps, 1))
+
+
+# ---------------------------------------------------------------------------
+# tuning sweeps
+# ---------------------------------------------------------------------------
+
+SWEEP_BWD_WORKLOADS = ["band_short", "band_mid", "band_long", "mid_skewed", "bwd_skew"]
+SWEEP_TAU = [16, 32, 64, 128, 256]
+SWEEP_CHUNK = [64, 128, 256]
+SWEEP_HIST_ROWS = [8, 16, 32, 64]
+SWEEP_HIST_LEN = [4, 8, 16, 32, 48, 64, 128, 256, 512]
+SWEEP_HIST_LOOKUPS = 4 << 20  # lookups per histogram-sweep batch (B = this / mean length)
+
+
+def time_replays(torch, fn, flush, reps, warm=2):
+    """Captures fn() in a CUDA graph and times `reps` replays, each after an
+    L2 flush, with CUDA events; returns (median, mean) in microseconds."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for k in range(warm):
+        flush(k)
+        g.replay()
+    torch.cuda.synchronize()
+    us = []
+    for k in range(reps):
+        flush(k)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        us.append(1e3 * e0.elapsed_time(e1))
+    return float(np.median(us)), float(np.mean(us))
+
+
+def sweep_backward(args, tbe, torch, flush):
+    """Backward time over long-run threshold x chunk (plus the defaults)."""
+    from tbe_inputs import make_config
+
+    default = tbe.get_tuning()
+    names = [args.workload] if args.workload != WORKLOAD else SWEEP_BWD_WORKLOADS
+    for name in names:
+        p = make_config(name, batch=0, B=args.B)
+        plan = tbe.Plan.from_problem(p)
+        ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
+        G = torch.from_numpy(p.grad_out).cuda()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        points = [(default["long_run_threshold"], default["long_chunk"])]
+        points += [(tau, ch) for tau in SWEEP_TAU for ch in SWEEP_CHUNK]
+        for tau, ch in points:
+            tbe.set_tuning(**dict(default, long_run_threshold=tau, long_chunk=ch))
+            bufs = tbe.BackwardBuffers(plan, p.B, p.N)
+
+            def fn():
+                tbe.tbe_backward(plan, G, ind, off, p.B, None, bufs=bufs, dev_status=status,
+                                 want_run_starts=False, want_sorted_positions=False)
+
+            med, mean = time_replays(torch, fn, flush, args.steps)
+            assert int(status.item()) == 0, f"device status {int(status.item())}"
+            U = int(bufs.unique_count[-1].item())
+            print(json.dumps(dict(sweep="backward", workload=name, N=p.N, U=U, long_run_threshold=tau,
+                                  long_chunk=ch, default=(tau, ch) == points[0], median_us=round(med, 2),
+                                  mean_us=round(mean, 2))), flush=True)
+            del bufs
+    tbe.set_tuning(**default)
+
+
+def sweep_histogram(args, tbe, torch, flush):
+    """Forward time of the histogram path and of the gather path on one fp16
+    table of `rows` x 128 with bag lengths U{L/2 .. 3L/2} and uniform ids."""
+    from tbe_inputs import DT_F16, DT_F32, make_problem, materialize_weights
+
+    for rows in SWEEP_HIST_ROWS:
+        for L in SWEEP_HIST_LEN:
+            B = int(min(262144, max(1024, SWEEP_HIST_LOOKUPS // L)))
+            rng = np.random.default_rng([rows, L])
+            lens = rng.integers(max(1, L // 2), L + L // 2 + 1, size=(1, B))
+            ids = [rng.integers(0, rows, size=int(lens.sum()))]
+            p = make_problem(1, B, rows=[rows], D=[128], weights_dtype=[DT_F16], out_dtype=DT_F32,
+                             lengths=lens, ids=ids, seed=rows * 1000 + L)
+            w = materialize_weights(p, device="cuda")
+            plan = tbe.Plan.from_problem(p)
+            ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
+            out = torch.empty((B, 128), dtype=torch.float32, device="cuda")
+            status = torch.zeros(1, dtype=torch.int32, device="cuda")
+            res = {}
+            for path, code in (("histogram", tbe.TBE_PATH_HISTOGRAM), ("gather", tbe.TBE_PATH_GATHER)):
+                def fn(code=code):
+                    tbe.tbe_forward(plan, w, ind, off, B, out=out, dev_status=status, path=code)
+
+                res[path] = time_replays(torch, fn, flush, args.steps)[0]
+            assert int(status.item()) == 0, f"device status {int(status.item())}"
+            print(json.dumps(dict(sweep="histogram", rows=rows, mean_bag=L, B=B, N=p.N,
+                                  histogram_us=round(res["histogram"], 2), gather_us=round(res["gather"], 2),
+                                  faster="histogram" if res["histogram"] < res["gather"] else "gather")), flush=True)
+
+
+def run_sweep(args):
+    import torch
+
+    import table_embedding_bags_gb300 as tbe
+
+    tbe.load_library()
+    torch.cuda.set_device(0)
+    apply_tuning(tbe, args.tuning)
+    flush = L2Flush(torch.device("cuda", 0))
+    if args.sweep == "backward":
+        sweep_backward(args, tbe, torch, flush)
+    else:
+        sweep_histogram(args, tbe, torch, flush)
 
 
 def run_ours(args, world, rank, local):
@@ -693,6 +811,9 @@ def main():
 
     if args.profile:
         print(json.dumps(run_profile(args)), flush=True)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     if world > 1:
         import torch.distributed as dist

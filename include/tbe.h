@@ -283,7 +283,8 @@ int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weigh
  *                        many as fit; 4 with fwd_unroll 4 selects a build
  *                        of the kernel with a smaller register budget)
  *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
- *                        N / B reaches this
+ *                        N / B reaches this; 0 (default) = the measured gate:
+ *                        16 for tables of at most 32 rows, 32 above
  *   short_item_lookups : lookups per work item of the short-run tier (runs
  *                        are grouped by 32 and cut into parts of about this
  *                        many lookups; raised to long_run_threshold if lower)

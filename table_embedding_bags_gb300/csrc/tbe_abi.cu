@@ -11,9 +11,17 @@
 
 namespace tbe {
 
-// Defaults come from the measured sweeps recorded with the benchmark.
+// Defaults, from sweeps timed on GB300 with `bench.py --sweep`:
+//  - long_run_threshold 32 with the automatic chunk (64 for batches of about
+//    0.3-1.3 M lookups, 256 from about 5 M) was the fastest, or within 3 %
+//    of it, of threshold {16, 32, 64, 128, 256} x chunk {64, 128, 256} on the
+//    mid-size, backward-skew and three run-length band workloads; a threshold
+//    of 256 was 1.34x slower on runs of 32..255 lookups;
+//  - hist_min_mean_bag 0 selects the measured gate: the histogram path beat
+//    the gather path from a mean bag length of 16 on tables of up to 32 rows
+//    and from 32 on tables of 33..64 rows (fp16, D = 128).
 static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/0, /*fwd_unroll=*/4,
-                          /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/48,
+                          /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/0,
                           /*short_item_lookups=*/32, /*fwd_lanes_per_row=*/16,
                           /*red_unroll=*/4, /*fwd_ring=*/3};
 
@@ -296,6 +304,12 @@ static int check_common(const tbe_plan* plan, const int64_t* indices, int64_t N,
   return TBE_OK;
 }
 
+// Mean bag length from which TBE_PATH_AUTO takes the histogram path.
+static int64_t hist_gate(const tbe_plan& plan) {
+  if (g_tuning.hist_min_mean_bag > 0) return g_tuning.hist_min_mean_bag;
+  return plan.hmeta[0].rows <= 32 ? 16 : 32;
+}
+
 static bool hist_eligible(const tbe_plan* plan, const float* psw) {
   return plan->hist_ok && (psw == nullptr || !plan->hmeta[0].weighted);
 }
@@ -331,7 +345,7 @@ int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* i
     hist = true;
   } else if (path == TBE_PATH_AUTO) {
     hist = hist_eligible(plan, per_sample_weights) &&
-           N >= (int64_t)g_tuning.hist_min_mean_bag * (int64_t)B;
+           N >= (int64_t)hist_gate(*plan) * (int64_t)B;
   }
   trace_begin(s);
   st = hist ? launch_forward_histogram(*plan, a, nullptr, s) : launch_forward_gather(*plan, a, s);
