@@ -312,6 +312,22 @@ int tbe_set_tuning(const tbe_tuning* in);
 int tbe_trace_enable(int32_t on);
 int tbe_trace_read(float* stage_ms, const char** stage_names, int32_t max_stages);
 
+/*
+ * Failure-reporting self-test ([FBT] "Three tiers, routed by run length":
+ * the fused tier's arrival counter is a wait between kernels' blocks; here
+ * every such wait is bounded and reports a status instead of hanging).
+ * Runs one of the library's bounded waits on something that never
+ * completes and lets it give up after `polls` polls:
+ *   kind 0 : the look-back word wait of the backward's scans, on a word no
+ *            kernel publishes;
+ *   kind 1 : the mbarrier wait of the histogram path, on a barrier that
+ *            expects one arrival that never comes (no copy is in flight).
+ * The kernel then OR-s TBE_DEV_TIMEOUT into *dev_status (device int32) and
+ * returns; nothing traps, and the device stays usable.
+ * Errors: TBE_ERR_INVALID_ARG (kind not 0/1, polls outside 1..2^20, null
+ * dev_status), TBE_ERR_CUDA. */
+int tbe_wait_selftest(int32_t kind, int32_t polls, int32_t* dev_status, void* stream);
+
 /* Human-readable text for a return code. */
 const char* tbe_status_string(int32_t code);
 

@@ -30,7 +30,7 @@ EXPORTED = [
     "tbe_plan_device_bytes", "tbe_plan_create", "tbe_plan_destroy", "tbe_forward", "tbe_forward_path",
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
-    "tbe_backward_static_workspace", "tbe_exact_update",
+    "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -104,6 +104,8 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_status_string.argtypes = [i32]
     lib.tbe_version.restype = ctypes.c_char_p
     lib.tbe_version.argtypes = []
+    lib.tbe_wait_selftest.restype = ctypes.c_int
+    lib.tbe_wait_selftest.argtypes = [i32, i32, P, P]
     _lib = lib
     return lib
 
@@ -312,6 +314,14 @@ def trace_read(max_stages: int = 32):
     if n < 0:
         raise TBEError(f"tbe_trace_read failed ({-n})")
     return [(names[k].decode(), float(ms[k])) for k in range(n)]
+
+
+def wait_selftest(kind: int, polls: int, dev_status, stream=None):
+    """Runs one of the library's bounded waits on something that never
+    completes (kind 0: a look-back word, 1: an mbarrier); it gives up after
+    `polls` polls and sets TBE_DEV_TIMEOUT in dev_status."""
+    _check(load_library().tbe_wait_selftest(int(kind), int(polls), _ptr(dev_status), _stream(stream)),
+           "tbe_wait_selftest")
 
 
 def version() -> str:

@@ -43,6 +43,33 @@ int sm_count() {
 int check_launch() { return cudaGetLastError() == cudaSuccess ? TBE_OK : TBE_ERR_CUDA; }
 
 // ---------------------------------------------------------------------------
+// bounded-wait self-test
+// ---------------------------------------------------------------------------
+namespace {
+// A look-back word that no kernel ever publishes (device memory is zero at
+// load time and nothing writes it).
+__device__ uint32_t g_unpublished_word;
+
+// One thread runs one of the library's bounded waits on something that
+// never completes -- kind 0: the look-back word wait of the backward's scans,
+// kind 1: the mbarrier wait of the histogram path (a barrier that expects
+// one arrival; nothing arrives and no copy is in flight) -- and reports
+// TBE_DEV_TIMEOUT when it gives up after `polls` polls.
+__global__ void wait_selftest_kernel(int32_t kind, int32_t polls, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  bool ok;
+  if (kind == 0) {
+    ok = poll_word(&g_unpublished_word, 0xffffffffu, polls) != 0;
+  } else {
+    mbar_init(&bar);
+    ok = mbar_wait(&bar, 0, polls);
+  }
+  if (!ok) report(status, TBE_DEV_TIMEOUT);
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // stage tracing
 // ---------------------------------------------------------------------------
 namespace {
@@ -91,6 +118,12 @@ struct tbe_plan : public tbe::Plan {};
 extern "C" {
 
 const char* tbe_version(void) { return "libtbe 0.1 (sm_103a)"; }
+
+int tbe_wait_selftest(int32_t kind, int32_t polls, int32_t* dev_status, void* stream) {
+  if ((kind != 0 && kind != 1) || polls < 1 || polls > (1 << 20) || !dev_status) return TBE_ERR_INVALID_ARG;
+  wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(kind, polls, dev_status);
+  return check_launch();
+}
 
 const char* tbe_status_string(int32_t code) {
   switch (code) {

@@ -76,11 +76,8 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 // Out of line: waiting is the rare path, and inlined copies would only grow
 // the hot code that every block fetches.
 __device__ __noinline__ uint32_t wait_flag(const uint32_t* p, int32_t* status) {
-  for (int it = 0; it < kSpinLimit; ++it) {
-    uint32_t v = ld_relaxed(p);
-    if (v & (kFlagAgg | kFlagInc)) return v;
-    if (it > 64) __nanosleep(100);
-  }
+  const uint32_t v = poll_word(p, kFlagAgg | kFlagInc, kSpinLimit);
+  if (v) return v;
   report(status, TBE_DEV_TIMEOUT);
   return kFlagInc;
 }

@@ -53,9 +53,6 @@ struct HistLayout {
   }
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // Canonical K-major layout without swizzle: element (row, k) of an operand
 // with `rows` rows sits in core matrix (row / 8, k / 8); core matrices are
@@ -76,27 +73,6 @@ __device__ __forceinline__ uint32_t instr_desc_f16(int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Bounded wait for phase `parity` of the barrier; false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  for (int it = 0; it < kWaitLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(a), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -261,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
       }
       mma_commit(mbar);
     }
-    const bool ok = mbar_wait(mbar, phase);
+    const bool ok = mbar_wait(mbar, phase, kWaitLimit);
     phase ^= 1u;
     if (__syncthreads_or(!ok)) {  // the whole CTA stops together
       if (tid == 0) report(a.status, TBE_DEV_TIMEOUT);

@@ -239,6 +239,47 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   return v;
 }
 
+
+// ---------------------------------------------------------------------------
+// bounded waits (every wait in the library gives up after a number of polls
+// and lets the caller report TBE_DEV_TIMEOUT; no kernel waits forever)
+// ---------------------------------------------------------------------------
+
+// Polls *p (relaxed, GPU scope) until (*p & mask) != 0; returns the word, or
+// 0 after `limit` polls.
+__device__ inline uint32_t poll_word(const uint32_t* p, uint32_t mask, int limit) {
+  for (int it = 0; it < limit; ++it) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v & mask) return v;
+    if (it > 64) __nanosleep(100);
+  }
+  return 0;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Waits for phase `parity` of the shared-memory barrier; false after `limit`
+// polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit) {
+  const uint32_t a = smem_u32(bar);
+  for (int it = 0; it < limit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // launchers (host)
 // ---------------------------------------------------------------------------

@@ -75,6 +75,9 @@ def test_tuning_round_trip(lib):
     assert lib.tbe_plan_create(None, None, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_forward(None, None, None, 0, None, 0, None, None, None, None) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_backward_workspace_bytes(None, 1, 1) == 0
+    # the bounded-wait self-test checks its arguments before any CUDA call
+    assert lib.tbe_wait_selftest(2, 10, None, None) == tbe.TBE_ERR_INVALID_ARG
+    assert lib.tbe_wait_selftest(0, 0, None, None) == tbe.TBE_ERR_INVALID_ARG
 
 
 def test_exact_update_rejects_without_plan(lib):

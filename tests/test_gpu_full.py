@@ -77,7 +77,14 @@ def test_forward_full_size_sampled(tbe, name):
     parity.compare_forward(p, got, ref[None, :], ref_abs[None, :], cols=np.concatenate(cols))
 
 
-@pytest.mark.parametrize("name", ["mixed", "bwd_skew"])
+def auto_chunk(N):
+    """Lookups per long-run chunk the library picks for a batch of N lookups
+    with the default tuning: N / (128 x SMs) rounded down to 32, in 64..256."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return min(256, max(64, N // (4 * 32 * sms) // 32 * 32))
+
+
+@pytest.mark.parametrize("name", ["mixed", "small_table", "bwd_skew"])
 def test_backward_full_size(tbe, name):
     p = make_config(name)
     d = parity.upload(p)
@@ -115,5 +122,9 @@ def test_backward_full_size(tbe, name):
     got = np.concatenate([rg_all[int(s):int(s) + int(D[t])].cpu().numpy() for s, t in zip(starts, t_of)])
     parity.compare_rowgrads(got.astype(np.float64), rg, rabs)
     assert lens.max() >= 256  # the workload exercises the chunked long-run tier
+    if name == "small_table":
+        # 18.9 M lookups on 64 rows: runs of ~295 K lookups are cut into more
+        # than 32 x 32 chunks, so the fan-in-32 combine tree has three levels
+        assert -(-int(lens.max()) // auto_chunk(p.N)) > 32 * 32
     del d, bufs
     _free()
