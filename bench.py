@@ -510,6 +510,20 @@ def run_ours(args, world, rank, local):
     with torch.cuda.graph(upd_graph):
         tbe.tbe_exact_update(plan, weights, bufs, tbe.TBE_OPT_EXACT_ROWWISE_ADAGRAD, OPT_LR, OPT_EPS,
                              momentum=momentum, dev_status=status)
+    # the same Adagrad step fused into the backward (tbe_backward_update), for
+    # layouts whose rows have at most 128 columns
+    fused_graphs = []
+    if int(p0.D.max()) <= 128:
+        fbufs = tbe.BackwardBuffers(plan, p0.B, nmax, device=dev, row_grads_capacity=0)
+        for k in range(N_BATCHES):
+            d = dev_in[k]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                tbe.tbe_backward_update(plan, weights, tbe.TBE_OPT_EXACT_ROWWISE_ADAGRAD, OPT_LR, d["grad"],
+                                        d["indices"], d["offsets"], p0.B, d["psw"], eps=OPT_EPS, momentum=momentum,
+                                        bufs=fbufs, dev_status=status, want_run_starts=False,
+                                        want_sorted_positions=False)
+            fused_graphs.append(g)
     graphs = capture(False)
     traced_graphs = capture(True)
     for k in range(args.warmup):
@@ -519,6 +533,8 @@ def run_ours(args, world, rank, local):
         graphs[k % N_BATCHES][1].replay()
         traced_graphs[k % N_BATCHES][1].replay()
         upd_graph.replay()
+        if fused_graphs:
+            fused_graphs[k % N_BATCHES].replay()
     torch.cuda.synchronize()
 
     if world > 1:
@@ -572,6 +588,16 @@ def run_ours(args, world, rank, local):
         e1.synchronize()
         upd_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
+    fused_ms = []
+    for k in range(args.steps if fused_graphs else 0):  # backward + Adagrad step as one call
+        flush(k)
+        e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        e0.record(stream)
+        fused_graphs[k % N_BATCHES].replay()
+        e1.record(stream)
+        e1.synchronize()
+        fused_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -609,6 +635,12 @@ def run_ours(args, world, rank, local):
                      traffic=traffic_from_profiles("exact_update"),
                      placement="timed alone right after the backward of the same batch (row gradients still in L2, "
                                "tables and momentum flushed with the step's L2 flush)")
+    if fused_ms:
+        optimizer["fused"] = dict(
+            ms=float(np.mean(fused_ms)), separate_ms=float(np.mean(bwd_ms)) + upd_mean,
+            note="tbe_backward_update: the same step applied where each row gradient is finished inside the "
+                 "backward (no row gradients written); separate_ms = backward graph + update graph, each after "
+                 "its own L2 flush")
 
     # e2e through the public API with host buffers
     e2e = None

@@ -257,6 +257,31 @@ int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weigh
                      void* stream);
 
 /*
+ * Backward with the exact optimizer fused into it ([FBT] "Why the backward
+ * is the hard half": the update runs once per distinct row, on its finished
+ * gradient, inside the backward; "Three tiers, routed by run length": the
+ * long-run tier's last chunk applies it).  Same inputs and indexing outputs
+ * as tbe_backward, but no row gradients are emitted: where a row's gradient
+ * is finished -- the short-run tier's end of run, a one-chunk long run, or
+ * the root of a long run's combine -- the row of `weights` (and its momentum)
+ * is updated in place exactly as tbe_exact_update would update it, bit for
+ * bit (same FP32 operations in the same order).
+ *   opt, weights, momentum : as for tbe_exact_update (momentum may be NULL for
+ *                            SGD)
+ *   everything else        : as for tbe_backward (workspace size from
+ *                            tbe_backward_workspace_bytes)
+ * Every table's width must be at most 128 columns (a row gradient is one
+ * quad per lane of one warp), else TBE_ERR_UNSUPPORTED; wider layouts use
+ * tbe_backward followed by tbe_exact_update.
+ * Errors: as tbe_backward, plus TBE_ERR_INVALID_ARG for an invalid optimizer
+ * or a missing weights / momentum buffer. */
+int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                        const float* grad_out, const int64_t* indices, int64_t N, const int64_t* offsets,
+                        int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                        int32_t* sorted_positions, int64_t* unique_count, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/*
  * Tuning knobs (process-wide; set them before launching work that should
  * use them, not concurrently with launches).
  *   long_run_threshold : runs with at least this many lookups take the

@@ -30,7 +30,7 @@ EXPORTED = [
     "tbe_plan_device_bytes", "tbe_plan_create", "tbe_plan_destroy", "tbe_forward", "tbe_forward_path",
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
-    "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest",
+    "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest", "tbe_backward_update",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -104,6 +104,9 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_status_string.argtypes = [i32]
     lib.tbe_version.restype = ctypes.c_char_p
     lib.tbe_version.argtypes = []
+    lib.tbe_backward_update.restype = ctypes.c_int
+    lib.tbe_backward_update.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, P, i64, P, i32, P, P, P, P, P, P, sz,
+                                        P, P]
     lib.tbe_wait_selftest.restype = ctypes.c_int
     lib.tbe_wait_selftest.argtypes = [i32, i32, P, P]
     _lib = lib
@@ -284,6 +287,27 @@ def tbe_exact_update(plan: Plan, weights, bufs: BackwardBuffers, kind: int, lear
                                          bufs.row_grads_capacity, _ptr(bufs.unique_count), _ptr(dev_status),
                                          _stream(stream))
     _check(rc, "tbe_exact_update")
+
+
+def tbe_backward_update(plan: Plan, weights, kind: int, learning_rate: float, grad_out, indices, offsets, B: int,
+                        per_sample_weights=None, eps: float = 0.0, momentum=None, bufs=None, dev_status=None,
+                        want_run_starts=True, want_sorted_positions=True, stream=None):
+    """Backward with the exact optimizer fused in: updates ``weights`` (and
+    ``momentum`` for row-wise Adagrad) in place; ``bufs`` receives the
+    indexing outputs (its row_grads are not written)."""
+    lib = load_library()
+    N = int(indices.numel())
+    if bufs is None:
+        bufs = BackwardBuffers(plan, B, N, device=indices.device, row_grads_capacity=0)
+    opt = Optimizer(int(kind), float(learning_rate), float(eps))
+    rc = lib.tbe_backward_update(plan.handle, ctypes.byref(opt), _ptr(weights), _ptr(momentum), _ptr(grad_out),
+                                 _ptr(indices), N, _ptr(offsets), int(B), _ptr(per_sample_weights),
+                                 _ptr(bufs.unique_rows), _ptr(bufs.run_starts) if want_run_starts else None,
+                                 _ptr(bufs.sorted_positions) if want_sorted_positions else None,
+                                 _ptr(bufs.unique_count), _ptr(bufs.workspace), bufs.workspace.numel(),
+                                 _ptr(dev_status), _stream(stream))
+    _check(rc, "tbe_backward_update")
+    return bufs
 
 
 def get_tuning() -> dict:

@@ -422,15 +422,18 @@ size_t tbe_backward_workspace_bytes(const tbe_plan* plan, int32_t B, int64_t N) 
   return backward_workspace_bytes(*plan, B, N);
 }
 
-int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
-                 const int64_t* offsets, int32_t B, const float* per_sample_weights,
-                 int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
-                 int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
-                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+// Shared by tbe_backward and tbe_backward_update: checks and launches the
+// backward; `opt` (may be null) fuses the exact optimizer into the reducer.
+static int backward_call(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
+                         const int64_t* offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
+                         int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
+                         int64_t row_grads_capacity, int64_t* unique_count, void* workspace, size_t workspace_bytes,
+                         int32_t* dev_status, void* stream, const tbe_optimizer* opt, void* weights,
+                         float* momentum) {
   int st = check_common(plan, indices, N, offsets, B);
   if (st != TBE_OK) return st;
   if (!unique_count || row_grads_capacity < 0) return TBE_ERR_INVALID_ARG;
-  if (N > 0 && (!unique_rows || !grad_out || (!row_grads && row_grads_capacity > 0)))
+  if (N > 0 && (!unique_rows || !grad_out || (!opt && !row_grads && row_grads_capacity > 0)))
     return TBE_ERR_INVALID_ARG;
   if ((uintptr_t)grad_out & 15) return TBE_ERR_UNSUPPORTED;
   if ((plan->sumD % 4) != 0) return TBE_ERR_UNSUPPORTED;
@@ -448,8 +451,8 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
   a.unique_rows = unique_rows;
   a.run_starts = run_starts;
   a.sorted_positions = sorted_positions;
-  a.row_grads = row_grads;
-  a.row_grads_capacity = row_grads_capacity;
+  a.row_grads = opt ? nullptr : row_grads;
+  a.row_grads_capacity = opt ? INT64_MAX : row_grads_capacity;
   a.unique_count = unique_count;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
@@ -458,9 +461,44 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
   a.B = B;
   a.N = N;
   a.sumD = plan->sumD;
+  a.opt_kind = opt ? opt->kind : -1;
+  a.lr = opt ? opt->learning_rate : 0.f;
+  a.eps = opt ? opt->eps : 0.f;
+  a.weights = static_cast<uint8_t*>(weights);
+  a.momentum = momentum;
   cudaStream_t s = (cudaStream_t)stream;
   trace_begin(s);
   return launch_backward(*plan, a, s);
+}
+
+int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
+                 const int64_t* offsets, int32_t B, const float* per_sample_weights,
+                 int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
+                 int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
+                 size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return backward_call(plan, grad_out, indices, N, offsets, B, per_sample_weights, unique_rows, run_starts,
+                       sorted_positions, row_grads, row_grads_capacity, unique_count, workspace, workspace_bytes,
+                       dev_status, stream, nullptr, nullptr, nullptr);
+}
+
+// Optimizer arguments valid on the host (kind, finite rate, eps >= 0).
+static bool opt_ok(const tbe_optimizer* opt) {
+  return opt && (opt->kind == TBE_OPT_EXACT_SGD || opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD) &&
+         std::isfinite(opt->learning_rate) && std::isfinite(opt->eps) && opt->eps >= 0.f;
+}
+
+int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                        const float* grad_out, const int64_t* indices, int64_t N, const int64_t* offsets,
+                        int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                        int32_t* sorted_positions, int64_t* unique_count, void* workspace,
+                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!plan || !opt_ok(opt)) return TBE_ERR_INVALID_ARG;
+  if (plan->maxD > 128) return TBE_ERR_UNSUPPORTED;  // a row gradient is one quad per lane of one warp
+  if (N > 0 && (!weights || (opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum))) return TBE_ERR_INVALID_ARG;
+  if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
+  return backward_call(plan, grad_out, indices, N, offsets, B, per_sample_weights, unique_rows, run_starts,
+                       sorted_positions, nullptr, 0, unique_count, workspace, workspace_bytes, dev_status, stream,
+                       opt, weights, momentum);
 }
 
 int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,

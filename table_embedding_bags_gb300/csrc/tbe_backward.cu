@@ -1172,6 +1172,11 @@ struct RedArgs {
   const int2* sub_list;       // short-run work items {batch, part}
   int64_t capacity;
   int32_t T, B, sumD, tau, chunk, slot_floats, item_lookups;
+  // fused exact optimizer (tbe_backward_update): every finished row gradient
+  // updates its table row (and momentum) in place instead of being stored
+  uint8_t* weights;
+  float* momentum;
+  float lr, eps;
 };
 
 // Where run u's row gradient goes and how wide it is.
@@ -1180,6 +1185,7 @@ struct RunInfo {
   int32_t col_off;   // first grad_out column of its table
   int32_t D;
   int32_t weighted;
+  int32_t t;         // its table
 };
 
 // Per-table row-gradient offsets and unique-row counts staged in shared
@@ -1192,6 +1198,7 @@ __shared__ int64_t s_red_uc[kRedSmemT + 1];
 __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
   const int32_t t = a.run_table[u];
   RunInfo r;
+  r.t = t;
   r.D = __ldg(&a.meta[t].D);
   r.col_off = __ldg(&a.meta[t].col_off);
   r.weighted = (a.psw_sorted != nullptr) && __ldg(&a.meta[t].weighted);
@@ -1235,6 +1242,83 @@ __device__ __forceinline__ void add_slice(float4& acc, float4 g, float w) {
   }
   add2(acc.x, acc.y, g.x, g.y);
   add2(acc.z, acc.w, g.z, g.w);
+}
+
+// Fused exact optimizer ([FBT] "Why the backward is the hard half": the
+// update runs once per distinct row on its finished gradient).  OPT is 0 (no
+// update: row gradients are stored), TBE_OPT_EXACT_SGD + 1 or
+// TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1.  Rows have at most 128 columns, so lane
+// c holds columns 4c .. 4c + 3 of a row gradient (zero past the row).  The
+// arithmetic is the update kernel's, so fused and separate steps agree bit
+// for bit.
+
+// Weights of global row `row` of table t: row bytes and dtype.
+__device__ __forceinline__ uint8_t* weight_row(const RedArgs& a, int t, int64_t row, int& dt) {
+  const TableMeta* m = a.meta + t;
+  dt = __ldg(&m->dtype);
+  const int64_t id = row - __ldg(&m->row_base);
+  return a.weights + __ldg(&m->w_off) + id * (int64_t)__ldg(&m->D) * (dt == TBE_F32 ? 4 : 2);
+}
+
+// Updates one row from its gradient (lane quads); all lanes call it.
+template <int OPT>
+__device__ __forceinline__ void update_row(const RedArgs& a, int t, int64_t row, float4 g, int lane) {
+  int dt;
+  uint8_t* w = weight_row(a, t, row, dt);
+  const int D = __ldg(&a.meta[t].D);
+  const bool live = lane * 4 < D;
+  const size_t qb = (size_t)lane * (dt == TBE_F32 ? 16 : 8);
+  float4 wv = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (live) wv = load_quad(dt, w + qb);
+  float step = a.lr;
+  if (OPT == TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1) {
+    const float m_old = a.momentum[row];
+    const float ss = warp_sum(sum_sq(g, 0.f));
+    float m_new = 0.f;
+    step = adagrad_step(a.lr, a.eps, m_old, ss, D, &m_new);
+    __syncwarp();  // every lane has read the old momentum
+    if (lane == 0) a.momentum[row] = m_new;
+  }
+  if (live) store_quad(dt, w + qb, fma_quad(step, g, wv));
+}
+
+// Rows finished by the short-run tier wait in a per-warp shared-memory
+// buffer: their gradient (lane quads) and their weights, which the lanes
+// start copying (cp.async) the moment the row is finished, so the copy runs
+// while the warp reduces the next runs.  Once at least kPendFlush rows wait
+// (checked after every UNR <= kPendFlush lookups, so at most
+// 2 * kPendFlush - 1 ever wait) they are updated from shared memory and
+// stored; nothing is loaded from global memory at that point.
+constexpr int kPendFlush = 4;
+constexpr int kPend = 2 * kPendFlush;
+
+struct PendRow {
+  uint8_t* w;     // the row's weights
+  int64_t row;    // global row (momentum index)
+  float m;        // its momentum before the step (row-wise Adagrad)
+  int32_t dt, D;
+};
+
+template <int OPT>
+__device__ __forceinline__ void update_pending(const RedArgs& a, const float4* pend_g, const uint4* pend_w,
+                                               const PendRow* pend, int n, int lane) {
+  asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's weight copies have landed
+#pragma unroll 1
+  for (int r = 0; r < n; ++r) {
+    const PendRow pr = pend[r];
+    const float4 g = pend_g[r * 32 + lane];
+    const uint4 raw = pend_w[r * 32 + lane];
+    const bool live = lane * 4 < pr.D;
+    const float4 wv = load_quad(pr.dt, reinterpret_cast<const uint8_t*>(&raw));
+    float step = a.lr;
+    if (OPT == TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1) {
+      const float ss = warp_sum(sum_sq(g, 0.f));
+      float m_new = 0.f;
+      step = adagrad_step(a.lr, a.eps, pr.m, ss, pr.D, &m_new);
+      if (lane == 0) a.momentum[pr.row] = m_new;
+    }
+    if (live) store_quad(pr.dt, pr.w + (size_t)lane * (pr.dt == TBE_F32 ? 16 : 8), fma_quad(step, g, wv));
+  }
 }
 
 __device__ __forceinline__ float4 ld_grad(const float* p) {
@@ -1303,7 +1387,7 @@ __device__ void sum_lookups(const RedArgs& a, const RunInfo& r, int32_t j0, int3
 // children-1 after a device-scope fence) sums the children in index order
 // and writes the node's slot, or the row gradient at the root.  The order of
 // every sum is fixed, so the result does not depend on arrival order.
-template <bool W, int UNR>
+template <bool W, int UNR, int OPT>
 __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
   const int4 rec = a.long_list[item];  // the record of the chunk's run
   const int32_t u = rec.x, e0 = rec.y, nch = rec.z, len = rec.w;
@@ -1318,9 +1402,10 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
     sum_lookups<W, UNR>(a, r, j0, j1, cb, lane, acc);
     const float4 v = acc.sum();
     const int c = (cb >> 2) + lane;
-    if (nch == 1)
-      store_col(a.row_grads, v, c, C4, a.capacity, r.out_off);
-    else
+    if (nch == 1) {
+      if (OPT) update_row<OPT>(a, r.t, a.unique_rows[u], v, lane);  // a one-chunk run is finished here
+      else store_col(a.row_grads, v, c, C4, a.capacity, r.out_off);
+    } else
       store_col(a.partials + (int64_t)(e0 + k) * a.slot_floats, v, c, C4, (int64_t)1 << 62, 0);
   }
   if (nch == 1) return;
@@ -1350,9 +1435,10 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
           s.w = __fadd_rn(s.w, x.w);
         }
       }
-      if (pnodes == 1)
-        store_col(a.row_grads, s, c, C4, a.capacity, r.out_off);
-      else
+      if (pnodes == 1) {
+        if (OPT) update_row<OPT>(a, r.t, a.unique_rows[u], s, lane);  // the root: the run's gradient is finished
+        else store_col(a.row_grads, s, c, C4, a.capacity, r.out_off);
+      } else
         store_col(a.partials + (int64_t)(e0 + parent * pspan) * a.slot_floats, s, c, C4, (int64_t)1 << 62, 0);
     }
     if (pnodes == 1) return;  // root written: the row gradient is complete
@@ -1371,16 +1457,28 @@ __device__ void long_chunk(const RedArgs& a, int32_t item, int lane) {
 // lookups).  The warp reduces the part's stream and stores a run's row
 // gradient at its last lookup.  Long runs are skipped (their chunks are
 // separate work items).
-template <bool W, int UNR>
-__device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32_t U, int lane) {
+template <bool W, int UNR, int OPT>
+__device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32_t U, int lane, float4* pend_g,
+                            uint4* pend_w, PendRow* pend) {
   const int32_t u = batch * 32 + lane;
   int32_t rs = 0, len = 0;
-  RunInfo r{0, 0, 4, 0};
+  // fused update: global row, weights, dtype and old momentum of run u
+  int64_t run_row = 0;
+  uint8_t* run_wrow = nullptr;
+  int32_t run_dt = TBE_F32;
+  float run_m = 0.f;
+  RunInfo r{0, 0, 4, 0, 0};
   if (u < U) {
     rs = a.run_starts[u];
     len = a.run_starts[u + 1] - rs;
     r = run_info(a, u);
+    if (OPT) {
+      run_row = a.unique_rows[u];
+      run_wrow = weight_row(a, r.t, run_row, run_dt);
+      if (OPT == TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1) run_m = a.momentum[run_row];
+    }
   }
+  int npend = 0;  // rows waiting in pend (fused update)
   int32_t cnt = (u < U && len < a.tau) ? len : 0;
   {  // keep the runs of this part
     int32_t x = cnt;
@@ -1449,9 +1547,29 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
       // lookup q ends its run: store the run's row gradient
       auto flush = [&](int q) {
         const int rr = __shfl_sync(kFull, my_r, q);
-        const int64_t off = __shfl_sync(kFull, r.out_off, rr);
-        const int32_t c4 = __shfl_sync(kFull, st_c4, rr);
-        if (c < c4) *reinterpret_cast<float4*>(a.row_grads + off + 4 * c) = acc;
+        if (OPT) {  // park the finished gradient and start copying the row's weights
+          const int64_t row = __shfl_sync(kFull, run_row, rr);
+          const unsigned long long wbits = __shfl_sync(kFull, (unsigned long long)(uintptr_t)run_wrow, rr);
+          uint8_t* w = (uint8_t*)(uintptr_t)wbits;
+          const int32_t dt = __shfl_sync(kFull, run_dt, rr);
+          const int32_t D = __shfl_sync(kFull, r.D, rr);
+          const float m = __shfl_sync(kFull, run_m, rr);
+          pend_g[npend * 32 + lane] = acc;
+          if (lane * 4 < D) {
+            const uint32_t dst = smem_u32(pend_w + npend * 32 + lane);
+            if (dt == TBE_F32)
+              cp_async16(dst, w + (size_t)lane * 16);
+            else
+              asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(w + (size_t)lane * 8) : "memory");
+          }
+          cp_commit();
+          if (lane == 0) pend[npend] = PendRow{w, row, m, dt, D};
+          ++npend;
+        } else {
+          const int64_t off = __shfl_sync(kFull, r.out_off, rr);
+          const int32_t c4 = __shfl_sync(kFull, st_c4, rr);
+          if (c < c4) *reinterpret_cast<float4*>(a.row_grads + off + 4 * c) = acc;
+        }
         acc = make_float4(0.f, 0.f, 0.f, 0.f);
       };
 #pragma unroll 2
@@ -1475,15 +1593,34 @@ __device__ void short_batch(const RedArgs& a, int32_t batch, int32_t part, int32
           add_slice<W>(acc, g[uu], W ? __shfl_sync(kFull, my_w, (q0 + uu) & 31) : 1.f);
           if ((ends >> (q0 + uu)) & 1u) flush(q0 + uu);
         }
+        if (OPT && npend >= kPendFlush) {  // UNR <= kPendFlush lookups ended at most that many runs
+          __syncwarp();
+          update_pending<OPT>(a, pend_g, pend_w, pend, npend, lane);
+          __syncwarp();  // the buffer is refilled next
+          npend = 0;
+        }
       }
     }
+  }
+  if (OPT && npend > 0) {
+    __syncwarp();
+    update_pending<OPT>(a, pend_g, pend_w, pend, npend, lane);
+    __syncwarp();
   }
 }
 
 // UNR: grad_out slices in flight per lane; MINB: resident blocks per SM the
 // register budget targets.
-template <bool W, int UNR, int MINB>
+// Per-warp shared memory of the fused update: kPend gradients, their weights
+// and their row records.
+constexpr size_t kPendBytesPerWarp = (size_t)kPend * 32 * 16 * 2 + kPend * sizeof(PendRow);
+
+template <bool W, int UNR, int MINB, int OPT>
 __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs a) {
+  extern __shared__ __align__(16) unsigned char red_pend[];
+  float4* pend_g = reinterpret_cast<float4*>(red_pend + (threadIdx.x >> 5) * kPendBytesPerWarp);
+  uint4* pend_w = reinterpret_cast<uint4*>(pend_g + kPend * 32);
+  PendRow* pend = reinterpret_cast<PendRow*>(pend_w + kPend * 32);
   wait_predecessor();
   release_dependents();
   if (a.T <= kRedSmemT) {
@@ -1504,10 +1641,10 @@ __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs
   while ((int32_t)item < n_items) {
     if (lane == 0) claim = atomicAdd(&a.counters[kCntWork * kCntStride], 1u);
     if ((int32_t)item < n_chunks) {
-      long_chunk<W, UNR>(a, (int32_t)item, lane);
+      long_chunk<W, UNR, OPT>(a, (int32_t)item, lane);
     } else {
       const int2 rec = a.sub_list[item - n_chunks];
-      short_batch<W, UNR>(a, rec.x, rec.y, U, lane);
+      short_batch<W, UNR, OPT>(a, rec.x, rec.y, U, lane, pend_g, pend_w, pend);
     }
     item = __shfl_sync(kFull, claim, 0);
   }
@@ -1518,11 +1655,11 @@ __global__ void __launch_bounds__(kRedThreads, MINB) reduce_kernel(const RedArgs
 // reading what the predecessor wrote.  Triggers stay implicit (block exit),
 // so it starts only once every block of the predecessor has finished.
 template <typename Arg>
-int launch_pdl(void (*kernel)(Arg), int grid, int threads, cudaStream_t s, const Arg& arg) {
+int launch_pdl(void (*kernel)(Arg), int grid, int threads, cudaStream_t s, const Arg& arg, size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3((unsigned)threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1721,19 +1858,37 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
   rd.item_lookups = L.item_lookups;
   rd.sub_list = at<int2>(ws, L.sub_list);
   rd.slot_floats = L.slot_floats;
+  rd.weights = a.weights;
+  rd.momentum = a.momentum;
+  rd.lr = a.lr;
+  rd.eps = a.eps;
   const bool weighted = rd.psw_sorted != nullptr;
-  const bool deep = tu.red_unroll == 8;
-  void (*kern)(RedArgs) = weighted ? (deep ? reduce_kernel<true, 8, 3> : reduce_kernel<true, 4, 4>)
-                                   : (deep ? reduce_kernel<false, 8, 3> : reduce_kernel<false, 4, 4>);
-  static int red_grid[4][64] = {{0}};
+  const int opt = a.opt_kind < 0 ? 0 : a.opt_kind + 1;
+  const bool deep = tu.red_unroll == 8 && opt == 0;  // the fused update uses the 4-slice build
+  void (*kern)(RedArgs);
+  if (opt == 0)
+    kern = weighted ? (deep ? reduce_kernel<true, 8, 3, 0> : reduce_kernel<true, 4, 4, 0>)
+                    : (deep ? reduce_kernel<false, 8, 3, 0> : reduce_kernel<false, 4, 4, 0>);
+  else if (opt == TBE_OPT_EXACT_SGD + 1)
+    kern = weighted ? reduce_kernel<true, 4, 3, TBE_OPT_EXACT_SGD + 1> : reduce_kernel<false, 4, 3, TBE_OPT_EXACT_SGD + 1>;
+  else
+    kern = weighted ? reduce_kernel<true, 4, 3, TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1>
+                    : reduce_kernel<false, 4, 3, TBE_OPT_EXACT_ROWWISE_ADAGRAD + 1>;
+  const size_t smem = opt ? (size_t)(kRedThreads / 32) * kPendBytesPerWarp : 0;
+  static int red_grid[8][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) dev = 63;
-  const int variant = (weighted ? 2 : 0) + (deep ? 1 : 0);
-  if (red_grid[variant][dev] == 0) red_grid[variant][dev] = grid_for((const void*)kern, kRedThreads);
+  const int variant = opt == 0 ? (weighted ? 1 : 0) + (deep ? 2 : 0) : 4 + (weighted ? 1 : 0) + 2 * (opt - 1);
+  if (red_grid[variant][dev] == 0) {
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return TBE_ERR_CUDA;
+    red_grid[variant][dev] = grid_for((const void*)kern, kRedThreads, smem);
+  }
   const int64_t want = ((N + 31) / 32 + 7) / 8 + 1;
   const int rgrid = (int)std::max<int64_t>(1, std::min<int64_t>(red_grid[variant][dev], want));
-  if (launch_pdl(kern, rgrid, kRedThreads, s, rd)) return TBE_ERR_CUDA;
+  if (launch_pdl(kern, rgrid, kRedThreads, s, rd, smem)) return TBE_ERR_CUDA;
   trace_mark(s, "bwd_reduce");
   return TBE_OK;
 }

@@ -280,6 +280,75 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int li
   return false;
 }
 
+
+// ---------------------------------------------------------------------------
+// exact optimizer arithmetic (shared by the update kernel and the backward's
+// fused update, so the two give bit-identical weights and momenta)
+// ---------------------------------------------------------------------------
+
+// Four consecutive elements of a table row of dtype dt, as floats and back
+// (stores round to nearest-even); p is 16-byte aligned for fp32, 8 for halves.
+__device__ __forceinline__ float4 load_quad(int dt, const uint8_t* p) {
+  if (dt == TBE_F32) return *reinterpret_cast<const float4*>(p);
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  if (dt == TBE_F16) {
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),  // bf16: exact
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+__device__ __forceinline__ void store_quad(int dt, uint8_t* p, float4 v) {
+  if (dt == TBE_F32) {
+    *reinterpret_cast<float4*>(p) = v;
+    return;
+  }
+  uint2 u;
+  if (dt == TBE_F16) {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    u.x = *reinterpret_cast<uint32_t*>(&a);
+    u.y = *reinterpret_cast<uint32_t*>(&b);
+  }
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// w - step * g, element by element, each one fused multiply-add.
+__device__ __forceinline__ float4 fma_quad(float step, float4 g, float4 w) {
+  w.x = fmaf(-step, g.x, w.x);
+  w.y = fmaf(-step, g.y, w.y);
+  w.z = fmaf(-step, g.z, w.z);
+  w.w = fmaf(-step, g.w, w.w);
+  return w;
+}
+
+// acc + the squares of the quad's elements (fused multiply-adds in order).
+__device__ __forceinline__ float sum_sq(float4 v, float acc) {
+  acc = fmaf(v.x, v.x, acc);
+  acc = fmaf(v.y, v.y, acc);
+  acc = fmaf(v.z, v.z, acc);
+  return fmaf(v.w, v.w, acc);
+}
+
+// Sum over the warp by an xor butterfly (offsets 16, 8, 4, 2, 1).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Row-wise Adagrad: new momentum m + ss / D and the step lr / (sqrt(m') + eps),
+// each operation rounded once (fp32).
+__device__ __forceinline__ float adagrad_step(float lr, float eps, float m_old, float ss, int D, float* m_new) {
+  *m_new = __fadd_rn(m_old, __fdiv_rn(ss, (float)D));
+  return __fdiv_rn(lr, __fadd_rn(__fsqrt_rn(*m_new), eps));
+}
+
 // ---------------------------------------------------------------------------
 // launchers (host)
 // ---------------------------------------------------------------------------
@@ -323,6 +392,11 @@ struct BwdArgs {
   int32_t B;
   int64_t N;
   int32_t sumD;
+  // fused exact optimizer: opt_kind TBE_OPT_* or -1 (row gradients are stored)
+  int32_t opt_kind;
+  float lr, eps;
+  uint8_t* weights;
+  float* momentum;
 };
 
 size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N);

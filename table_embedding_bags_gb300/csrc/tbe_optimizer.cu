@@ -34,85 +34,6 @@ constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ void wait_predecessor() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Four consecutive elements of a table row, as floats and back (stores round
-// to nearest-even).  Callers keep the address 8-byte aligned (16 for fp32):
-// rows start on 16-byte boundaries and the column is a multiple of 4.
-template <int DT>
-struct Quad;
-
-template <>
-struct Quad<TBE_F32> {
-  __device__ __forceinline__ static float4 load(const uint8_t* p) { return *reinterpret_cast<const float4*>(p); }
-  __device__ __forceinline__ static void store(uint8_t* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-};
-
-template <>
-struct Quad<TBE_F16> {
-  __device__ __forceinline__ static float4 load(const uint8_t* p) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-    return make_float4(a.x, a.y, b.x, b.y);
-  }
-  __device__ __forceinline__ static void store(uint8_t* p, float4 v) {
-    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-  }
-};
-
-template <>
-struct Quad<TBE_BF16> {
-  __device__ __forceinline__ static float4 load(const uint8_t* p) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);  // bf16 -> fp32 is exact: the bits move up
-    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-  }
-  __device__ __forceinline__ static void store(uint8_t* p, float4 v) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<uint32_t*>(&a);
-    u.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(p) = u;
-  }
-};
-
-// Four consecutive elements of a row of any table dtype.
-__device__ __forceinline__ float4 load_quad(int dt, const uint8_t* p) {
-  if (dt == TBE_F32) return Quad<TBE_F32>::load(p);
-  if (dt == TBE_F16) return Quad<TBE_F16>::load(p);
-  return Quad<TBE_BF16>::load(p);
-}
-
-__device__ __forceinline__ void store_quad(int dt, uint8_t* p, float4 v) {
-  if (dt == TBE_F32) Quad<TBE_F32>::store(p, v);
-  else if (dt == TBE_F16) Quad<TBE_F16>::store(p, v);
-  else Quad<TBE_BF16>::store(p, v);
-}
-
-__device__ __forceinline__ float4 fma_quad(float step, float4 g, float4 w) {
-  w.x = fmaf(-step, g.x, w.x);
-  w.y = fmaf(-step, g.y, w.y);
-  w.z = fmaf(-step, g.z, w.z);
-  w.w = fmaf(-step, g.w, w.w);
-  return w;
-}
-
-__device__ __forceinline__ float sum_sq(float4 v, float acc) {
-  acc = fmaf(v.x, v.x, acc);
-  acc = fmaf(v.y, v.y, acc);
-  acc = fmaf(v.z, v.z, acc);
-  return fmaf(v.w, v.w, acc);
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  return v;
-}
-
 // Where one distinct row's update reads and writes.
 struct RowJob {
   const float* g;   // its gradient (D floats)
@@ -133,8 +54,7 @@ constexpr int kRowsPerWarp = 4;
 template <int KIND>
 __device__ __forceinline__ float row_step(const UpdArgs& a, float m_old, float ss, int D, float* m_new) {
   if (KIND != TBE_OPT_EXACT_ROWWISE_ADAGRAD) return a.lr;
-  *m_new = __fadd_rn(m_old, __fdiv_rn(ss, (float)D));
-  return __fdiv_rn(a.lr, __fadd_rn(__fsqrt_rn(*m_new), a.eps));
+  return adagrad_step(a.lr, a.eps, m_old, ss, D, m_new);
 }
 
 template <int KIND>
