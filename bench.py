@@ -226,6 +226,12 @@ class L2Flush:
         torch.sum(self.r, dim=0, out=self.acc)
 
 
+def spread(ms):
+    """Mean, median and 90th percentile of a list of times (microseconds)."""
+    a = 1e3 * np.asarray(ms, np.float64)
+    return dict(mean_us=float(a.mean()), median_us=float(np.median(a)), p90_us=float(np.percentile(a, 90)))
+
+
 def apply_tuning(tbe, spec):
     """Sets the tbe_tuning fields named in the JSON object `spec` (None: the
     library's defaults) and returns the tuning in effect."""
@@ -598,6 +604,18 @@ def run_ours(args, world, rank, local):
         e1.synchronize()
         fused_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
+    warm_ms = []
+    for k in range(args.steps):  # the same step graphs with the L2 left warm by the previous replay
+        e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        e0.record(stream)
+        step_graphs[k % N_BATCHES].replay()
+        e1.record(stream)
+        e1.synchronize()
+        warm_ms.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    control = None
+    if args.workload == WORKLOAD:
+        control = run_uniform_control(args, tbe, torch, plan, weights, out, bufs, status, dev, flush, stream)
     clocks = sampler.stop()
     if world > 1:
         torch.distributed.barrier()
@@ -668,6 +686,9 @@ def run_ours(args, world, rank, local):
         stages_ms={k: float(np.mean(v)) for k, v in stage.items()},
         n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=float(np.mean(step_ms)),
+        spread=dict(step=spread(step_ms), fwd=spread(fwd_ms), bwd=spread(bwd_ms)),
+        warm_l2=dict(step=spread(warm_ms), GBps=(fwd_bytes + bwd_bytes) / (sum(warm_ms) / 1e3) / 1e9,
+                     note="the step graphs replayed back to back with no L2 flush"),
         wall_s=t_wall,
         higher_is_better=True, scaling="weak", vs_baseline=None,
         dtype="f32", data="synthetic",
@@ -677,9 +698,7 @@ def run_ours(args, world, rank, local):
                     l2="flushed before every step (256 MB write + 256 MB read of another buffer, outside the step events)",
                     table_dtype="/".join(sorted({DT_NAMES[int(d)] for d in p0.weights_dtype})), accumulate="f32",
                     out_dtype=DT_NAMES[int(p0.out_dtype)], parallelism=f"replicas x{world}"),
-        roofline=dict(bound="hbm", kernel=dom, achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
-                      peak_kind=f"{peak_kind} (copy)", bytes_per_launch=kb[dom], launch_ms=per_kernel[dom],
-                      traffic=traffic_from_profiles(dom)),
+        roofline=roofline_entry(dom, kb[dom], per_kernel[dom], achieved, peak, peak_kind),
         optimizer=optimizer,
         clocks=clocks,
         gpu_launches=args.steps + sum(bwd_kernels),
@@ -688,7 +707,81 @@ def run_ours(args, world, rank, local):
     )
     if e2e is not None:
         res["e2e"] = e2e
+    if control is not None:
+        res["control_uniform"] = control
     return res, (fwd_bytes + bwd_bytes), tot_s, lookups
+
+
+# what the ncu captures of the dominant kernels show limits them (mid-size
+# skewed workload), for the roofline entry
+LIMITERS = {
+    "fwd_gather": "issue and dependent-load latency (DRAM bytes equal the compulsory bytes; DRAM and L2 "
+                  "throughput far below peak)",
+    "bwd_reduce": "L2 latency of the bag -> grad_out chain (grad_out and the row gradients stay in L2; DRAM "
+                  "traffic is a few per cent of the algorithmic bytes)",
+}
+
+
+def roofline_entry(kernel, nbytes, launch_ms, achieved, peak, peak_kind):
+    """Roofline of the dominant kernel.  `achieved` is the effective rate
+    (algorithmic bytes per launch / launch time); `dram_frac` is the HBM
+    side: the ncu-measured DRAM bytes of a launch (when the committed record
+    matches the current source) over the same time, against the same peak."""
+    traffic = traffic_from_profiles(kernel)
+    dram = None if traffic is None else traffic / (launch_ms * 1e-3) / 1e9
+    return dict(bound="hbm", kernel=kernel, achieved=achieved, achieved_kind="effective (algorithmic bytes)",
+                peak=peak, unit="GB/s", frac=achieved / peak, peak_kind=f"{peak_kind} (copy)",
+                bytes_per_launch=nbytes, launch_ms=launch_ms, traffic=traffic,
+                dram_GBps=dram, dram_frac=None if dram is None else dram / peak,
+                limiter=LIMITERS.get(kernel))
+
+
+def run_uniform_control(args, tbe, torch, plan, weights, out, bufs, status, dev, flush, stream):
+    """The mid-size workload's tables, bag lengths and empty bags with
+    uniform ids (no skew): forward and backward graphs timed like the
+    headline's split."""
+    from tbe_inputs import make_config
+
+    probs = [make_config("mid_uniform", batch=k) for k in range(2)]
+    outs = []
+    for p in probs:
+        d = dict(indices=torch.from_numpy(p.indices).to(dev), offsets=torch.from_numpy(p.offsets).to(dev),
+                 grad=torch.from_numpy(p.grad_out).to(dev))
+        if p.N > bufs.N:
+            return None
+        gf, gb = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p.B, out=out, dev_status=status)
+        tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p.B, bufs=bufs, dev_status=status,
+                         want_run_starts=False, want_sorted_positions=False)
+        torch.cuda.synchronize()
+        U = np.diff(bufs.unique_count.cpu().numpy())
+        with torch.cuda.graph(gf):
+            tbe.tbe_forward(plan, weights, d["indices"], d["offsets"], p.B, out=out, dev_status=status)
+        with torch.cuda.graph(gb):
+            tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p.B, bufs=bufs, dev_status=status,
+                             want_run_starts=False, want_sorted_positions=False)
+        outs.append((p, d, gf, gb, U))
+    fwd_ms, bwd_ms, fb, bb = [], [], 0, 0
+    for k in range(args.warmup + args.steps):
+        p, d, gf, gb, U = outs[k % len(outs)]
+        flush(k)
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        gf.replay()
+        e1.record(stream)
+        gb.replay()
+        e2.record(stream)
+        e2.synchronize()
+        if k >= args.warmup:
+            fwd_ms.append(e0.elapsed_time(e1))
+            bwd_ms.append(e1.elapsed_time(e2))
+            f, b = effective_bytes(p, U)
+            fb += f
+            bb += b
+    return dict(workload="mid_uniform: the mid-size tables, bag lengths and empty bags with uniform ids",
+                lookups=int(np.mean([o[0].N for o in outs])), unique_rows=int(np.mean([o[4].sum() for o in outs])),
+                fwd=dict(spread(fwd_ms), GBps=fb / (sum(fwd_ms) / 1e3) / 1e9),
+                bwd=dict(spread(bwd_ms), GBps=bb / (sum(bwd_ms) / 1e3) / 1e9))
 
 
 def run_e2e(args, tbe, torch, plan, probs, weights, out, bufs, status, dev, flush, uniq):

@@ -221,14 +221,17 @@ def tbe_backward_workspace_bytes(plan: Plan, B: int, N: int) -> int:
 
 
 class BackwardBuffers:
-    """Preallocated outputs + workspace for one (B, N) capacity."""
+    """Preallocated outputs + workspace for one (B, N) capacity
+    (with_workspace=False: outputs only, for tbe_backward_static_workspace)."""
 
-    def __init__(self, plan: Plan, B: int, N: int, device="cuda", row_grads_capacity=None):
+    def __init__(self, plan: Plan, B: int, N: int, device="cuda", row_grads_capacity=None, with_workspace=True):
         import torch
 
         self.B, self.N = int(B), int(N)
-        ws = tbe_backward_workspace_bytes(plan, B, N)
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
+        self.workspace = None
+        if with_workspace:
+            ws = tbe_backward_workspace_bytes(plan, B, N)
+            self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=device)
         self.unique_rows = torch.empty(max(N, 1), dtype=torch.int64, device=device)
         self.run_starts = torch.empty(N + 1, dtype=torch.int32, device=device)
         self.sorted_positions = torch.empty(max(N, 1), dtype=torch.int32, device=device)
@@ -266,7 +269,7 @@ def tbe_backward_static_workspace(plan: Plan, grad_out, indices, offsets, B: int
     lib = load_library()
     N = int(indices.numel())
     if bufs is None:
-        bufs = BackwardBuffers(plan, B, N, device=indices.device)
+        bufs = BackwardBuffers(plan, B, N, device=indices.device, with_workspace=False)
     rc = lib.tbe_backward_static_workspace(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
                                            _ptr(per_sample_weights), _ptr(bufs.unique_rows), _ptr(bufs.run_starts),
                                            _ptr(bufs.sorted_positions), _ptr(bufs.row_grads),

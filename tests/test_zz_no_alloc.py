@@ -5,8 +5,9 @@ or code running while a global-mode stream capture forbids cudaMalloc --
 cannot provide a workspace.  tbe_backward_static_workspace() serves them from
 an array compiled into the library.  This file checks, through the C ABI,
 that two calls in a row give the same rows, run boundaries, sorted positions
-and row gradients as tbe_backward() with a caller workspace, and that a batch
-too large for the array is refused.  It is collected last so that a run that
+and row gradients as tbe_backward() with a caller workspace, that the second
+call leaves the device's allocated and free memory unchanged, and that a
+batch too large for the array is refused.  It is collected last so that a run that
 stops at the first failure has already run every other test; it also passes
 on its own in a fresh process.
 """
@@ -53,10 +54,14 @@ def test_static_workspace_matches_caller_workspace(tbe):
     torch.cuda.synchronize()
     ref = _outputs(ref_bufs, p.N)
     lib = tbe.load_library()
+    outs = [tbe.BackwardBuffers(plan, p.B, p.N, with_workspace=False) for _ in range(2)]
+    statuses = [torch.zeros(1, dtype=torch.int32, device="cuda") for _ in range(2)]
     for call in range(2):  # the array keeps the previous call's contents
-        bufs = tbe.BackwardBuffers(plan, p.B, p.N)
-        bufs.workspace = None  # not used by this entry point
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        bufs, status = outs[call], statuses[call]
+        assert bufs.workspace is None
+        torch.cuda.synchronize()
+        if call == 1:  # after the first call (which looks up the array's address): nothing is allocated
+            used_before, free_before = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
         rc = lib.tbe_backward_static_workspace(
             plan.handle, ctypes.c_void_p(d["grad"].data_ptr()), ctypes.c_void_p(d["indices"].data_ptr()), p.N,
             ctypes.c_void_p(d["offsets"].data_ptr()), p.B, None, ctypes.c_void_p(bufs.unique_rows.data_ptr()),
@@ -66,6 +71,9 @@ def test_static_workspace_matches_caller_workspace(tbe):
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == tbe.TBE_OK, f"call {call}: {tbe.load_library().tbe_status_string(rc)}"
         torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.memory_allocated() == used_before
+            assert torch.cuda.mem_get_info()[0] == free_before
         assert int(status.item()) == 0
         got = _outputs(bufs, p.N)
         assert got["U"] == ref["U"]
