@@ -150,6 +150,15 @@ int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* i
                      const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
                      int32_t* dev_status, void* stream, int32_t path);
 
+/* The forward with 32-bit ids and offsets (indices: device int32 [N];
+ * offsets: device int32 [T*B + 1]; everything else as tbe_forward_path).
+ * Half the index traffic of the int64 layout ([FBT] "A lookup table that is
+ * most of the model": the jagged indices / offsets pair); results are
+ * identical to tbe_forward_path on the same values. */
+int tbe_forward_i32(const tbe_plan* plan, const void* weights, const int32_t* indices, int64_t N,
+                    const int32_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                    int32_t* dev_status, void* stream, int32_t path);
+
 /* Per-bag id histogram of the single table of a histogram-eligible plan, the
  * count matrix the histogram path multiplies by the table:
  * counts[b * rows_0 + r] = #{i in bag(0, b) : id_i = r}  (device int32
@@ -189,6 +198,14 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
                  int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions,
                  float* row_grads, int64_t row_grads_capacity, int64_t* unique_count,
                  void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* The backward with 32-bit ids and offsets (int32 [N] and [T*B + 1]);
+ * everything else, and every result, as tbe_backward. */
+int tbe_backward_i32(const tbe_plan* plan, const float* grad_out, const int32_t* indices, int64_t N,
+                     const int32_t* offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
+                     int32_t* run_starts, int32_t* sorted_positions, float* row_grads, int64_t row_grads_capacity,
+                     int64_t* unique_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream);
 
 /*
  * Backward without a caller-provided workspace (the page has no counterpart;

@@ -31,6 +31,7 @@ EXPORTED = [
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
     "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest", "tbe_backward_update",
+    "tbe_forward_i32", "tbe_backward_i32",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -104,6 +105,10 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_status_string.argtypes = [i32]
     lib.tbe_version.restype = ctypes.c_char_p
     lib.tbe_version.argtypes = []
+    lib.tbe_forward_i32.restype = ctypes.c_int
+    lib.tbe_forward_i32.argtypes = [P, P, P, i64, P, i32, P, P, P, P, i32]
+    lib.tbe_backward_i32.restype = ctypes.c_int
+    lib.tbe_backward_i32.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, sz, P, P]
     lib.tbe_backward_update.restype = ctypes.c_int
     lib.tbe_backward_update.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, P, i64, P, i32, P, P, P, P, P, P, sz,
                                         P, P]
@@ -121,6 +126,17 @@ def _check(rc: int, what: str):
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _is_i32(indices, offsets):
+    """True for int32 ids and offsets (the *_i32 entry points); both arrays
+    must have the same width."""
+    import torch
+
+    a, b = indices.dtype == torch.int32, offsets.dtype == torch.int32
+    if a != b:
+        raise TBEError("indices and offsets must both be int64 or both int32")
+    return a
 
 
 def _stream(stream=None):
@@ -197,8 +213,9 @@ def tbe_forward(plan: Plan, weights, indices, offsets, B: int, per_sample_weight
     if out is None:
         out = torch.empty((B, plan.sumD), dtype=_out_torch_dtype(plan.out_dtype), device=indices.device)
     N = int(indices.numel())
-    rc = lib.tbe_forward_path(plan.handle, _ptr(weights), _ptr(indices), N, _ptr(offsets), int(B),
-                              _ptr(per_sample_weights), _ptr(out), _ptr(dev_status), _stream(stream), int(path))
+    fn = lib.tbe_forward_i32 if _is_i32(indices, offsets) else lib.tbe_forward_path
+    rc = fn(plan.handle, _ptr(weights), _ptr(indices), N, _ptr(offsets), int(B), _ptr(per_sample_weights), _ptr(out),
+            _ptr(dev_status), _stream(stream), int(path))
     _check(rc, "tbe_forward")
     return out
 
@@ -251,7 +268,8 @@ def tbe_backward(plan: Plan, grad_out, indices, offsets, B: int, per_sample_weig
     N = int(indices.numel())
     if bufs is None:
         bufs = BackwardBuffers(plan, B, N, device=indices.device)
-    rc = lib.tbe_backward(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
+    fn = lib.tbe_backward_i32 if _is_i32(indices, offsets) else lib.tbe_backward
+    rc = fn(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
                           _ptr(per_sample_weights), _ptr(bufs.unique_rows),
                           _ptr(bufs.run_starts) if want_run_starts else None,
                           _ptr(bufs.sorted_positions) if want_sorted_positions else None,

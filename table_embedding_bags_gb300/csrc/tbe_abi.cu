@@ -323,8 +323,7 @@ void tbe_plan_destroy(tbe_plan* plan) {
 // forward
 // ---------------------------------------------------------------------------
 
-static int check_common(const tbe_plan* plan, const int64_t* indices, int64_t N, const int64_t* offsets,
-                        int32_t B) {
+static int check_common(const tbe_plan* plan, const void* indices, int64_t N, const void* offsets, int32_t B) {
   if (!plan) return TBE_ERR_INVALID_ARG;
   if (B < 0 || N < 0 || N >= (int64_t(1) << 30)) return TBE_ERR_INVALID_ARG;
   if ((int64_t)plan->T * B >= (int64_t(1) << 31)) return TBE_ERR_UNSUPPORTED;
@@ -347,10 +346,11 @@ static bool hist_eligible(const tbe_plan* plan, const float* psw) {
   return plan->hist_ok && (psw == nullptr || !plan->hmeta[0].weighted);
 }
 
-int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
-                     const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
-                     int32_t* dev_status, void* stream, int32_t path) {
-  int st = check_common(plan, indices, N, offsets, B);
+// Shared by the int64 and int32 forward entry points.
+static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indices, int64_t N, IdxPtr offsets,
+                        int32_t B, const float* per_sample_weights, void* out, int32_t* dev_status, void* stream,
+                        int32_t path) {
+  int st = check_common(plan, indices.p, N, offsets.p, B);
   if (st != TBE_OK) return st;
   if (path < TBE_PATH_AUTO || path > TBE_PATH_HISTOGRAM) return TBE_ERR_INVALID_ARG;
   if ((int64_t)plan->T * B == 0) return TBE_OK;
@@ -386,6 +386,20 @@ int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* i
   return st;
 }
 
+int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
+                     const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                     int32_t* dev_status, void* stream, int32_t path) {
+  return forward_call(plan, weights, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B, per_sample_weights, out,
+                      dev_status, stream, path);
+}
+
+int tbe_forward_i32(const tbe_plan* plan, const void* weights, const int32_t* indices, int64_t N,
+                    const int32_t* offsets, int32_t B, const float* per_sample_weights, void* out,
+                    int32_t* dev_status, void* stream, int32_t path) {
+  return forward_call(plan, weights, IdxPtr{indices, 1}, N, IdxPtr{offsets, 1}, B, per_sample_weights, out,
+                      dev_status, stream, path);
+}
+
 int tbe_forward(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
                 const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
                 int32_t* dev_status, void* stream) {
@@ -403,8 +417,8 @@ int tbe_histogram_counts(const tbe_plan* plan, const int64_t* indices, int64_t N
   FwdArgs a;
   std::memset(&a, 0, sizeof(a));
   a.meta = plan->dmeta;
-  a.indices = indices;
-  a.offsets = offsets;
+  a.indices = IdxPtr{indices, 0};
+  a.offsets = IdxPtr{offsets, 0};
   a.status = dev_status;
   a.T = plan->T;
   a.B = B;
@@ -424,13 +438,13 @@ size_t tbe_backward_workspace_bytes(const tbe_plan* plan, int32_t B, int64_t N) 
 
 // Shared by tbe_backward and tbe_backward_update: checks and launches the
 // backward; `opt` (may be null) fuses the exact optimizer into the reducer.
-static int backward_call(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
-                         const int64_t* offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
+static int backward_call(const tbe_plan* plan, const float* grad_out, IdxPtr indices, int64_t N,
+                         IdxPtr offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
                          int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
                          int64_t row_grads_capacity, int64_t* unique_count, void* workspace, size_t workspace_bytes,
                          int32_t* dev_status, void* stream, const tbe_optimizer* opt, void* weights,
                          float* momentum) {
-  int st = check_common(plan, indices, N, offsets, B);
+  int st = check_common(plan, indices.p, N, offsets.p, B);
   if (st != TBE_OK) return st;
   if (!unique_count || row_grads_capacity < 0) return TBE_ERR_INVALID_ARG;
   if (N > 0 && (!unique_rows || !grad_out || (!opt && !row_grads && row_grads_capacity > 0)))
@@ -476,9 +490,19 @@ int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* ind
                  int64_t* unique_rows, int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
                  int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
                  size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  return backward_call(plan, grad_out, indices, N, offsets, B, per_sample_weights, unique_rows, run_starts,
-                       sorted_positions, row_grads, row_grads_capacity, unique_count, workspace, workspace_bytes,
-                       dev_status, stream, nullptr, nullptr, nullptr);
+  return backward_call(plan, grad_out, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B, per_sample_weights,
+                       unique_rows, run_starts, sorted_positions, row_grads, row_grads_capacity, unique_count,
+                       workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, nullptr);
+}
+
+int tbe_backward_i32(const tbe_plan* plan, const float* grad_out, const int32_t* indices, int64_t N,
+                     const int32_t* offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
+                     int32_t* run_starts, int32_t* sorted_positions, float* row_grads, int64_t row_grads_capacity,
+                     int64_t* unique_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                     void* stream) {
+  return backward_call(plan, grad_out, IdxPtr{indices, 1}, N, IdxPtr{offsets, 1}, B, per_sample_weights,
+                       unique_rows, run_starts, sorted_positions, row_grads, row_grads_capacity, unique_count,
+                       workspace, workspace_bytes, dev_status, stream, nullptr, nullptr, nullptr);
 }
 
 // Optimizer arguments valid on the host (kind, finite rate, eps >= 0).
@@ -496,9 +520,9 @@ int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* we
   if (plan->maxD > 128) return TBE_ERR_UNSUPPORTED;  // a row gradient is one quad per lane of one warp
   if (N > 0 && (!weights || (opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum))) return TBE_ERR_INVALID_ARG;
   if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
-  return backward_call(plan, grad_out, indices, N, offsets, B, per_sample_weights, unique_rows, run_starts,
-                       sorted_positions, nullptr, 0, unique_count, workspace, workspace_bytes, dev_status, stream,
-                       opt, weights, momentum);
+  return backward_call(plan, grad_out, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B, per_sample_weights,
+                       unique_rows, run_starts, sorted_positions, nullptr, 0, unique_count, workspace,
+                       workspace_bytes, dev_status, stream, opt, weights, momentum);
 }
 
 int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,

@@ -277,8 +277,8 @@ T* at(void* ws, size_t off) {
 // 1. linearize + digit histograms
 // ---------------------------------------------------------------------------
 struct LinArgs {
-  const int64_t* indices;
-  const int64_t* offsets;
+  IdxPtr indices;
+  IdxPtr offsets;
   const TableMeta* meta;
   uint32_t* keys;
   int32_t* bag_of;
@@ -298,11 +298,10 @@ struct LinArgs {
 };
 
 // largest g in [lo, hi] with offsets[g] <= pos (global memory)
-__device__ __forceinline__ int32_t bag_search_global(const int64_t* offsets, int32_t lo, int32_t hi,
-                                                     int64_t pos) {
+__device__ __forceinline__ int32_t bag_search_global(const IdxPtr& offsets, int32_t lo, int32_t hi, int64_t pos) {
   while (lo < hi) {
     int32_t mid = lo + ((hi - lo + 1) >> 1);
-    if (__ldg(offsets + mid) <= pos) lo = mid; else hi = mid - 1;
+    if (offsets.ldg(mid) <= pos) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -311,12 +310,12 @@ __device__ __forceinline__ int32_t bag_search_global(const int64_t* offsets, int
 // 32-ary search: each round the lanes probe 32 evenly spaced bags and keep
 // the sub-range after the last probe that is <= pos (3 rounds for 16K bags).
 // Broken (non-monotone) offsets still give an index inside [0, nb).
-__device__ __forceinline__ int32_t bag_search_warp(const int64_t* offsets, int32_t nb, int64_t pos, int lane) {
+__device__ __forceinline__ int32_t bag_search_warp(const IdxPtr& offsets, int32_t nb, int64_t pos, int lane) {
   int32_t lo = 0, hi = nb - 1;
   while (hi > lo) {
     const int32_t step = (hi - lo + 32) / 32;  // ceil((hi - lo + 1) / 32)
     const int32_t cand = lo + lane * step;
-    const bool ok = cand <= hi && __ldg(offsets + cand) <= pos;
+    const bool ok = cand <= hi && offsets.ldg(cand) <= pos;
     const unsigned m = __ballot_sync(kFull, ok);
     if (m == 0) break;  // pos precedes every probe: lo
     const int last = 31 - __clz(m);
@@ -355,7 +354,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
 #pragma unroll
   for (int q = 0; q < kIPT; ++q) {
     const int64_t i = p0 + q * kLinThreads + tid;
-    id[q] = i < p1 ? ld_stream_i64(a.indices + i) : 0;
+    id[q] = i < p1 ? a.indices.stream(i) : 0;
   }
   if (tid < 64) {  // warp 0 finds the bag of p0, warp 1 the bag of p1 - 1
     const int32_t g = bag_search_warp(a.offsets, nb, tid < 32 ? p0 : p1 - 1, lane);
@@ -369,7 +368,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   const int32_t t_first = g0 / max(a.B, 1);
   const bool staged = ng <= kLinOffs;
   if (staged)
-    for (int k = tid; k < ng; k += kLinThreads) s_off[k] = __ldg(a.offsets + g0 + k);
+    for (int k = tid; k < ng; k += kLinThreads) s_off[k] = a.offsets.ldg(g0 + k);
   __syncthreads();
   int bad = 0, invalid = 0;
 #pragma unroll
@@ -416,7 +415,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   // offsets must start at 0, never decrease and end at N
   const int64_t gstride = (int64_t)gridDim.x * kLinThreads;
   for (int64_t g = (int64_t)blockIdx.x * kLinThreads + tid; g < nb; g += gstride) {
-    const int64_t o0 = __ldg(a.offsets + g), o1 = __ldg(a.offsets + g + 1);
+    const int64_t o0 = a.offsets.ldg(g), o1 = a.offsets.ldg(g + 1);
     if (o1 < o0 || (g == 0 && o0 != 0) || (g == nb - 1 && o1 != a.N)) bad |= 2;
   }
   if (bad & 1) report(a.status, TBE_DEV_BAD_INDEX);
@@ -644,7 +643,7 @@ struct SegSortArgs {
   int32_t* vals_out;
   const uint32_t* hist;     // [T][2][kSegBk] digit counts per table
   const uint32_t* inv;      // [T] ids outside their table
-  const int64_t* offsets;
+  IdxPtr offsets;
   const TableMeta* meta;
   uint32_t* lookback;       // [tiles][kSegBk] of this pass
   uint32_t* tile_counter;
@@ -703,7 +702,7 @@ __global__ void __launch_bounds__(kSortThreads, 2) seg_sort_pass_kernel(const Se
   for (int k = tid; k < kSegBk; k += kSortThreads) s_cnt[k] = 0;
   // table ranges, clamped so that broken offsets still give ranges inside [0, N)
   if (tid <= a.T) {
-    int64_t P = __ldg(a.offsets + (int64_t)tid * a.B);
+    int64_t P = a.offsets.ldg((int64_t)tid * a.B);
     s_P[tid] = min(max(P, (int64_t)0), (int64_t)a.N);
   }
   wait_predecessor();

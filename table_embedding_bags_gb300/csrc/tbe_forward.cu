@@ -59,7 +59,7 @@ __device__ __forceinline__ void load_window(const FwdArgs& a, const TableMeta& m
 #pragma unroll
   for (int k = 0; k < kIdsPerLane; ++k) {  // the whole window in one request
     const int idx = k * lpr + sub;
-    const int64_t raw = idx < nwin ? ld_stream_i64(a.indices + base + idx) : 0;
+    const int64_t raw = idx < nwin ? a.indices.stream(base + idx) : 0;
     iw.id[k] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
     iw.w[k] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
   }
@@ -207,8 +207,8 @@ __device__ __forceinline__ Task locate_task(const FwdArgs& a, const int32_t* s_p
 
 __device__ __forceinline__ void bag_bounds(const FwdArgs& a, const Task& k, int64_t& start, int64_t& end) {
   const int64_t g = (int64_t)k.t * a.B + k.b;
-  start = ld_stream_i64(a.offsets + g);
-  end = ld_stream_i64(a.offsets + g + 1);
+  start = a.offsets.stream(g);
+  end = a.offsets.stream(g + 1);
 }
 
 // Offsets must start at 0, never decrease and end at N; a broken bag is
@@ -350,7 +350,7 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
 #pragma unroll
     for (int k = 0; k < kIdsPerLane; ++k) {  // the window's ids, one coalesced request
       const int idx = k * lpr + sub;
-      const int64_t raw = idx < nwin ? ld_stream_i64(a.indices + base + idx) : 0;
+      const int64_t raw = idx < nwin ? a.indices.stream(base + idx) : 0;
       ids[idx] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
       if (WT) wts[idx] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
     }
@@ -630,8 +630,8 @@ __device__ __forceinline__ void stream_bounds(const FwdArgs& a, const StreamTask
   st = en = 0;
   if (lane < k.nb) {
     const int64_t g = (int64_t)k.t * a.B + k.b0 + lane;
-    st = ld_stream_i64(a.offsets + g);
-    en = ld_stream_i64(a.offsets + g + 1);
+    st = a.offsets.stream(g);
+    en = a.offsets.stream(g + 1);
   }
 }
 
@@ -709,7 +709,7 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
         const int32_t lk = __shfl_sync(kFull, len, kb);
         iu[u] = __shfl_sync(kFull, st, kb) + r;
         vu[u] = q < nwin && r < lk;
-        raw[u] = vu[u] ? ld_stream_i64(a.indices + iu[u]) : 0;
+        raw[u] = vu[u] ? a.indices.stream(iu[u]) : 0;
       }
       float wv[4];
       if (WT) {
@@ -842,8 +842,8 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
     for (int q = 0; q < per; ++q) {
       const int t = tid * per + q;
       if (t < a.T) {
-        const int64_t lo = min(max(__ldg(a.offsets + (int64_t)t * a.B), (int64_t)0), a.N);
-        const int64_t hi = min(max(__ldg(a.offsets + (int64_t)(t + 1) * a.B), (int64_t)0), a.N);
+        const int64_t lo = min(max(a.offsets.ldg((int64_t)t * a.B), (int64_t)0), a.N);
+        const int64_t hi = min(max(a.offsets.ldg((int64_t)(t + 1) * a.B), (int64_t)0), a.N);
         const int64_t n = hi - lo;
         const int bpt = n > 0 ? (int)min((int64_t)32, max((int64_t)1, (per_task * a.B + n - 1) / n)) : 32;
         s_bpt[t] = (uint8_t)bpt;

@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
     if (tid < kM / 32) over[tid] = 0;
     // bag bounds (feature-major offsets of table 0): must start at 0, never
     // decrease and end at N; a broken tile is reported and pooled as empty
-    for (int m = tid; m <= nbag; m += kThreads) off[m] = ld_stream_i64(a.offsets + b0 + m);
+    for (int m = tid; m <= nbag; m += kThreads) off[m] = a.offsets.stream(b0 + m);
     __syncthreads();
     {
       int bad = off[0] < 0 || off[nbag] > a.N || (b0 == 0 && off[0] != 0) || (b0 + nbag == a.B && off[nbag] != a.N);
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int64_t p = pb + u * kThreads + tid;
-        id[u] = p < p1 ? ld_stream_i64(a.indices + p) : -1;
+        id[u] = p < p1 ? a.indices.stream(p) : -1;
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {

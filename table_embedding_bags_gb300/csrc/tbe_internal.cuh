@@ -91,6 +91,28 @@ __device__ __forceinline__ int64_t ld_stream_i64(const int64_t* p) {
   return v;
 }
 
+// An index or offset array: int64 (the default entry points) or int32 (the
+// *_i32 entry points).  The flag is the same for a whole launch.
+struct IdxPtr {
+  const void* p;
+  int32_t i32;
+  // read once, not kept in L1
+  __device__ __forceinline__ int64_t stream(int64_t i) const {
+    if (i32) {
+      int32_t v;
+      asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(static_cast<const int32_t*>(p) + i));
+      return v;
+    }
+    int64_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(v) : "l"(static_cast<const int64_t*>(p) + i));
+    return v;
+  }
+  // read-only path (cached)
+  __device__ __forceinline__ int64_t ldg(int64_t i) const {
+    return i32 ? (int64_t)__ldg(static_cast<const int32_t*>(p) + i) : __ldg(static_cast<const int64_t*>(p) + i);
+  }
+};
+
 __device__ __forceinline__ float ld_stream_f32(const float* p) {
   float v;
   asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
@@ -356,8 +378,8 @@ __device__ __forceinline__ float adagrad_step(float lr, float eps, float m_old, 
 struct FwdArgs {
   const uint8_t* weights;
   const TableMeta* meta;
-  const int64_t* indices;
-  const int64_t* offsets;
+  IdxPtr indices;
+  IdxPtr offsets;
   const float* psw;
   void* out;
   int32_t* status;
@@ -376,8 +398,8 @@ int launch_forward_histogram(const Plan& p, const FwdArgs& a, int32_t* counts_ou
 struct BwdArgs {
   const float* grad_out;
   const TableMeta* meta;
-  const int64_t* indices;
-  const int64_t* offsets;
+  IdxPtr indices;
+  IdxPtr offsets;
   const float* psw;
   int64_t* unique_rows;
   int32_t* run_starts;
