@@ -140,11 +140,14 @@ int tbe_forward(const tbe_plan* plan, const void* weights, const int64_t* indice
                 const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
                 int32_t* dev_status, void* stream);
 
-/* Forward with an explicit path (TBE_PATH_*).  The histogram path needs
- * T == 1, an fp16 table of at most TBE_HIST_MAX_ROWS rows with D a multiple
- * of 16 and at most 256, and no per-sample weights; otherwise
- * TBE_ERR_UNSUPPORTED.  TBE_PATH_AUTO additionally requires the mean bag
- * length N / B to reach the tuned threshold. */
+/* Forward with an explicit path (TBE_PATH_*).  The histogram path ([FBT]
+ * "The forward: a general gather and one clever special case": pooled sums
+ * as per-bag counts times the table on the tensor cores) needs every table
+ * of the plan to be fp16 or bf16 with 1..TBE_HIST_MAX_ROWS rows and D a
+ * multiple of 16 up to 256; otherwise TBE_ERR_UNSUPPORTED.  It takes all T
+ * tables in one launch, and per-sample weights on weighted tables (their
+ * "counts" are fp32 sums of the weights).  TBE_PATH_AUTO additionally
+ * requires the mean bag length N / (T * B) to reach the tuned threshold. */
 #define TBE_HIST_MAX_ROWS 64
 int tbe_forward_path(const tbe_plan* plan, const void* weights, const int64_t* indices, int64_t N,
                      const int64_t* offsets, int32_t B, const float* per_sample_weights, void* out,
@@ -159,10 +162,12 @@ int tbe_forward_i32(const tbe_plan* plan, const void* weights, const int32_t* in
                     const int32_t* offsets, int32_t B, const float* per_sample_weights, void* out,
                     int32_t* dev_status, void* stream, int32_t path);
 
-/* Per-bag id histogram of the single table of a histogram-eligible plan, the
- * count matrix the histogram path multiplies by the table:
- * counts[b * rows_0 + r] = #{i in bag(0, b) : id_i = r}  (device int32
- * [B, rows_0]).  Produced by the same kernel code as the histogram forward. */
+/* Per-bag id histograms of every table of a histogram-eligible plan, the
+ * count matrices the histogram path multiplies by the tables (device int32,
+ * caller-owned, B * table_row_base[T] entries):
+ *   counts[table_row_base[t] * B + b * rows_t + r] = #{i in bag(t, b) : id_i = r}.
+ * Per-sample weights play no part.  Produced by the same kernel code as the
+ * histogram forward. */
 int tbe_histogram_counts(const tbe_plan* plan, const int64_t* indices, int64_t N,
                          const int64_t* offsets, int32_t B, int32_t* counts, int32_t* dev_status,
                          void* stream);
@@ -325,8 +330,9 @@ int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* we
  *                        many as fit; 4 with fwd_unroll 4 selects a build
  *                        of the kernel with a smaller register budget)
  *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
- *                        N / B reaches this; 0 (default) = the measured gate:
- *                        16 for tables of at most 32 rows, 32 above
+ *                        N / (T * B) reaches this; 0 (default) = the
+ *                        measured gate: 16 when no table has more than 32
+ *                        rows, 32 above
  *   short_item_lookups : lookups per work item of the short-run tier (runs
  *                        are grouped by 32 and cut into parts of about this
  *                        many lookups; raised to long_run_threshold if lower)

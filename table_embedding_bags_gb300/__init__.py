@@ -223,14 +223,16 @@ def tbe_forward(plan: Plan, weights, indices, offsets, B: int, per_sample_weight
 def tbe_histogram_counts(plan: Plan, indices, offsets, B: int, counts=None, dev_status=None, stream=None):
     import torch
 
+    """Per-bag id histograms of every table: a list of int32 [B, rows_t]
+    views of one buffer of B * total_rows counts (``counts`` if given)."""
     lib = load_library()
-    rows = int(plan.table_row_base[1] - plan.table_row_base[0])
+    base = plan.table_row_base
     if counts is None:
-        counts = torch.empty((B, rows), dtype=torch.int32, device=indices.device)
+        counts = torch.empty(int(B) * int(base[plan.T]), dtype=torch.int32, device=indices.device)
     rc = lib.tbe_histogram_counts(plan.handle, _ptr(indices), int(indices.numel()), _ptr(offsets), int(B),
                                   _ptr(counts), _ptr(dev_status), _stream(stream))
     _check(rc, "tbe_histogram_counts")
-    return counts
+    return [counts[int(base[t]) * B:int(base[t + 1]) * B].view(B, int(base[t + 1] - base[t])) for t in range(plan.T)]
 
 
 def tbe_backward_workspace_bytes(plan: Plan, B: int, N: int) -> int:

@@ -299,8 +299,14 @@ int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, 
     if (p->hmeta[t].D != p->hmeta[0].D || p->hmeta[t].dtype != p->hmeta[0].dtype ||
         p->hmeta[t].weighted != p->hmeta[0].weighted)
       p->uniform = 0;
-  p->hist_ok = (T == 1 && L->weights_dtype[0] == TBE_F16 && p->hmeta[0].rows >= 1 &&
-                p->hmeta[0].rows <= TBE_HIST_MAX_ROWS && p->hmeta[0].D % 16 == 0 && p->hmeta[0].D <= 256);
+  // histogram path: every table small enough for one MMA tile, fp16 or bf16
+  p->hist_ok = T >= 1;
+  for (int32_t t = 0; t < T; ++t) {
+    const TableMeta& m = p->hmeta[t];
+    if (!(m.dtype == TBE_F16 || m.dtype == TBE_BF16) || m.rows < 1 || m.rows > TBE_HIST_MAX_ROWS ||
+        m.D % 16 != 0 || m.D > 256)
+      p->hist_ok = 0;
+  }
   cudaGetDevice(&p->device);
   p->dmeta = reinterpret_cast<const TableMeta*>(dev_meta);
   if (cudaMemcpyAsync(dev_meta, p->hmeta, sizeof(TableMeta) * (T + 1), cudaMemcpyHostToDevice,
@@ -339,12 +345,12 @@ static int check_common(const tbe_plan* plan, const void* indices, int64_t N, co
 // Mean bag length from which TBE_PATH_AUTO takes the histogram path.
 static int64_t hist_gate(const tbe_plan& plan) {
   if (g_tuning.hist_min_mean_bag > 0) return g_tuning.hist_min_mean_bag;
-  return plan.hmeta[0].rows <= 32 ? 16 : 32;
+  int32_t max_rows = 0;
+  for (int32_t t = 0; t < plan.T; ++t) max_rows = std::max(max_rows, plan.hmeta[t].rows);
+  return max_rows <= 32 ? 16 : 32;
 }
 
-static bool hist_eligible(const tbe_plan* plan, const float* psw) {
-  return plan->hist_ok && (psw == nullptr || !plan->hmeta[0].weighted);
-}
+static bool hist_eligible(const tbe_plan* plan) { return plan->hist_ok; }
 
 // Shared by the int64 and int32 forward entry points.
 static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indices, int64_t N, IdxPtr offsets,
@@ -374,11 +380,10 @@ static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indice
   a.balance = plan->uniform ? 0 : 1;
   bool hist = false;
   if (path == TBE_PATH_HISTOGRAM) {
-    if (!hist_eligible(plan, per_sample_weights)) return TBE_ERR_UNSUPPORTED;
+    if (!hist_eligible(plan)) return TBE_ERR_UNSUPPORTED;
     hist = true;
   } else if (path == TBE_PATH_AUTO) {
-    hist = hist_eligible(plan, per_sample_weights) &&
-           N >= (int64_t)hist_gate(*plan) * (int64_t)B;
+    hist = hist_eligible(plan) && N >= hist_gate(*plan) * (int64_t)plan->T * B;
   }
   trace_begin(s);
   st = hist ? launch_forward_histogram(*plan, a, nullptr, s) : launch_forward_gather(*plan, a, s);

@@ -5,25 +5,42 @@
 // threshold moved from 32 to 256", section "The forward: a general gather and
 // one clever special case": a pooled sum is a count-weighted sum of table
 // rows, so for a table small enough to sit in one tile the pooled outputs of
-// a group of bags are the matrix product counts[bags, rows] x table[rows, D];
-// counts are exact in fp16 (every integer up to 2048 is an fp16 value).
+// a group of bags are the matrix product counts[bags, rows] x table[rows, D].
+// The page's kernel takes one unweighted fp16 table; this one takes every
+// table of a plan whose tables are all small (at most 64 rows, D a multiple
+// of 16 up to 256, fp16 or bf16), weighted or not, in one launch.
 //
-// Design (sm_103a), one CTA of 256 threads per tile of 128 bags (persistent):
-//   1. H2: the tile's ids are one contiguous range of `indices`; all threads
-//      stream it with coalesced loads and add each id to its bag's row in a
-//      shared-memory int32 histogram (the bag of a position is found in the
-//      tile's 129 offsets staged in shared memory).
-//   2. The counts are written as an fp16 A tile [128 x K] and the table (once
-//      per CTA) as an fp16 B tile [K x D] in the canonical K-major layout
-//      without swizzle (8 x 16-byte core matrices; SBO = distance between
-//      8-row groups, LBO = distance between core matrices along K).
-//   3. H3: one thread issues K/16 tcgen05.mma.cta_group::1.kind::f16
-//      (M = 128, N = D, fp32 accumulate in TMEM) and commits them to an
-//      mbarrier; every wait on it is bounded.
+// Design (sm_103a), one CTA of 256 threads per tile of 128 bags of one table;
+// the tiles are ordered table-major and each persistent CTA takes one
+// contiguous range of them, so it loads a table into shared memory (the B
+// operand, K-major) only when its range crosses into the next table.
+//   1. Histogram.  Unweighted: all threads stream the tile's ids (one
+//      contiguous range of `indices`) with coalesced loads and add 1 to the
+//      bag's row in a shared-memory int32 histogram.  Weighted: the "count" of
+//      (bag, row) is the sum of the per-sample weights of the bag's lookups of
+//      that row, in fp32; a warp owns a bag and reads it 32 lookups at a time,
+//      lanes holding the same row are summed in lane (= position) order by
+//      the lowest of them, which then adds the sum to the cell: the
+//      accumulation order is fixed, so the result does not depend on timing.
+//   2. The A operand, per mode (A and B of one MMA always share a type):
+//      * fp16 table:  counts as fp16, exact up to 2048;
+//      * bf16 table:  counts are exact in bf16 only up to 256, so each count c
+//        is split as lo = c mod 256 and hi = c - lo (a multiple of 256 up to
+//        2048, exact too) and A = [lo | hi] runs two passes over K against
+//        the same B tile;
+//      * weighted:    the fp32 sum s is split into two tf32 terms
+//        s1 = tf32(s), s2 = tf32(s - s1) (|s - s1 - s2| <= 2^-22 |s|),
+//        A = [s1 | s2] and the table is widened to fp32 (exact for fp16 and
+//        bf16 values), multiplied with kind::tf32.
+//      Every product of a count term and a table value is exact in fp32; the
+//      tensor core accumulates them in fp32.
+//   3. One thread issues the MMAs (M = 128, N = D, fp32 accumulate in TMEM)
+//      and commits them to an mbarrier; every wait on it is bounded.
 //   4. Four warp pairs read the accumulator back with tcgen05.ld (each warp
 //      reads its 32-lane TMEM quarter, the pair splits the columns), round
-//      once to the output type and store.  A bag longer than 2048 ids (where
-//      fp16 counts may stop being exact) is recomputed from the int32 counts.
+//      once to the output type and store.  An unweighted bag longer than 2048
+//      ids (where a count may not fit its 16-bit form) is recomputed from the
+//      int32 counts.
 #include <algorithm>
 
 #include "tbe_internal.cuh"
@@ -32,33 +49,42 @@ namespace tbe {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
 constexpr int kM = 128;                // bags per tile (MMA M)
 constexpr int kMaxK = 64;              // table rows, padded to a multiple of 16
-constexpr uint32_t kExactCount = 2048; // largest count every fp16 value can hold exactly
+constexpr uint32_t kExactCount = 2048; // largest count both 16-bit count forms hold exactly
 constexpr int kWaitLimit = 1 << 24;    // mbarrier polls before giving up (TBE_DEV_TIMEOUT)
 
+// What a tile multiplies: the MMA kind and the form of its counts.
+enum HistMode : int { kModeF16 = 0, kModeBF16 = 1, kModeTF32 = 2 };
+
 // Dynamic shared memory of one CTA (offsets from a 1024-byte aligned base).
+//   [0, 64 KB)   unweighted: int32 counts [kM][kMaxK] then the 16-bit A tile
+//                [kM x 2K]; weighted: the tf32 A tile [kM x 2K], whose first K
+//                columns accumulate the fp32 sums before they are split
+//   b_tile       the table, [D x K] 16-bit or fp32, sized for the widest table
 struct HistLayout {
-  uint32_t counts, a_tile, b_tile, off, over, mbar, tmem, total;
-  __host__ __device__ HistLayout(int D) {
-    const int K = kMaxK;
-    counts = 0;                                       // int32 [kM][kMaxK]
-    a_tile = counts + kM * kMaxK * 4;                 // fp16 [kM][K] canonical K-major
-    b_tile = a_tile + kM * K * 2;                     // fp16 [D][K] canonical K-major
-    off = b_tile + ((D * K * 2 + 1023) & ~1023);      // int64 [kM + 1]
-    over = off + (kM + 1) * 8;                        // uint32 [kM / 32]
-    mbar = (over + (kM / 32) * 4 + 7) & ~7u;          // uint64
-    tmem = mbar + 8;                                  // uint32
+  uint32_t counts, a16, b_tile, off, over, stage, mbar, tmem, total;
+  __host__ __device__ HistLayout(int maxD, int b_esz) {
+    counts = 0;
+    a16 = kM * kMaxK * 4;
+    b_tile = 2 * kM * kMaxK * 4;
+    off = b_tile + ((maxD * kMaxK * b_esz + 1023) & ~1023);  // int64 [kM + 1]
+    over = off + (kM + 1) * 8;                                // uint32 [kM / 32]
+    stage = over + (kM / 32) * 4;                             // float [kWarps][32]
+    mbar = (stage + kWarps * 32 * 4 + 7) & ~7u;               // uint64
+    tmem = mbar + 8;                                          // uint32
     total = tmem + 8;
   }
 };
 
-
-// Canonical K-major layout without swizzle: element (row, k) of an operand
-// with `rows` rows sits in core matrix (row / 8, k / 8); core matrices are
-// stored 8-row group first, so SBO = 128 bytes and LBO = (rows / 8) * 128.
-__device__ __forceinline__ int kmajor_index(int row, int k, int rows) {
-  return (((k >> 3) * (rows >> 3) + (row >> 3)) << 6) + ((row & 7) << 3) + (k & 7);
+// Canonical K-major layout without swizzle, in bytes: element (row, k) of an
+// operand with `rows` rows and `esz`-byte elements sits in the 8-row x 16-byte
+// core matrix (row / 8, k * esz / 16); core matrices are stored 8-row group
+// first, so SBO = 128 bytes and LBO = (rows / 8) * 128 bytes.
+__device__ __forceinline__ int kmajor_byte(int row, int k, int rows, int esz) {
+  const int kb = k * esz;
+  return (((kb >> 4) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + (kb & 15);
 }
 
 // tcgen05 shared-memory matrix descriptor (no swizzle, version 1).
@@ -67,12 +93,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3fff) << 32) | (1ull << 46);
 }
 
-// Instruction descriptor of kind::f16: fp16 A and B (both K-major), fp32 D,
-// M = 128, N = n.
-__device__ __forceinline__ uint32_t instr_desc_f16(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kM >> 4) << 24);
+// Instruction descriptor of kind::f16 / kind::tf32: A and B K-major of
+// format fmt (0 = fp16, 1 = bf16, 2 = tf32), fp32 D, M = 128, N = n.
+__device__ __forceinline__ uint32_t instr_desc(int fmt, int n) {
+  return (1u << 4) | ((uint32_t)fmt << 7) | ((uint32_t)fmt << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(kM >> 4) << 24);
 }
 
+// Round to the nearest tf32 value (10 fraction bits, ties to even), as fp32
+// bits with the 13 low fraction bits zero.  Finite inputs only.
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t u = __float_as_uint(x);
+  u += 0xfffu + ((u >> 13) & 1u);
+  return __uint_as_float(u & 0xffffe000u);
+}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -91,6 +125,16 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.u32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -118,122 +162,224 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
 }
 
+// Launch-wide shape of the histogram path.
+struct HistShape {
+  int32_t maxD;   // widest table (sizes the B tile and the TMEM accumulator)
+  int32_t b_esz;  // 4 when some tile may take the weighted (tf32) form, else 2
+  int32_t tpt;    // tiles per table, ceil(B / kM)
+};
+
+// A table element as fp32 (fp16 or bf16 storage).
+__device__ __forceinline__ float table_value(uint16_t bits, int dtype) {
+  return dtype == TBE_F16 ? __half2float(__ushort_as_half(bits)) : __bfloat162float(__ushort_as_bfloat16(bits));
+}
+
+// The tile's table into the B tile: element (n = column d, k = row r) = W[r][d];
+// rows r >= rows (the K padding) are zero.
+__device__ void load_table(unsigned char* b_tile, const uint16_t* table, int rows, int K, int D, int dtype,
+                           int mode, int tid) {
+  for (int e = tid; e < D * K; e += kThreads) {
+    const int r = e / D, d = e - r * D;
+    const uint16_t bits = r < rows ? table[(int64_t)r * D + d] : (uint16_t)0;
+    if (mode == kModeTF32)
+      *reinterpret_cast<float*>(b_tile + kmajor_byte(d, r, D, 4)) = r < rows ? table_value(bits, dtype) : 0.f;
+    else
+      *reinterpret_cast<uint16_t*>(b_tile + kmajor_byte(d, r, D, 2)) = bits;
+  }
+}
+
 template <typename OutT, bool COUNTS_ONLY>
-__global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int32_t* counts_out) {
+__global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, const HistShape h, int32_t* counts_out) {
   extern __shared__ unsigned char smem_raw[];
-  const int D = __ldg(&a.meta[0].D);
-  const HistLayout L(D);
+  const HistLayout L(h.maxD, h.b_esz);
   unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   int32_t* counts = reinterpret_cast<int32_t*>(base + L.counts);
-  __half* a_tile = reinterpret_cast<__half*>(base + L.a_tile);
-  __half* b_tile = reinterpret_cast<__half*>(base + L.b_tile);
+  unsigned char* a32 = base + L.counts;  // the tf32 A tile shares the counts region
+  unsigned char* a16 = base + L.a16;
+  unsigned char* b_tile = base + L.b_tile;
   int64_t* off = reinterpret_cast<int64_t*>(base + L.off);
   uint32_t* over = reinterpret_cast<uint32_t*>(base + L.over);
   uint64_t* mbar = reinterpret_cast<uint64_t*>(base + L.mbar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rows = (int)__ldg(&a.meta[0].rows);
-  const int K = (rows + 15) & ~15;                      // MMA K, padded to 16
-  const uint32_t ncols = D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : 256));  // TMEM columns
-  const int ntiles = (a.B + kM - 1) / kM;
+  float* stage = reinterpret_cast<float*>(base + L.stage) + warp * 32;
+  const uint32_t ncols = h.maxD <= 32 ? 32 : (h.maxD <= 64 ? 64 : (h.maxD <= 128 ? 128 : 256));  // TMEM columns
+  const int64_t ntiles = (int64_t)a.T * h.tpt;
+  const int64_t TB = (int64_t)a.T * a.B;
+  const int64_t tile_begin = ntiles * blockIdx.x / gridDim.x;
+  const int64_t tile_end = ntiles * (blockIdx.x + 1) / gridDim.x;
 
   if (!COUNTS_ONLY) {
     if (warp == 0) tmem_alloc(tmem_slot, ncols);
     if (tid == 0) mbar_init(mbar);
-    // the table as the B operand: element (n = column d, k = row r) = W[r][d]
-    const __half* table = reinterpret_cast<const __half*>(a.weights + __ldg(&a.meta[0].w_off));
-    for (int e = tid; e < D * K; e += kThreads) {
-      const int r = e / D, d = e - r * D;
-      b_tile[kmajor_index(d, r, D)] = r < rows ? table[(int64_t)r * D + d] : __float2half_rn(0.f);
-    }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   }
   __syncthreads();
   const uint32_t tmem = COUNTS_ONLY ? 0u : *tmem_slot;
   uint32_t phase = 0;
+  int cur_t = -1, cur_mode = -1;
 
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int b0 = tile * kM;
+  for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
+    const int t = (int)(tile / h.tpt);
+    const int b0 = (int)(tile - (int64_t)t * h.tpt) * kM;
     const int nbag = min(kM, a.B - b0);
-    for (int e = tid; e < kM * kMaxK / 4; e += kThreads) reinterpret_cast<int4*>(counts)[e] = make_int4(0, 0, 0, 0);
+    const TableMeta m = a.meta[t];
+    const int rows = m.rows, D = m.D;
+    const int K = (rows + 15) & ~15;  // MMA K, padded to 16
+    const bool weighted = !COUNTS_ONLY && a.psw != nullptr && m.weighted;
+    const int mode = weighted ? kModeTF32 : (m.dtype == TBE_F16 ? kModeF16 : kModeBF16);
+    const int64_t g0 = (int64_t)t * a.B + b0;
+
+    if (weighted) {
+      for (int e = tid; e < K * (kM * 4 / 16); e += kThreads) reinterpret_cast<int4*>(a32)[e] = make_int4(0, 0, 0, 0);
+    } else {
+      for (int e = tid; e < kM * kMaxK / 4; e += kThreads) reinterpret_cast<int4*>(counts)[e] = make_int4(0, 0, 0, 0);
+    }
     if (tid < kM / 32) over[tid] = 0;
-    // bag bounds (feature-major offsets of table 0): must start at 0, never
-    // decrease and end at N; a broken tile is reported and pooled as empty
-    for (int m = tid; m <= nbag; m += kThreads) off[m] = a.offsets.stream(b0 + m);
+    for (int q = tid; q <= nbag; q += kThreads) off[q] = a.offsets.stream(g0 + q);
+    if (!COUNTS_ONLY && (t != cur_t || mode != cur_mode)) {
+      load_table(b_tile, reinterpret_cast<const uint16_t*>(a.weights + m.w_off), rows, K, D, m.dtype, mode, tid);
+      cur_t = t;
+      cur_mode = mode;
+    }
     __syncthreads();
     {
-      int bad = off[0] < 0 || off[nbag] > a.N || (b0 == 0 && off[0] != 0) || (b0 + nbag == a.B && off[nbag] != a.N);
-      for (int m = tid; m < nbag; m += kThreads) bad |= off[m + 1] < off[m];
+      // bag bounds: must start at 0, never decrease and end at N; a broken
+      // tile is reported and pooled as empty
+      int bad = off[0] < 0 || off[nbag] > a.N || (g0 == 0 && off[0] != 0) || (g0 + nbag == TB && off[nbag] != a.N);
+      for (int q = tid; q < nbag; q += kThreads) bad |= off[q + 1] < off[q];
       bad = __syncthreads_or(bad);
       if (bad) {
         if (tid == 0) report(a.status, TBE_DEV_BAD_OFFSETS);
-        for (int m = tid; m <= nbag; m += kThreads) off[m] = 0;
+        for (int q = tid; q <= nbag; q += kThreads) off[q] = 0;
       }
       __syncthreads();
     }
-    // H2: histogram of every bag of the tile; a thread's positions only grow,
-    // so its bag index only moves forward
-    const int64_t p0 = off[0], p1 = off[nbag];
+
     bool bad_id = false;
-    int m = 0;
-    {
-      const int64_t p = p0 + tid;
-      int lo = 0, hi = nbag - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= p) lo = mid; else hi = mid - 1;
+    const int64_t p0 = off[0], p1 = off[nbag];
+    if (!weighted) {
+      // counts of every bag of the tile; a thread's positions only grow, so
+      // its bag index only moves forward
+      int q = 0;
+      {
+        const int64_t p = p0 + tid;
+        int lo = 0, hi = nbag - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (off[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        q = lo;
       }
-      m = lo;
-    }
-    constexpr int kU = 16;
-    for (int64_t pb = p0; pb < p1; pb += kThreads * kU) {
-      int64_t id[kU];
+      constexpr int kU = 16;
+      for (int64_t pb = p0; pb < p1; pb += kThreads * kU) {
+        int64_t id[kU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t p = pb + u * kThreads + tid;
-        id[u] = p < p1 ? a.indices.stream(p) : -1;
+        for (int u = 0; u < kU; ++u) {
+          const int64_t p = pb + u * kThreads + tid;
+          id[u] = p < p1 ? a.indices.stream(p) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int64_t p = pb + u * kThreads + tid;
+          if (p >= p1) break;
+          while (q < nbag - 1 && off[q + 1] <= p) ++q;
+          if ((uint64_t)id[u] < (uint64_t)rows) atomicAdd(&counts[q * kMaxK + (int)id[u]], 1);
+          else bad_id = true;
+        }
       }
+      for (int b = tid; b < nbag; b += kThreads)
+        if (off[b + 1] - off[b] > (int64_t)kExactCount) atomicOr(&over[b >> 5], 1u << (b & 31));
+    } else {
+      // sums of per-sample weights: warp per bag, 32 lookups per step in
+      // position order; lanes holding the same row are summed in lane order
+      // by the lowest of them, which alone adds to the cell
+      constexpr int kWU = 4;
+      for (int q = warp; q < nbag; q += kWarps) {
+        const int64_t s = off[q], e = off[q + 1];
+        for (int64_t pb = s; pb < e; pb += 32 * kWU) {
+          int64_t id[kWU];
+          float w[kWU];
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int64_t p = pb + u * kThreads + tid;
-        if (p >= p1) break;
-        while (m < nbag - 1 && off[m + 1] <= p) ++m;
-        if ((uint64_t)id[u] < (uint64_t)rows) atomicAdd(&counts[m * kMaxK + (int)id[u]], 1);
-        else bad_id = true;
+          for (int u = 0; u < kWU; ++u) {
+            const int64_t p = pb + u * 32 + lane;
+            id[u] = p < e ? a.indices.stream(p) : -1;
+            w[u] = p < e ? __ldg(a.psw + p) : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < kWU; ++u) {
+            if (pb + u * 32 >= e) break;  // warp-uniform
+            const bool in = pb + u * 32 + lane < e;
+            const bool ok = in && (uint64_t)id[u] < (uint64_t)rows;
+            bad_id |= in && !ok;
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? (unsigned long long)id[u] : ~0ull);
+            stage[lane] = w[u];
+            __syncwarp();
+            if (ok && __ffs(peers) - 1 == lane) {
+              float sum = 0.f;
+              for (unsigned mm = peers; mm; mm &= mm - 1) sum += stage[__ffs(mm) - 1];
+              *reinterpret_cast<float*>(a32 + kmajor_byte(q, (int)id[u], kM, 4)) += sum;
+            }
+            __syncwarp();
+          }
+        }
       }
     }
     if (bad_id) report(a.status, TBE_DEV_BAD_INDEX);
-    for (int q = tid; q < nbag; q += kThreads)
-      if (off[q + 1] - off[q] > (int64_t)kExactCount) atomicOr(&over[q >> 5], 1u << (q & 31));
     __syncthreads();
 
     if (COUNTS_ONLY) {
+      int32_t* dst = counts_out + m.row_base * (int64_t)a.B + (int64_t)b0 * rows;
       for (int e = tid; e < nbag * rows; e += kThreads) {
         const int q = e / rows, r = e - q * rows;
-        counts_out[(int64_t)(b0 + q) * rows + r] = counts[q * kMaxK + r];
+        dst[e] = counts[q * kMaxK + r];
       }
       __syncthreads();
       continue;
     }
-    // counts -> fp16 A operand [128 x K] (exact up to 2048; longer bags are redone below)
-    for (int e = tid; e < kM * K; e += kThreads) {
-      const int q = e / K, r = e - q * K;
-      const int32_t c = q < nbag ? counts[q * kMaxK + r] : 0;
-      a_tile[kmajor_index(q, r, kM)] = __int2half_rn(min(c, (int32_t)kExactCount));
+
+    // the A operand (see the header: one or two K passes per mode)
+    if (mode == kModeTF32) {
+      for (int e = tid; e < kM * K; e += kThreads) {
+        const int q = e / K, r = e - q * K;
+        float* cell = reinterpret_cast<float*>(a32 + kmajor_byte(q, r, kM, 4));
+        const float s = *cell, s1 = round_tf32(s);
+        *cell = s1;
+        *reinterpret_cast<float*>(a32 + kmajor_byte(q, K + r, kM, 4)) = round_tf32(s - s1);
+      }
+    } else if (mode == kModeF16) {
+      for (int e = tid; e < kM * K; e += kThreads) {
+        const int q = e / K, r = e - q * K;
+        const int32_t c = min(counts[q * kMaxK + r], (int32_t)kExactCount);
+        *reinterpret_cast<__half*>(a16 + kmajor_byte(q, r, kM, 2)) = __int2half_rn(c);
+      }
+    } else {
+      for (int e = tid; e < kM * K; e += kThreads) {
+        const int q = e / K, r = e - q * K;
+        const int32_t c = min(counts[q * kMaxK + r], (int32_t)kExactCount), lo = c & 255;
+        *reinterpret_cast<__nv_bfloat16*>(a16 + kmajor_byte(q, r, kM, 2)) = __float2bfloat16_rn((float)lo);
+        *reinterpret_cast<__nv_bfloat16*>(a16 + kmajor_byte(q, K + r, kM, 2)) = __float2bfloat16_rn((float)(c - lo));
+      }
     }
     // make the generic-proxy shared-memory writes visible to the tensor core
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
     if (tid == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t idesc = instr_desc_f16(D);
-      const uint32_t a_addr = smem_u32(a_tile), b_addr = smem_u32(b_tile);
-      for (int ks = 0; ks < K / 16; ++ks) {
-        // K step ks covers core-matrix columns 2ks and 2ks+1 (LBO apart)
-        const uint64_t ad = smem_desc(a_addr + ks * 2 * (kM / 8) * 128, (kM / 8) * 128, 128);
-        const uint64_t bd = smem_desc(b_addr + ks * 2 * (D / 8) * 128, (D / 8) * 128, 128);
-        mma_f16(tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+      const int esz = mode == kModeTF32 ? 4 : 2;
+      const uint32_t idesc = instr_desc(mode, D);  // the mode values are the descriptor's formats
+      const int a_steps = (mode == kModeF16 ? K : 2 * K) * esz / 32;  // 32 bytes of K per MMA
+      const int b_steps = K * esz / 32;
+      const uint32_t a_addr = smem_u32(mode == kModeTF32 ? a32 : a16), b_addr = smem_u32(b_tile);
+      for (int st = 0; st < a_steps; ++st) {
+        // step st covers core-matrix columns 2st and 2st+1 (LBO apart); the
+        // second pass over K reuses the B steps
+        const int sb = st % b_steps;
+        const uint64_t ad = smem_desc(a_addr + st * 2 * (kM / 8) * 128, (kM / 8) * 128, 128);
+        const uint64_t bd = smem_desc(b_addr + sb * 2 * (D / 8) * 128, (D / 8) * 128, 128);
+        if (mode == kModeTF32) mma_tf32(tmem, ad, bd, idesc, st > 0 ? 1u : 0u);
+        else mma_f16(tmem, ad, bd, idesc, st > 0 ? 1u : 0u);
       }
       mma_commit(mbar);
     }
@@ -249,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
       // split the 32-column groups
       const int q = (warp & 3) * 32 + lane;
       const bool is_over = q < nbag && ((over[q >> 5] >> (q & 31)) & 1u);
-      OutT* orow = reinterpret_cast<OutT*>(a.out) + (int64_t)(b0 + q) * a.sumD + __ldg(&a.meta[0].col_off);
+      OutT* orow = reinterpret_cast<OutT*>(a.out) + (int64_t)(b0 + q) * a.sumD + m.col_off;
       const int ngroups = (D + 31) / 32;
       const int per_warp = (ngroups + 1) / 2;
       const bool vec = a.out_vec_ok;
@@ -258,14 +404,15 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
         if (cg >= ngroups) break;
         float v[32];
         tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(cg * 32), v);
-        if (is_over) {  // exact recount for bags too long for fp16 counts
+        if (is_over) {  // exact recount of an unweighted bag too long for 16-bit counts
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             if (cg * 32 + c < D) {
               float acc = 0.f;
-              for (int r = 0; r < rows; ++r)
-                acc = __fadd_rn(acc, __fmul_rn((float)counts[q * kMaxK + r],
-                                               __half2float(b_tile[kmajor_index(cg * 32 + c, r, D)])));
+              for (int r = 0; r < rows; ++r) {
+                const uint16_t bits = *reinterpret_cast<const uint16_t*>(b_tile + kmajor_byte(cg * 32 + c, r, D, 2));
+                acc = __fadd_rn(acc, __fmul_rn((float)counts[q * kMaxK + r], table_value(bits, m.dtype)));
+              }
               v[c] = acc;
             }
           }
@@ -287,18 +434,17 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, int3
 }
 
 template <typename OutT, bool COUNTS_ONLY>
-int launch_hist(const FwdArgs& a, int32_t* counts, int D, cudaStream_t s) {
-  const size_t smem = HistLayout(D).total + 1024;  // + alignment slack
+int launch_hist(const FwdArgs& a, const HistShape& h, int32_t* counts, cudaStream_t s) {
+  const size_t smem = HistLayout(h.maxD, h.b_esz).total + 1024;  // + alignment slack
   if (cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return TBE_ERR_CUDA;
-  const int ntiles = (a.B + kM - 1) / kM;
-  // CTAs per SM: what shared memory allows, capped so that their TMEM
-  // accumulators (<= 256 columns each) fit the 512 columns of an SM
+  const int64_t ntiles = (int64_t)a.T * h.tpt;
   // CTAs per SM from the kernel's registers and shared memory (the launch
-  // bounds keep it at <= 128 registers, so two fit the register file)
+  // bounds keep it at <= 128 registers, so two fit the register file),
+  // capped so that their TMEM accumulators fit the 512 columns of an SM
   int per_sm = 2;
   {
     cudaFuncAttributes fa;
@@ -311,22 +457,25 @@ int launch_hist(const FwdArgs& a, int32_t* counts, int D, cudaStream_t s) {
       per_sm = std::max(1, std::min(by_regs, by_smem));
     }
   }
-  const int ncols = D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : 256));
+  const int ncols = h.maxD <= 32 ? 32 : (h.maxD <= 64 ? 64 : (h.maxD <= 128 ? 128 : 256));
   if (!COUNTS_ONLY) per_sm = std::min(per_sm, 512 / ncols);
-  const int grid = std::max(1, std::min(ntiles, sm_count() * per_sm));
-  hist_kernel<OutT, COUNTS_ONLY><<<grid, kThreads, smem, s>>>(a, counts);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, (int64_t)sm_count() * per_sm));
+  hist_kernel<OutT, COUNTS_ONLY><<<grid, kThreads, smem, s>>>(a, h, counts);
   return check_launch();
 }
 
 }  // namespace
 
 int launch_forward_histogram(const Plan& p, const FwdArgs& a, int32_t* counts_out, cudaStream_t s) {
-  const int D = p.hmeta[0].D;
-  if (counts_out) return launch_hist<float, true>(a, counts_out, D, s);
+  HistShape h;
+  h.maxD = p.maxD;
+  h.b_esz = (!counts_out && a.psw != nullptr && p.any_weighted) ? 4 : 2;
+  h.tpt = (a.B + kM - 1) / kM;
+  if (counts_out) return launch_hist<float, true>(a, h, counts_out, s);
   switch (p.out_dtype) {
-    case TBE_F32: return launch_hist<float, false>(a, nullptr, D, s);
-    case TBE_F16: return launch_hist<__half, false>(a, nullptr, D, s);
-    default: return launch_hist<__nv_bfloat16, false>(a, nullptr, D, s);
+    case TBE_F32: return launch_hist<float, false>(a, h, nullptr, s);
+    case TBE_F16: return launch_hist<__half, false>(a, h, nullptr, s);
+    default: return launch_hist<__nv_bfloat16, false>(a, h, nullptr, s);
   }
 }
 
