@@ -44,6 +44,8 @@ WORKLOAD_DESC = ("TBE mid-size skewed: T=8 fp16 tables x 100000 rows, D=128, B=2
                  "Poisson(20) (one empty bag per table), ids Zipf(1.05) through a per-table permutation, "
                  "fp16 output, fp32 grad_out; forward + backward (row gradients)")
 N_BATCHES = 4
+INDEX_BYTES = 8  # width of ids and offsets in the byte accounting (--index-bits)
+IDX_NP = {8: np.int64, 4: np.int32}
 DT_NAMES = {0: "f32", 1: "f16", 2: "bf16"}
 OPT_LR, OPT_EPS = 0.01, 1e-8  # exact row-wise Adagrad step timed beside the headline
 FLUSH_BYTES = 256 << 20
@@ -62,6 +64,10 @@ def parse_args():
     ap.add_argument("--B", type=int, default=None, help="batch size override (profiling of smaller cases)")
     ap.add_argument("--only", choices=["both", "fwd", "bwd"], default="both")
     ap.add_argument("--path", choices=["auto", "gather", "histogram"], default="auto")
+    ap.add_argument("--hist-variant", choices=["fp16", "bf16", "weighted", "tables4", "all"], default="fp16",
+                    help="tables of the histogram sweep")
+    ap.add_argument("--index-bits", type=int, choices=[64, 32], default=64,
+                    help="width of ids and offsets (32: the *_i32 entry points)")
     ap.add_argument("--tuning", default=None,
                     help='JSON object of tbe_tuning fields to set first, e.g. \'{"long_run_threshold": 256}\'')
     ap.add_argument("--sweep", choices=["backward", "histogram"], default=None,
@@ -100,10 +106,11 @@ def effective_bytes(p, unique_per_table):
     D = p.D.astype(np.int64)
     w = (p.table_weighted.astype(np.int64) if p.per_sample_weights is not None else np.zeros(p.T, np.int64))
     s_out = ELEM_BYTES[int(p.out_dtype)]
-    offs = (p.T * p.B + 1) * 8
-    fwd = int(np.sum(lens * (D * sw + 8 + 4 * w)) + offs + p.B * int(D.sum()) * s_out)
+    ib = INDEX_BYTES
+    offs = (p.T * p.B + 1) * ib
+    fwd = int(np.sum(lens * (D * sw + ib + 4 * w)) + offs + p.B * int(D.sum()) * s_out)
     U = np.asarray(unique_per_table, np.int64)
-    bwd = int(np.sum(lens * (4 * D + 8 + 4 * w)) + offs + np.sum(U * (8 + 4 * D)))
+    bwd = int(np.sum(lens * (4 * D + ib + 4 * w)) + offs + np.sum(U * (8 + 4 * D)))
     return fwd, bwd
 
 
@@ -122,8 +129,8 @@ def compulsory_bytes(p, unique_per_table):
     D = p.D.astype(np.int64)
     w = (p.table_weighted.astype(np.int64) if p.per_sample_weights is not None else np.zeros(p.T, np.int64))
     U = np.asarray(unique_per_table, np.int64)
-    ids = int(np.sum(lens * (8 + 4 * w)))
-    offs = (p.T * p.B + 1) * 8
+    ids = int(np.sum(lens * (INDEX_BYTES + 4 * w)))
+    offs = (p.T * p.B + 1) * INDEX_BYTES
     sumD = int(D.sum())
     fwd = int(np.sum(U * D * sw)) + ids + offs + p.B * sumD * ELEM_BYTES[int(p.out_dtype)]
     bwd = ids + offs + 4 * p.B * sumD + int(np.sum(U * (8 + 4 * D)))
@@ -150,7 +157,7 @@ def kernel_bytes(p, U_total):
     D = int(p.D[0])
     tb = p.T * p.B
     return {
-        "bwd_linearize": 8 * N + 8 * (tb + 1) + 4 * N + 4 * N,
+        "bwd_linearize": INDEX_BYTES * (N + tb + 1) + 4 * N + 4 * N,
         "bwd_sort_pass": 16 * N,
         "bwd_rle": 4 * N + 12 * U_total,
         "bwd_classify": 4 * U_total,
@@ -286,7 +293,8 @@ def run_profile(args):
     apply_tuning(tbe, args.tuning)
     p = make_config(args.workload, B=args.B, with_grad=args.only != "fwd")
     plan = tbe.Plan.from_problem(p)
-    ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
+    ind = torch.from_numpy(p.indices.astype(IDX_NP[INDEX_BYTES])).cuda()
+    off = torch.from_numpy(p.offsets.astype(IDX_NP[INDEX_BYTES])).cuda()
     psw = None if p.per_sample_weights is None else torch.from_numpy(p.per_sample_weights).cuda()
     path = {"auto": tbe.TBE_PATH_AUTO, "gather": tbe.TBE_PATH_GATHER, "histogram": tbe.TBE_PATH_HISTOGRAM}[args.path]
     w = materialize_weights(p, device="cuda") if args.only != "bwd" else None
@@ -377,34 +385,52 @@ def sweep_backward(args, tbe, torch, flush):
     tbe.set_tuning(**default)
 
 
+HIST_VARIANTS = {  # name: (table dtype, tables, weighted)
+    "fp16": ("fp16", 1, False), "bf16": ("bf16", 1, False), "weighted": ("fp16", 1, True),
+    "tables4": ("fp16", 4, False),
+}
+
+
 def sweep_histogram(args, tbe, torch, flush):
-    """Forward time of the histogram path and of the gather path on one fp16
-    table of `rows` x 128 with bag lengths U{L/2 .. 3L/2} and uniform ids."""
-    from tbe_inputs import DT_F16, DT_F32, make_problem, materialize_weights
+    """Forward time of the histogram path and of the gather path on T tables
+    of `rows` x 128 with bag lengths U{L/2 .. 3L/2} and uniform ids; the
+    variant fixes the table dtype, T and whether lookups carry per-sample
+    weights."""
+    from tbe_inputs import DT_BF16, DT_F16, DT_F32, make_problem, materialize_weights
 
-    for rows in SWEEP_HIST_ROWS:
-        for L in SWEEP_HIST_LEN:
-            B = int(min(262144, max(1024, SWEEP_HIST_LOOKUPS // L)))
-            rng = np.random.default_rng([rows, L])
-            lens = rng.integers(max(1, L // 2), L + L // 2 + 1, size=(1, B))
-            ids = [rng.integers(0, rows, size=int(lens.sum()))]
-            p = make_problem(1, B, rows=[rows], D=[128], weights_dtype=[DT_F16], out_dtype=DT_F32,
-                             lengths=lens, ids=ids, seed=rows * 1000 + L)
-            w = materialize_weights(p, device="cuda")
-            plan = tbe.Plan.from_problem(p)
-            ind, off = torch.from_numpy(p.indices).cuda(), torch.from_numpy(p.offsets).cuda()
-            out = torch.empty((B, 128), dtype=torch.float32, device="cuda")
-            status = torch.zeros(1, dtype=torch.int32, device="cuda")
-            res = {}
-            for path, code in (("histogram", tbe.TBE_PATH_HISTOGRAM), ("gather", tbe.TBE_PATH_GATHER)):
-                def fn(code=code):
-                    tbe.tbe_forward(plan, w, ind, off, B, out=out, dev_status=status, path=code)
+    names = list(HIST_VARIANTS) if args.hist_variant == "all" else [args.hist_variant]
+    for name in names:
+        dt_name, T, weighted = HIST_VARIANTS[name]
+        dt = DT_F16 if dt_name == "fp16" else DT_BF16
+        rows_list = SWEEP_HIST_ROWS if name == "fp16" else [16, 64]
+        for rows in rows_list:
+            for L in SWEEP_HIST_LEN:
+                B = int(min(262144, max(1024, SWEEP_HIST_LOOKUPS // (L * T))))
+                rng = np.random.default_rng([rows, L, T])
+                lens = rng.integers(max(1, L // 2), L + L // 2 + 1, size=(T, B))
+                ids = [rng.integers(0, rows, size=int(lens[t].sum())) for t in range(T)]
+                psw = rng.random(int(lens.sum())).astype(np.float32) if weighted else None
+                p = make_problem(T, B, rows=[rows] * T, D=[128] * T, weights_dtype=[dt] * T, out_dtype=DT_F32,
+                                 lengths=lens, ids=ids, psw=psw, seed=rows * 1000 + L)
+                w = materialize_weights(p, device="cuda")
+                plan = tbe.Plan.from_problem(p)
+                ind = torch.from_numpy(p.indices.astype(IDX_NP[INDEX_BYTES])).cuda()
+                off = torch.from_numpy(p.offsets.astype(IDX_NP[INDEX_BYTES])).cuda()
+                d_psw = torch.from_numpy(psw).cuda() if weighted else None
+                out = torch.empty((B, 128 * T), dtype=torch.float32, device="cuda")
+                status = torch.zeros(1, dtype=torch.int32, device="cuda")
+                res = {}
+                for path, code in (("histogram", tbe.TBE_PATH_HISTOGRAM), ("gather", tbe.TBE_PATH_GATHER)):
+                    def fn(code=code):
+                        tbe.tbe_forward(plan, w, ind, off, B, d_psw, out=out, dev_status=status, path=code)
 
-                res[path] = time_replays(torch, fn, flush, args.steps)[0]
-            assert int(status.item()) == 0, f"device status {int(status.item())}"
-            print(json.dumps(dict(sweep="histogram", rows=rows, mean_bag=L, B=B, N=p.N,
-                                  histogram_us=round(res["histogram"], 2), gather_us=round(res["gather"], 2),
-                                  faster="histogram" if res["histogram"] < res["gather"] else "gather")), flush=True)
+                    res[path] = time_replays(torch, fn, flush, args.steps)[0]
+                assert int(status.item()) == 0, f"device status {int(status.item())}"
+                print(json.dumps(dict(sweep="histogram", variant=name, rows=rows, T=T, mean_bag=L, B=B, N=p.N,
+                                      index_bits=8 * INDEX_BYTES, histogram_us=round(res["histogram"], 2),
+                                      gather_us=round(res["gather"], 2),
+                                      faster="histogram" if res["histogram"] < res["gather"] else "gather")),
+                      flush=True)
 
 
 def run_sweep(args):
@@ -442,7 +468,8 @@ def run_ours(args, world, rank, local):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     dev_in = []
     for p in probs:
-        dev_in.append(dict(indices=torch.from_numpy(p.indices).to(dev), offsets=torch.from_numpy(p.offsets).to(dev),
+        dev_in.append(dict(indices=torch.from_numpy(p.indices.astype(IDX_NP[INDEX_BYTES])).to(dev),
+                           offsets=torch.from_numpy(p.offsets.astype(IDX_NP[INDEX_BYTES])).to(dev),
                            grad=torch.from_numpy(p.grad_out).to(dev),
                            psw=None if p.per_sample_weights is None else torch.from_numpy(p.per_sample_weights).to(dev)))
     flush = L2Flush(dev)
@@ -697,7 +724,8 @@ def run_ours(args, world, rank, local):
                     lookups_per_step=int(np.mean([p.N for p in probs])), index_batches=N_BATCHES,
                     l2="flushed before every step (256 MB write + 256 MB read of another buffer, outside the step events)",
                     table_dtype="/".join(sorted({DT_NAMES[int(d)] for d in p0.weights_dtype})), accumulate="f32",
-                    out_dtype=DT_NAMES[int(p0.out_dtype)], parallelism=f"replicas x{world}"),
+                    out_dtype=DT_NAMES[int(p0.out_dtype)], index_bits=8 * INDEX_BYTES,
+                    parallelism=f"replicas x{world}"),
         roofline=roofline_entry(dom, kb[dom], per_kernel[dom], achieved, peak, peak_kind),
         optimizer=optimizer,
         clocks=clocks,
@@ -790,12 +818,13 @@ def run_e2e(args, tbe, torch, plan, probs, weights, out, bufs, status, dev, flus
     results back (pooled output, unique rows and their row gradients)."""
     host = []
     for p in probs:
-        host.append(dict(indices=torch.from_numpy(p.indices).pin_memory(),
-                         offsets=torch.from_numpy(p.offsets).pin_memory(),
+        host.append(dict(indices=torch.from_numpy(p.indices.astype(IDX_NP[INDEX_BYTES])).pin_memory(),
+                         offsets=torch.from_numpy(p.offsets.astype(IDX_NP[INDEX_BYTES])).pin_memory(),
                          grad=torch.from_numpy(p.grad_out).pin_memory()))
     nmax = max(p.N for p in probs)
-    d_ind = torch.empty(nmax, dtype=torch.int64, device=dev)
-    d_off = torch.empty(probs[0].offsets.shape[0], dtype=torch.int64, device=dev)
+    idt = torch.int32 if INDEX_BYTES == 4 else torch.int64
+    d_ind = torch.empty(nmax, dtype=idt, device=dev)
+    d_off = torch.empty(probs[0].offsets.shape[0], dtype=idt, device=dev)
     d_grad = torch.empty(probs[0].grad_out.shape, dtype=torch.float32, device=dev)
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h_rows = torch.empty(nmax, dtype=torch.int64).pin_memory()
@@ -826,7 +855,7 @@ def run_e2e(args, tbe, torch, plan, probs, weights, out, bufs, status, dev, flus
         t1 = time.perf_counter()
         if k >= args.warmup:
             times.append(t1 - t0)
-            bi = n * 8 + p.offsets.nbytes + p.grad_out.nbytes
+            bi = (n + p.offsets.shape[0]) * INDEX_BYTES + p.grad_out.nbytes
             bo = out.numel() * out.element_size() + h_uc.numel() * 8 + U * 8 + U * D * 4
             bin_ += bi
             bout += bo
@@ -926,7 +955,9 @@ def combine_ranks(tot_s, nbytes, lookups, steps, device):
 
 
 def main():
+    global INDEX_BYTES
     args = parse_args()
+    INDEX_BYTES = args.index_bits // 8
     world, rank, local = dist_env()
     if args.impl == "reference":
         if rank == 0:

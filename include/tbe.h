@@ -303,6 +303,15 @@ int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* we
                         int32_t* sorted_positions, int64_t* unique_count, void* workspace,
                         size_t workspace_bytes, int32_t* dev_status, void* stream);
 
+/* tbe_backward_update with 32-bit ids and offsets (indices: device int32
+ * [N]; offsets: device int32 [T*B + 1]; everything else as
+ * tbe_backward_update); results identical to it on the same values. */
+int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                            const float* grad_out, const int32_t* indices, int64_t N, const int32_t* offsets,
+                            int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                            int32_t* sorted_positions, int64_t* unique_count, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream);
+
 /*
  * Tuning knobs (process-wide; set them before launching work that should
  * use them, not concurrently with launches).

@@ -31,7 +31,7 @@ EXPORTED = [
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
     "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest", "tbe_backward_update",
-    "tbe_forward_i32", "tbe_backward_i32",
+    "tbe_forward_i32", "tbe_backward_i32", "tbe_backward_update_i32",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -110,8 +110,10 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_backward_i32.restype = ctypes.c_int
     lib.tbe_backward_i32.argtypes = [P, P, P, i64, P, i32, P, P, P, P, P, i64, P, P, sz, P, P]
     lib.tbe_backward_update.restype = ctypes.c_int
+    lib.tbe_backward_update_i32.restype = ctypes.c_int
     lib.tbe_backward_update.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, P, i64, P, i32, P, P, P, P, P, P, sz,
                                         P, P]
+    lib.tbe_backward_update_i32.argtypes = lib.tbe_backward_update.argtypes
     lib.tbe_wait_selftest.restype = ctypes.c_int
     lib.tbe_wait_selftest.argtypes = [i32, i32, P, P]
     _lib = lib
@@ -128,15 +130,43 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _is_i32(indices, offsets):
-    """True for int32 ids and offsets (the *_i32 entry points); both arrays
-    must have the same width."""
+def _need(t, dtypes, numel, what, optional=False):
+    """Checks a tensor argument before its pointer crosses the C ABI: a
+    contiguous CUDA tensor of one of ``dtypes`` with at least ``numel``
+    elements (the kernels read or write that many, so a smaller or host
+    buffer would be accessed out of bounds)."""
+    if t is None:
+        if optional:
+            return
+        raise TBEError(f"{what} is required")
+    if t.device.type != "cuda":
+        raise TBEError(f"{what} must be a CUDA tensor (got {t.device})")
+    if t.dtype not in dtypes:
+        raise TBEError(f"{what} has dtype {t.dtype}; expected {' or '.join(str(d) for d in dtypes)}")
+    if not t.is_contiguous():
+        raise TBEError(f"{what} must be contiguous")
+    if t.numel() < numel:
+        raise TBEError(f"{what} has {t.numel()} elements; at least {numel} are read or written")
+
+
+def _is_i32(plan, indices, offsets, B, allow_i32=True):
+    """Checks the id and offset arrays; True for int32 (the *_i32 entry
+    points).  Both arrays must have the same width."""
     import torch
 
-    a, b = indices.dtype == torch.int32, offsets.dtype == torch.int32
-    if a != b:
-        raise TBEError("indices and offsets must both be int64 or both int32")
-    return a
+    widths = (torch.int64, torch.int32) if allow_i32 else (torch.int64,)
+    _need(indices, widths, 0, "indices")
+    _need(offsets, (indices.dtype,), plan.T * int(B) + 1, "offsets")
+    return indices.dtype == torch.int32
+
+
+def _need_weights(plan, weights):
+    import torch
+
+    _need(weights, (torch.uint8, torch.int8, torch.float32, torch.float16, torch.bfloat16), 0, "weights")
+    if weights.numel() * weights.element_size() < plan.weights_bytes:
+        raise TBEError(f"weights holds {weights.numel() * weights.element_size()} bytes; the plan's tables "
+                       f"need {plan.weights_bytes}")
 
 
 def _stream(stream=None):
@@ -167,6 +197,10 @@ class Plan:
         self.out_dtype = int(out_dtype)
         self.sumD = int(self.D_offsets[-1])
         self.D = np.diff(self.D_offsets).astype(np.int64)
+        esz = np.array([{TBE_F32: 4, TBE_F16: 2, TBE_BF16: 2}.get(int(d), 4) for d in self.weights_dtype], np.int64)
+        rows = np.diff(self.table_row_base)
+        self.weights_bytes = int(np.max(self.weights_offsets[:self.T] + rows * self.D * esz)) if self.T else 0
+        self.total_rows = int(self.table_row_base[self.T]) if self.T else 0
         nbytes = lib.tbe_plan_device_bytes(self.T)
         if nbytes == 0:
             raise TBEError("tbe_plan_device_bytes: T out of range")
@@ -213,7 +247,12 @@ def tbe_forward(plan: Plan, weights, indices, offsets, B: int, per_sample_weight
     if out is None:
         out = torch.empty((B, plan.sumD), dtype=_out_torch_dtype(plan.out_dtype), device=indices.device)
     N = int(indices.numel())
-    fn = lib.tbe_forward_i32 if _is_i32(indices, offsets) else lib.tbe_forward_path
+    i32 = _is_i32(plan, indices, offsets, B)
+    _need_weights(plan, weights)
+    _need(per_sample_weights, (torch.float32,), N, "per_sample_weights", optional=True)
+    _need(out, (_out_torch_dtype(plan.out_dtype),), int(B) * plan.sumD, "out")
+    _need(dev_status, (torch.int32,), 1, "dev_status", optional=True)
+    fn = lib.tbe_forward_i32 if i32 else lib.tbe_forward_path
     rc = fn(plan.handle, _ptr(weights), _ptr(indices), N, _ptr(offsets), int(B), _ptr(per_sample_weights), _ptr(out),
             _ptr(dev_status), _stream(stream), int(path))
     _check(rc, "tbe_forward")
@@ -221,14 +260,18 @@ def tbe_forward(plan: Plan, weights, indices, offsets, B: int, per_sample_weight
 
 
 def tbe_histogram_counts(plan: Plan, indices, offsets, B: int, counts=None, dev_status=None, stream=None):
+    """Per-bag id histograms of every table: a list of int32 [B, rows_t]
+    views of one buffer of B * total_rows counts (``counts`` if given).
+    int64 ids and offsets only."""
     import torch
 
-    """Per-bag id histograms of every table: a list of int32 [B, rows_t]
-    views of one buffer of B * total_rows counts (``counts`` if given)."""
     lib = load_library()
     base = plan.table_row_base
+    _is_i32(plan, indices, offsets, B, allow_i32=False)
     if counts is None:
         counts = torch.empty(int(B) * int(base[plan.T]), dtype=torch.int32, device=indices.device)
+    _need(counts, (torch.int32,), int(B) * plan.total_rows, "counts")
+    _need(dev_status, (torch.int32,), 1, "dev_status", optional=True)
     rc = lib.tbe_histogram_counts(plan.handle, _ptr(indices), int(indices.numel()), _ptr(offsets), int(B),
                                   _ptr(counts), _ptr(dev_status), _stream(stream))
     _check(rc, "tbe_histogram_counts")
@@ -262,15 +305,31 @@ class BackwardBuffers:
         self.unique_count = torch.empty(plan.T + 1, dtype=torch.int64, device=device)
 
 
+def _need_backward(plan, grad_out, N, B, per_sample_weights, bufs, dev_status):
+    import torch
+
+    _need(grad_out, (torch.float32,), int(B) * plan.sumD, "grad_out")
+    _need(per_sample_weights, (torch.float32,), N, "per_sample_weights", optional=True)
+    _need(dev_status, (torch.int32,), 1, "dev_status", optional=True)
+    if bufs.N < N:
+        raise TBEError(f"bufs were sized for {bufs.N} lookups; this batch has {N}")
+    _need(bufs.unique_count, (torch.int64,), plan.T + 1, "bufs.unique_count")
+
+
 def tbe_backward(plan: Plan, grad_out, indices, offsets, B: int, per_sample_weights=None, bufs=None,
                  dev_status=None, want_run_starts=True, want_sorted_positions=True, stream=None):
     """Row gradients.  Returns the BackwardBuffers whose leading entries hold
     the results (U = unique_count[T], read it after a synchronisation)."""
+    import torch
+
     lib = load_library()
     N = int(indices.numel())
+    i32 = _is_i32(plan, indices, offsets, B)
     if bufs is None:
         bufs = BackwardBuffers(plan, B, N, device=indices.device)
-    fn = lib.tbe_backward_i32 if _is_i32(indices, offsets) else lib.tbe_backward
+    _need_backward(plan, grad_out, N, B, per_sample_weights, bufs, dev_status)
+    _need(bufs.workspace, (torch.uint8,), 1, "bufs.workspace")
+    fn = lib.tbe_backward_i32 if i32 else lib.tbe_backward
     rc = fn(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
                           _ptr(per_sample_weights), _ptr(bufs.unique_rows),
                           _ptr(bufs.run_starts) if want_run_starts else None,
@@ -288,8 +347,10 @@ def tbe_backward_static_workspace(plan: Plan, grad_out, indices, offsets, B: int
     supplies the outputs; its workspace is not used."""
     lib = load_library()
     N = int(indices.numel())
+    _is_i32(plan, indices, offsets, B, allow_i32=False)
     if bufs is None:
         bufs = BackwardBuffers(plan, B, N, device=indices.device, with_workspace=False)
+    _need_backward(plan, grad_out, N, B, per_sample_weights, bufs, dev_status)
     rc = lib.tbe_backward_static_workspace(plan.handle, _ptr(grad_out), _ptr(indices), N, _ptr(offsets), int(B),
                                            _ptr(per_sample_weights), _ptr(bufs.unique_rows), _ptr(bufs.run_starts),
                                            _ptr(bufs.sorted_positions), _ptr(bufs.row_grads),
@@ -304,6 +365,12 @@ def tbe_exact_update(plan: Plan, weights, bufs: BackwardBuffers, kind: int, lear
     """One exact optimizer step, in place on ``weights`` (and ``momentum``
     for row-wise Adagrad), from the outputs of a tbe_backward call that
     filled ``bufs`` on the same stream."""
+    import torch
+
+    _need_weights(plan, weights)
+    _need(momentum, (torch.float32,), plan.total_rows, "momentum", optional=True)
+    _need(bufs.unique_count, (torch.int64,), plan.T + 1, "bufs.unique_count")
+    _need(dev_status, (torch.int32,), 1, "dev_status", optional=True)
     opt = Optimizer(int(kind), float(learning_rate), float(eps))
     rc = load_library().tbe_exact_update(plan.handle, ctypes.byref(opt), _ptr(weights), _ptr(momentum),
                                          _ptr(bufs.unique_rows), bufs.N, _ptr(bufs.row_grads),
@@ -318,12 +385,20 @@ def tbe_backward_update(plan: Plan, weights, kind: int, learning_rate: float, gr
     """Backward with the exact optimizer fused in: updates ``weights`` (and
     ``momentum`` for row-wise Adagrad) in place; ``bufs`` receives the
     indexing outputs (its row_grads are not written)."""
+    import torch
+
     lib = load_library()
     N = int(indices.numel())
+    i32 = _is_i32(plan, indices, offsets, B)
     if bufs is None:
         bufs = BackwardBuffers(plan, B, N, device=indices.device, row_grads_capacity=0)
+    _need_weights(plan, weights)
+    _need(momentum, (torch.float32,), plan.total_rows, "momentum", optional=True)
+    _need_backward(plan, grad_out, N, B, per_sample_weights, bufs, dev_status)
+    _need(bufs.workspace, (torch.uint8,), 1, "bufs.workspace")
     opt = Optimizer(int(kind), float(learning_rate), float(eps))
-    rc = lib.tbe_backward_update(plan.handle, ctypes.byref(opt), _ptr(weights), _ptr(momentum), _ptr(grad_out),
+    fn = lib.tbe_backward_update_i32 if i32 else lib.tbe_backward_update
+    rc = fn(plan.handle, ctypes.byref(opt), _ptr(weights), _ptr(momentum), _ptr(grad_out),
                                  _ptr(indices), N, _ptr(offsets), int(B), _ptr(per_sample_weights),
                                  _ptr(bufs.unique_rows), _ptr(bufs.run_starts) if want_run_starts else None,
                                  _ptr(bufs.sorted_positions) if want_sorted_positions else None,

@@ -516,18 +516,39 @@ static bool opt_ok(const tbe_optimizer* opt) {
          std::isfinite(opt->learning_rate) && std::isfinite(opt->eps) && opt->eps >= 0.f;
 }
 
+// Shared by the int64 and int32 fused entry points.
+static int backward_update_call(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                                const float* grad_out, IdxPtr indices, int64_t N, IdxPtr offsets, int32_t B,
+                                const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                                int32_t* sorted_positions, int64_t* unique_count, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (!plan || !opt_ok(opt)) return TBE_ERR_INVALID_ARG;
+  if (plan->maxD > 128) return TBE_ERR_UNSUPPORTED;  // a row gradient is one quad per lane of one warp
+  if (N > 0 && (!weights || (opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum))) return TBE_ERR_INVALID_ARG;
+  if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
+  return backward_call(plan, grad_out, indices, N, offsets, B, per_sample_weights, unique_rows, run_starts,
+                       sorted_positions, nullptr, 0, unique_count, workspace, workspace_bytes, dev_status, stream,
+                       opt, weights, momentum);
+}
+
 int tbe_backward_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
                         const float* grad_out, const int64_t* indices, int64_t N, const int64_t* offsets,
                         int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
                         int32_t* sorted_positions, int64_t* unique_count, void* workspace,
                         size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  if (!plan || !opt_ok(opt)) return TBE_ERR_INVALID_ARG;
-  if (plan->maxD > 128) return TBE_ERR_UNSUPPORTED;  // a row gradient is one quad per lane of one warp
-  if (N > 0 && (!weights || (opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum))) return TBE_ERR_INVALID_ARG;
-  if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
-  return backward_call(plan, grad_out, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B, per_sample_weights,
-                       unique_rows, run_starts, sorted_positions, nullptr, 0, unique_count, workspace,
-                       workspace_bytes, dev_status, stream, opt, weights, momentum);
+  return backward_update_call(plan, opt, weights, momentum, grad_out, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B,
+                              per_sample_weights, unique_rows, run_starts, sorted_positions, unique_count,
+                              workspace, workspace_bytes, dev_status, stream);
+}
+
+int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                            const float* grad_out, const int32_t* indices, int64_t N, const int32_t* offsets,
+                            int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                            int32_t* sorted_positions, int64_t* unique_count, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return backward_update_call(plan, opt, weights, momentum, grad_out, IdxPtr{indices, 1}, N, IdxPtr{offsets, 1}, B,
+                              per_sample_weights, unique_rows, run_starts, sorted_positions, unique_count,
+                              workspace, workspace_bytes, dev_status, stream);
 }
 
 int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,

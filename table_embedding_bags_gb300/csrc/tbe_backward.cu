@@ -350,11 +350,11 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
   // all of this thread's ids are requested first (the bag search below
   // overlaps their latency)
   constexpr int kIPT = IPT;
-  int64_t id[kIPT];
+  uint64_t id[kIPT];  // raw id bits (out of range for the table when invalid)
 #pragma unroll
   for (int q = 0; q < kIPT; ++q) {
     const int64_t i = p0 + q * kLinThreads + tid;
-    id[q] = i < p1 ? a.indices.stream(i) : 0;
+    id[q] = i < p1 ? a.indices.id_bits(i) : 0;
   }
   if (tid < 64) {  // warp 0 finds the bag of p0, warp 1 the bag of p1 - 1
     const int32_t g = bag_search_warp(a.offsets, nb, tid < 32 ? p0 : p1 - 1, lane);
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     const int32_t t = g / a.B;
     const int32_t b = g - t * a.B;
     const int32_t rows = __ldg(&a.meta[t].rows);
-    const bool valid = (uint64_t)id[q] < (uint64_t)rows;
+    const bool valid = id[q] < (uint64_t)rows;
     if (!valid) { bad = 1; ++invalid; }
     uint32_t key;
     if (a.seg_dbits > 0) {

@@ -59,8 +59,8 @@ __device__ __forceinline__ void load_window(const FwdArgs& a, const TableMeta& m
 #pragma unroll
   for (int k = 0; k < kIdsPerLane; ++k) {  // the whole window in one request
     const int idx = k * lpr + sub;
-    const int64_t raw = idx < nwin ? a.indices.stream(base + idx) : 0;
-    iw.id[k] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
+    const uint64_t raw = idx < nwin ? a.indices.id_bits(base + idx) : 0;
+    iw.id[k] = raw < (uint64_t)m.rows ? (int32_t)raw : -1;
     iw.w[k] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
   }
 }
@@ -350,8 +350,8 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
 #pragma unroll
     for (int k = 0; k < kIdsPerLane; ++k) {  // the window's ids, one coalesced request
       const int idx = k * lpr + sub;
-      const int64_t raw = idx < nwin ? a.indices.stream(base + idx) : 0;
-      ids[idx] = (uint64_t)raw < (uint64_t)m.rows ? (int32_t)raw : -1;
+      const uint64_t raw = idx < nwin ? a.indices.id_bits(base + idx) : 0;
+      ids[idx] = raw < (uint64_t)m.rows ? (int32_t)raw : -1;
       if (WT) wts[idx] = (weighted && idx < nwin) ? ld_stream_f32(a.psw + base + idx) : 1.f;
     }
     __syncwarp(vmask);
@@ -697,7 +697,7 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
     // the zero row to npad; 128 positions per round, all loads issued first
 #pragma unroll 1
     for (int32_t q0 = 0; q0 < npad; q0 += 128) {
-      int64_t raw[4];
+      uint64_t raw[4];
       int32_t iu[4];
       bool vu[4];
 #pragma unroll
@@ -709,7 +709,7 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
         const int32_t lk = __shfl_sync(kFull, len, kb);
         iu[u] = __shfl_sync(kFull, st, kb) + r;
         vu[u] = q < nwin && r < lk;
-        raw[u] = vu[u] ? a.indices.stream(iu[u]) : 0;
+        raw[u] = vu[u] ? a.indices.id_bits(iu[u]) : 0;
       }
       float wv[4];
       if (WT) {
@@ -719,9 +719,9 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (q0 + u * 32 < npad) {
-          const bool ok = vu[u] && (uint64_t)raw[u] < (uint64_t)m.rows;
+          const bool ok = vu[u] && raw[u] < (uint64_t)m.rows;
           bad |= vu[u] && !ok;  // reported; contributes nothing
-          srcs[q0 + u * 32 + lane] = ok ? reinterpret_cast<uint64_t>(tbl) + (uint64_t)raw[u] * row_bytes : zero_row;
+          srcs[q0 + u * 32 + lane] = ok ? reinterpret_cast<uint64_t>(tbl) + raw[u] * row_bytes : zero_row;
           if (WT) wts[q0 + u * 32 + lane] = ok ? wv[u] : 0.f;
         }
       }

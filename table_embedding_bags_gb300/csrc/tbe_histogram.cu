@@ -48,33 +48,42 @@
 namespace tbe {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumers = 512;                 // threads that count, multiply and store
+constexpr int kWarps = kConsumers / 32;         // consumer warps
+constexpr int kThreads = kConsumers + 32;       // + one producer warp streaming the ids
 constexpr int kM = 128;                // bags per tile (MMA M)
 constexpr int kMaxK = 64;              // table rows, padded to a multiple of 16
 constexpr uint32_t kExactCount = 2048; // largest count both 16-bit count forms hold exactly
 constexpr int kWaitLimit = 1 << 24;    // mbarrier polls before giving up (TBE_DEV_TIMEOUT)
+constexpr int kChunk = 8192;           // bytes per id chunk (16 bytes per consumer thread)
+constexpr int kRingMin = 2;            // chunks in the id ring: as many as shared memory leaves room for
+constexpr int kRingMax = 24;
+constexpr int kLut = 4096;             // bag of every 32nd position of a tile (tiles of up to 128 Ki ids)
 
 // What a tile multiplies: the MMA kind and the form of its counts.
 enum HistMode : int { kModeF16 = 0, kModeBF16 = 1, kModeTF32 = 2 };
 
 // Dynamic shared memory of one CTA (offsets from a 1024-byte aligned base).
-//   [0, 64 KB)   unweighted: int32 counts [kM][kMaxK] then the 16-bit A tile
-//                [kM x 2K]; weighted: the tf32 A tile [kM x 2K], whose first K
-//                columns accumulate the fp32 sums before they are split
+//   [0, 32 KB)   unweighted: int32 counts [kM][kMaxK]
+//   [32, 64 KB)  the 16-bit A tile [kM x 2K].  Weighted tiles use [0, 64 KB)
+//                as the tf32 A tile [kM x 2K], whose first K columns
+//                accumulate the fp32 sums before they are split.
 //   b_tile       the table, [D x K] 16-bit or fp32, sized for the widest table
+//   ring         `ring` chunks of kChunk bytes of ids
 struct HistLayout {
-  uint32_t counts, a16, b_tile, off, over, stage, mbar, tmem, total;
-  __host__ __device__ HistLayout(int maxD, int b_esz) {
+  uint32_t counts, a16, b_tile, ring, off, over, stage, mbar, tmem, flags, total;
+  __host__ __device__ HistLayout(int maxD, int b_esz, int nring) {
     counts = 0;
     a16 = kM * kMaxK * 4;
     b_tile = 2 * kM * kMaxK * 4;
-    off = b_tile + ((maxD * kMaxK * b_esz + 1023) & ~1023);  // int64 [kM + 1]
-    over = off + (kM + 1) * 8;                                // uint32 [kM / 32]
-    stage = over + (kM / 32) * 4;                             // float [kWarps][32]
-    mbar = (stage + kWarps * 32 * 4 + 7) & ~7u;               // uint64
-    tmem = mbar + 8;                                          // uint32
-    total = tmem + 8;
+    ring = b_tile + ((maxD * kMaxK * b_esz + 1023) & ~1023);
+    off = ring + nring * kChunk;                              // int64 [kM + 1]
+    over = off + (kM + 1) * 8;  // uint32 [kM / 32]; then int32 off32 [kM + 1], uint8 lut [kLut]
+    stage = over + (kM / 32) * 4 + ((kM + 1) * 4 + 15) / 16 * 16 + kLut;  // float [kWarps][32]
+    mbar = (stage + kWarps * 32 * 4 + 7) & ~7u;               // uint64: MMA, full[kRingMax], empty[kRingMax]
+    tmem = mbar + 8 * (1 + 2 * kRingMax);                     // uint32
+    flags = tmem + 4;                                         // int32 [4]: stop, producer done, chunks issued
+    total = flags + 16;
   }
 };
 
@@ -145,6 +154,80 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+static_assert(kChunk == kConsumers * 16, "a chunk is one 16-byte run per consumer thread");
+
+__device__ __forceinline__ void mbar_init_count(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier 1 over the consumer warps only (the producer warp never joins).
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+__device__ __forceinline__ int consumers_sync_or(int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "n"(kConsumers)
+      : "memory");
+  return r;
+}
+
+// The ids a tile streams through the ring: the 16-byte aligned middle of its
+// range [p0, p1) (clamped to [0, N]), cut into chunks; the ragged ends (under
+// 16 bytes each) are read directly.  Producer and consumers derive it from
+// the same two offsets, so they agree on every chunk.
+struct ChunkPlan {
+  uintptr_t beg, end;  // aligned byte range
+  int64_t p0, p1;      // the tile's positions
+  int64_t pa, pe;      // first position of the aligned middle / of the ragged tail
+  int nch;             // chunks
+  __device__ ChunkPlan(const void* ids, int w, int64_t r0, int64_t r1, int64_t N) {
+    p0 = min(max(r0, (int64_t)0), N);
+    p1 = min(max(r1, p0), N);
+    const uintptr_t src0 = (uintptr_t)ids + (uintptr_t)(p0 * w), src1 = (uintptr_t)ids + (uintptr_t)(p1 * w);
+    beg = min((src0 + 15) & ~(uintptr_t)15, src1);
+    end = max(src1 & ~(uintptr_t)15, beg);
+    pa = p0 + (int64_t)((beg - src0) / w);
+    pe = p0 + (int64_t)((end - src0) / w);
+    nch = (int)((end - beg + kChunk - 1) / kChunk);
+  }
+  __device__ uint32_t bytes(int c) const { return (uint32_t)min((uintptr_t)kChunk, end - beg - (uintptr_t)c * kChunk); }
+};
+
+// The producer's arrival on a ring barrier, announcing the bytes its copy brings.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16); its bytes complete the transaction count of `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Bag of position p within a tile: the last q < nbag with off[q] <= p.
+__device__ __forceinline__ int tile_bag(const int64_t* off, int nbag, int64_t p) {
+  int lo = 0, hi = nbag - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= p) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -166,7 +249,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
 struct HistShape {
   int32_t maxD;   // widest table (sizes the B tile and the TMEM accumulator)
   int32_t b_esz;  // 4 when some tile may take the weighted (tf32) form, else 2
-  int32_t tpt;    // tiles per table, ceil(B / kM)
+  int32_t mb;     // bags per tile (<= kM; rows nbag..kM-1 of the MMA are zero)
+  int32_t tpt;    // tiles per table, ceil(B / mb)
+  int32_t ring;   // chunks in the id ring (kRingMin .. kRingMax)
 };
 
 // A table element as fp32 (fp16 or bf16 storage).
@@ -175,55 +260,177 @@ __device__ __forceinline__ float table_value(uint16_t bits, int dtype) {
 }
 
 // The tile's table into the B tile: element (n = column d, k = row r) = W[r][d];
-// rows r >= rows (the K padding) are zero.
-__device__ void load_table(unsigned char* b_tile, const uint16_t* table, int rows, int K, int D, int dtype,
+// rows r >= rows (the K padding) are zero.  The table is read as 16-byte
+// chunks (8 elements of a row), all of a thread's chunks in flight at once.
+__device__ void load_table(unsigned char* b_tile, const unsigned char* table, int rows, int K, int D, int dtype,
                            int mode, int tid) {
-  for (int e = tid; e < D * K; e += kThreads) {
-    const int r = e / D, d = e - r * D;
-    const uint16_t bits = r < rows ? table[(int64_t)r * D + d] : (uint16_t)0;
-    if (mode == kModeTF32)
-      *reinterpret_cast<float*>(b_tile + kmajor_byte(d, r, D, 4)) = r < rows ? table_value(bits, dtype) : 0.f;
-    else
-      *reinterpret_cast<uint16_t*>(b_tile + kmajor_byte(d, r, D, 2)) = bits;
+  constexpr int kPer = kMaxK * 256 / 8 / kConsumers;  // chunks per thread of the largest table
+  const int cpr = D >> 3;                           // chunks per row
+  const int n = rows * cpr;
+  uint4 v[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + u * kConsumers;
+    if (e < n) v[u] = __ldg(reinterpret_cast<const uint4*>(table) + e);
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int e = tid + u * kConsumers;
+    if (e >= n) break;
+    const int r = e / cpr, d0 = (e - r * cpr) << 3;
+    const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint16_t bits = (uint16_t)(w4[k >> 1] >> ((k & 1) * 16));
+      if (mode == kModeTF32)
+        *reinterpret_cast<float*>(b_tile + kmajor_byte(d0 + k, r, D, 4)) = table_value(bits, dtype);
+      else
+        *reinterpret_cast<uint16_t*>(b_tile + kmajor_byte(d0 + k, r, D, 2)) = bits;
+    }
+  }
+  for (int e = tid; e < (K - rows) * D; e += kConsumers) {
+    const int r = rows + e / D, d = e - (r - rows) * D;
+    if (mode == kModeTF32) *reinterpret_cast<float*>(b_tile + kmajor_byte(d, r, D, 4)) = 0.f;
+    else *reinterpret_cast<uint16_t*>(b_tile + kmajor_byte(d, r, D, 2)) = 0;
   }
 }
 
+// Counts this thread's run of a staged id chunk: the 16 bytes at tid * 16
+// (2 int64 or 4 int32 ids).  Positions are relative to the tile's first id,
+// in 32 bits.  The bag of the run's first position starts from the tile's
+// lookup of every 32nd position (lut, when the tile has one) and moves
+// forward past the bag starts up to it.
+template <int W>
+__device__ __forceinline__ void count_run(const unsigned char* chunk, int bytes, int32_t pc, const int32_t* off32,
+                                          const uint8_t* lut, int nbag, int rows, int32_t* counts, int tid, int& q,
+                                          int32_t& nb, bool& bad_id) {
+  constexpr int kPer = 16 / W;
+  const int b0 = tid * 16;
+  if (b0 >= bytes) return;  // chunk sizes are multiples of 16: a run is whole or absent
+  const uint4 v = *reinterpret_cast<const uint4*>(chunk + b0);
+  uint32_t id[kPer];  // an int64 id is in range only if its high word is 0
+  if (W == 8) {
+    id[0] = v.y ? 0xffffffffu : v.x;
+    id[1 % kPer] = v.w ? 0xffffffffu : v.z;
+  } else {
+    id[0] = v.x;
+    id[1] = v.y;
+    id[2 % kPer] = v.z;
+    id[3 % kPer] = v.w;
+  }
+  const int32_t p0 = pc + b0 / W;
+  if (lut) {
+    q = lut[p0 >> 5];
+    nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    while (p0 + k >= nb) {
+      ++q;
+      nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
+    }
+    if (id[k] < (uint32_t)rows) atomicAdd(&counts[q * kMaxK + (int)id[k]], 1);
+    else bad_id = true;
+  }
+}
+
+// The producer (one lane of the last warp): streams the id chunks of every
+// unweighted tile of the CTA's range through the ring, running ahead of the
+// consumers across tiles; a slot is refilled once all consumer warps have
+// released it.  Every wait is bounded; on a timeout, or once the consumers
+// stop, it issues nothing more.
+__device__ void produce_ids(const FwdArgs& a, const HistShape& h, int64_t tile_begin, int64_t tile_end, bool counts_only,
+                            unsigned char* ring, uint64_t* full, uint64_t* empty, volatile int32_t* flags) {
+  const int w = a.indices.i32 ? 4 : 8;
+  const int R = h.ring;
+  uint32_t seq = 0, slot = 0, par = 0;  // chunks issued; slot and fill parity of the next
+  for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
+    const int t = (int)(tile / h.tpt);
+    const int b0 = (int)(tile - (int64_t)t * h.tpt) * h.mb;
+    const int nbag = min(h.mb, a.B - b0);
+    if (!counts_only && a.psw != nullptr && __ldg(&a.meta[t].weighted)) continue;  // read directly
+    const int64_t g0 = (int64_t)t * a.B + b0;
+    const ChunkPlan cp(a.indices.p, w, a.offsets.ldg(g0), a.offsets.ldg(g0 + nbag), a.N);
+    for (int c = 0; c < cp.nch; ++c, ++seq) {
+      // a refill waits until all consumer warps released the slot's previous chunk
+      if (seq >= (uint32_t)R && !mbar_wait(&empty[slot], par ^ 1u, kWaitLimit)) {
+        report(a.status, TBE_DEV_TIMEOUT);
+        flags[0] = 1;
+      }
+      if (flags[0]) {
+        flags[1] = 1;
+        return;
+      }
+      mbar_expect_tx(&full[slot], cp.bytes(c));
+      bulk_g2s(ring + slot * kChunk, reinterpret_cast<const void*>(cp.beg + (uintptr_t)c * kChunk), cp.bytes(c),
+               &full[slot]);
+      flags[2] = (int32_t)(seq + 1);
+      if (++slot == (uint32_t)R) {
+        slot = 0;
+        par ^= 1u;
+      }
+    }
+  }
+  flags[1] = 1;
+}
+
 template <typename OutT, bool COUNTS_ONLY>
-__global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, const HistShape h, int32_t* counts_out) {
+__global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, const HistShape h, int32_t* counts_out) {
   extern __shared__ unsigned char smem_raw[];
-  const HistLayout L(h.maxD, h.b_esz);
+  const HistLayout L(h.maxD, h.b_esz, h.ring);
   unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   int32_t* counts = reinterpret_cast<int32_t*>(base + L.counts);
-  unsigned char* a32 = base + L.counts;  // the tf32 A tile shares the counts region
+  unsigned char* a32 = base + L.counts;  // the tf32 A tile spans the counts and 16-bit A regions
   unsigned char* a16 = base + L.a16;
   unsigned char* b_tile = base + L.b_tile;
+  unsigned char* ring = base + L.ring;
   int64_t* off = reinterpret_cast<int64_t*>(base + L.off);
   uint32_t* over = reinterpret_cast<uint32_t*>(base + L.over);
+  int32_t* off32 = reinterpret_cast<int32_t*>(base + L.over + (kM / 32) * 4);  // off - off[0] of a valid tile
+  uint8_t* lut = reinterpret_cast<uint8_t*>(off32) + ((kM + 1) * 4 + 15) / 16 * 16;  // bag of position 32k
   uint64_t* mbar = reinterpret_cast<uint64_t*>(base + L.mbar);
+  uint64_t* full = mbar + 1;
+  uint64_t* empty = mbar + 1 + kRingMax;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.tmem);
+  volatile int32_t* flags = reinterpret_cast<volatile int32_t*>(base + L.flags);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* stage = reinterpret_cast<float*>(base + L.stage) + warp * 32;
   const uint32_t ncols = h.maxD <= 32 ? 32 : (h.maxD <= 64 ? 64 : (h.maxD <= 128 ? 128 : 256));  // TMEM columns
   const int64_t ntiles = (int64_t)a.T * h.tpt;
   const int64_t TB = (int64_t)a.T * a.B;
   const int64_t tile_begin = ntiles * blockIdx.x / gridDim.x;
   const int64_t tile_end = ntiles * (blockIdx.x + 1) / gridDim.x;
+  const int R = h.ring;
 
-  if (!COUNTS_ONLY) {
-    if (warp == 0) tmem_alloc(tmem_slot, ncols);
-    if (tid == 0) mbar_init(mbar);
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  if (tid == 0) {
+    mbar_init(mbar);
+    for (int k = 0; k < R; ++k) {
+      mbar_init_count(&full[k], 1);
+      mbar_init_count(&empty[k], kWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    flags[0] = flags[1] = flags[2] = 0;
   }
-  __syncthreads();
+  if (!COUNTS_ONLY && warp == 0) tmem_alloc(tmem_slot, ncols);
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();  // the only barrier of all threads: from here the producer warp runs on its own
+  if (warp == kWarps) {
+    if (lane == 0) produce_ids(a, h, tile_begin, tile_end, COUNTS_ONLY, ring, full, empty, flags);
+    return;
+  }
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = COUNTS_ONLY ? 0u : *tmem_slot;
+  float* stage = reinterpret_cast<float*>(base + L.stage) + warp * 32;
   uint32_t phase = 0;
+  uint32_t slot = 0, par = 0;  // ring slot of the next chunk, and the parity of its fill
+  bool stop = false;  // a bounded wait ran out: the consumers stop
   int cur_t = -1, cur_mode = -1;
+  const int w = a.indices.i32 ? 4 : 8;
 
   for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
     const int t = (int)(tile / h.tpt);
-    const int b0 = (int)(tile - (int64_t)t * h.tpt) * kM;
-    const int nbag = min(kM, a.B - b0);
+    const int b0 = (int)(tile - (int64_t)t * h.tpt) * h.mb;
+    const int nbag = min(h.mb, a.B - b0);
     const TableMeta m = a.meta[t];
     const int rows = m.rows, D = m.D;
     const int K = (rows + 15) & ~15;  // MMA K, padded to 16
@@ -232,64 +439,84 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, cons
     const int64_t g0 = (int64_t)t * a.B + b0;
 
     if (weighted) {
-      for (int e = tid; e < K * (kM * 4 / 16); e += kThreads) reinterpret_cast<int4*>(a32)[e] = make_int4(0, 0, 0, 0);
+      for (int e = tid; e < K * (kM * 4 / 16); e += kConsumers) reinterpret_cast<int4*>(a32)[e] = make_int4(0, 0, 0, 0);
     } else {
-      for (int e = tid; e < kM * kMaxK / 4; e += kThreads) reinterpret_cast<int4*>(counts)[e] = make_int4(0, 0, 0, 0);
+      for (int e = tid; e < kM * kMaxK / 4; e += kConsumers) reinterpret_cast<int4*>(counts)[e] = make_int4(0, 0, 0, 0);
     }
     if (tid < kM / 32) over[tid] = 0;
-    for (int q = tid; q <= nbag; q += kThreads) off[q] = a.offsets.stream(g0 + q);
+    for (int q = tid; q <= nbag; q += kConsumers) off[q] = a.offsets.stream(g0 + q);
     if (!COUNTS_ONLY && (t != cur_t || mode != cur_mode)) {
-      load_table(b_tile, reinterpret_cast<const uint16_t*>(a.weights + m.w_off), rows, K, D, m.dtype, mode, tid);
+      load_table(b_tile, a.weights + m.w_off, rows, K, D, m.dtype, mode, tid);
       cur_t = t;
       cur_mode = mode;
     }
-    __syncthreads();
+    consumers_sync();
+    // the chunks this tile streams (from the offsets as read, like the producer)
+    const ChunkPlan cp(a.indices.p, w, off[0], off[nbag], a.N);
+    bool bad = false;
     {
       // bag bounds: must start at 0, never decrease and end at N; a broken
-      // tile is reported and pooled as empty
-      int bad = off[0] < 0 || off[nbag] > a.N || (g0 == 0 && off[0] != 0) || (g0 + nbag == TB && off[nbag] != a.N);
-      for (int q = tid; q < nbag; q += kThreads) bad |= off[q + 1] < off[q];
-      bad = __syncthreads_or(bad);
+      // tile is reported and pooled as empty (its chunks are still consumed)
+      int b = off[0] < 0 || off[nbag] > a.N || (g0 == 0 && off[0] != 0) || (g0 + nbag == TB && off[nbag] != a.N);
+      for (int q = tid; q < nbag; q += kConsumers) b |= off[q + 1] < off[q];
+      bad = consumers_sync_or(b);
       if (bad) {
         if (tid == 0) report(a.status, TBE_DEV_BAD_OFFSETS);
-        for (int q = tid; q <= nbag; q += kThreads) off[q] = 0;
+        for (int q = tid; q <= nbag; q += kConsumers) off[q] = 0;
+      } else {
+        for (int q = tid; q <= nbag; q += kConsumers) off32[q] = (int32_t)(off[q] - off[0]);
       }
-      __syncthreads();
+      consumers_sync();
+      // lookup of every 32nd position's bag: entry k belongs to the bag whose
+      // range holds position 32k; four threads share a bag's entries
+      if (!bad && !weighted && off[nbag] - off[0] <= (int64_t)kLut * 32) {
+        for (int i = tid; i < 4 * nbag; i += kConsumers) {
+          const int q = i >> 2;
+          for (int k = (off32[q] + 31) / 32 + (i & 3); k < (off32[q + 1] + 31) / 32; k += 4) lut[k] = (uint8_t)q;
+        }
+        consumers_sync();
+      }
     }
 
     bool bad_id = false;
-    const int64_t p0 = off[0], p1 = off[nbag];
     if (!weighted) {
-      // counts of every bag of the tile; a thread's positions only grow, so
-      // its bag index only moves forward
-      int q = 0;
-      {
-        const int64_t p = p0 + tid;
-        int lo = 0, hi = nbag - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (off[mid] <= p) lo = mid; else hi = mid - 1;
-        }
-        q = lo;
-      }
-      constexpr int kU = 16;
-      for (int64_t pb = p0; pb < p1; pb += kThreads * kU) {
-        int64_t id[kU];
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int64_t p = pb + u * kThreads + tid;
-          id[u] = p < p1 ? a.indices.stream(p) : -1;
-        }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int64_t p = pb + u * kThreads + tid;
-          if (p >= p1) break;
-          while (q < nbag - 1 && off[q + 1] <= p) ++q;
-          if ((uint64_t)id[u] < (uint64_t)rows) atomicAdd(&counts[q * kMaxK + (int)id[u]], 1);
+      // counts of every bag of the tile: the ragged ends read directly, the
+      // aligned middle from the ring, where every thread counts its own run
+      // of 32 bytes of each chunk and releases it (per warp) when done; its
+      // positions only grow, so its bag index only moves forward
+      if (!bad) {
+        const int nh = (int)(cp.pa - cp.p0), nt = (int)(cp.p1 - cp.pe);
+        if (tid < nh + nt) {
+          const int64_t p = tid < nh ? cp.p0 + tid : cp.pe + (tid - nh);
+          const uint64_t id = a.indices.id_bits(p);
+          if (id < (uint64_t)rows) atomicAdd(&counts[tile_bag(off, nbag, p) * kMaxK + (int)id], 1);
           else bad_id = true;
         }
       }
-      for (int b = tid; b < nbag; b += kThreads)
+      int q = 0;  // this thread's bag, and where the next one starts (tile-relative)
+      int32_t nb = nbag > 1 ? off32[1] : INT32_MAX;
+      const int32_t pa = bad ? 0 : (int32_t)(cp.pa - off[0]);
+      const uint8_t* tl = (off[nbag] - off[0] <= (int64_t)kLut * 32) ? lut : nullptr;  // else walk from run to run
+      for (int c = 0; c < cp.nch; ++c) {
+        const bool got = mbar_wait(&full[slot], par, kWaitLimit);
+        if (!__all_sync(0xffffffffu, got)) {  // chunk c never arrived (decided per warp)
+          stop = true;
+          break;
+        }
+        if (!bad) {
+          const unsigned char* chunk = ring + slot * kChunk;
+          const int32_t pc = pa + c * (kChunk / w);
+          if (w == 8) count_run<8>(chunk, (int)cp.bytes(c), pc, off32, tl, nbag, rows, counts, tid, q, nb, bad_id);
+          else count_run<4>(chunk, (int)cp.bytes(c), pc, off32, tl, nbag, rows, counts, tid, q, nb, bad_id);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (++slot == (uint32_t)R) {
+          slot = 0;
+          par ^= 1u;
+        }
+      }
+      for (int b = tid; b < nbag; b += kConsumers)
         if (off[b + 1] - off[b] > (int64_t)kExactCount) atomicOr(&over[b >> 5], 1u << (b & 31));
     } else {
       // sums of per-sample weights: warp per bag, 32 lookups per step in
@@ -297,24 +524,24 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, cons
       // by the lowest of them, which alone adds to the cell
       constexpr int kWU = 4;
       for (int q = warp; q < nbag; q += kWarps) {
-        const int64_t s = off[q], e = off[q + 1];
-        for (int64_t pb = s; pb < e; pb += 32 * kWU) {
-          int64_t id[kWU];
-          float w[kWU];
+        const int64_t s0 = off[q], e = off[q + 1];
+        for (int64_t pb = s0; pb < e; pb += 32 * kWU) {
+          uint64_t id[kWU];
+          float wt[kWU];
 #pragma unroll
           for (int u = 0; u < kWU; ++u) {
             const int64_t p = pb + u * 32 + lane;
-            id[u] = p < e ? a.indices.stream(p) : -1;
-            w[u] = p < e ? __ldg(a.psw + p) : 0.f;
+            id[u] = p < e ? a.indices.id_bits(p) : ~0ull;
+            wt[u] = p < e ? __ldg(a.psw + p) : 0.f;
           }
 #pragma unroll
           for (int u = 0; u < kWU; ++u) {
             if (pb + u * 32 >= e) break;  // warp-uniform
             const bool in = pb + u * 32 + lane < e;
-            const bool ok = in && (uint64_t)id[u] < (uint64_t)rows;
+            const bool ok = in && id[u] < (uint64_t)rows;
             bad_id |= in && !ok;
-            const unsigned peers = __match_any_sync(0xffffffffu, ok ? (unsigned long long)id[u] : ~0ull);
-            stage[lane] = w[u];
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? id[u] : ~0ull);
+            stage[lane] = wt[u];
             __syncwarp();
             if (ok && __ffs(peers) - 1 == lane) {
               float sum = 0.f;
@@ -327,44 +554,63 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, cons
       }
     }
     if (bad_id) report(a.status, TBE_DEV_BAD_INDEX);
-    __syncthreads();
+    if (consumers_sync_or(stop)) {
+      stop = true;
+      break;
+    }
 
     if (COUNTS_ONLY) {
       int32_t* dst = counts_out + m.row_base * (int64_t)a.B + (int64_t)b0 * rows;
-      for (int e = tid; e < nbag * rows; e += kThreads) {
+      for (int e = tid; e < nbag * rows; e += kConsumers) {
         const int q = e / rows, r = e - q * rows;
         dst[e] = counts[q * kMaxK + r];
       }
-      __syncthreads();
+      consumers_sync();
       continue;
     }
 
-    // the A operand (see the header: one or two K passes per mode)
+    // the A operand (see the header: one or two K passes per mode), one
+    // 16-byte row of a core matrix per item (bag q = item mod 128, so the
+    // 8 rows of a core matrix are written by neighbouring lanes)
     if (mode == kModeTF32) {
-      for (int e = tid; e < kM * K; e += kThreads) {
-        const int q = e / K, r = e - q * K;
-        float* cell = reinterpret_cast<float*>(a32 + kmajor_byte(q, r, kM, 4));
-        const float s = *cell, s1 = round_tf32(s);
+      for (int i = tid; i < kM * (K >> 2); i += kConsumers) {
+        const int q = i & (kM - 1), k0 = (i >> 7) << 2;
+        float4* cell = reinterpret_cast<float4*>(a32 + kmajor_byte(q, k0, kM, 4));
+        const float4 c = *cell;
+        const float4 s1 = make_float4(round_tf32(c.x), round_tf32(c.y), round_tf32(c.z), round_tf32(c.w));
         *cell = s1;
-        *reinterpret_cast<float*>(a32 + kmajor_byte(q, K + r, kM, 4)) = round_tf32(s - s1);
-      }
-    } else if (mode == kModeF16) {
-      for (int e = tid; e < kM * K; e += kThreads) {
-        const int q = e / K, r = e - q * K;
-        const int32_t c = min(counts[q * kMaxK + r], (int32_t)kExactCount);
-        *reinterpret_cast<__half*>(a16 + kmajor_byte(q, r, kM, 2)) = __int2half_rn(c);
+        *reinterpret_cast<float4*>(a32 + kmajor_byte(q, K + k0, kM, 4)) =
+            make_float4(round_tf32(c.x - s1.x), round_tf32(c.y - s1.y), round_tf32(c.z - s1.z), round_tf32(c.w - s1.w));
       }
     } else {
-      for (int e = tid; e < kM * K; e += kThreads) {
-        const int q = e / K, r = e - q * K;
-        const int32_t c = min(counts[q * kMaxK + r], (int32_t)kExactCount), lo = c & 255;
-        *reinterpret_cast<__nv_bfloat16*>(a16 + kmajor_byte(q, r, kM, 2)) = __float2bfloat16_rn((float)lo);
-        *reinterpret_cast<__nv_bfloat16*>(a16 + kmajor_byte(q, K + r, kM, 2)) = __float2bfloat16_rn((float)(c - lo));
+      for (int i = tid; i < kM * (K >> 3); i += kConsumers) {
+        const int q = i & (kM - 1), k0 = (i >> 7) << 3;
+        const int4 c0 = *reinterpret_cast<const int4*>(&counts[q * kMaxK + k0]);
+        const int4 c1 = *reinterpret_cast<const int4*>(&counts[q * kMaxK + k0 + 4]);
+        const int32_t c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+          const int32_t x = min(c[k], (int32_t)kExactCount), y = min(c[k + 1], (int32_t)kExactCount);
+          if (mode == kModeF16) {
+            const __half2 h2 = __halves2half2(__int2half_rn(x), __int2half_rn(y));
+            lo[k >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+            hi[k >> 1] = 0;
+          } else {
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn((float)(x & 255), (float)(y & 255));
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn((float)(x - (x & 255)), (float)(y - (y & 255)));
+            lo[k >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+            hi[k >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+        }
+        *reinterpret_cast<uint4*>(a16 + kmajor_byte(q, k0, kM, 2)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (mode == kModeBF16)
+          *reinterpret_cast<uint4*>(a16 + kmajor_byte(q, K + k0, kM, 2)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       }
     }
     // make the generic-proxy shared-memory writes visible to the tensor core
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
+    consumers_sync();
     if (tid == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int esz = mode == kModeTF32 ? 4 : 2;
@@ -385,19 +631,20 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, cons
     }
     const bool ok = mbar_wait(mbar, phase, kWaitLimit);
     phase ^= 1u;
-    if (__syncthreads_or(!ok)) {  // the whole CTA stops together
+    if (consumers_sync_or(!ok)) {  // the consumers stop together
       if (tid == 0) report(a.status, TBE_DEV_TIMEOUT);
+      stop = true;
       break;
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     {
-      // epilogue: warp w reads TMEM lanes 32*(w%4).. (bags); warps w and w+4
-      // split the 32-column groups
+      // epilogue: warp w reads TMEM lanes 32*(w%4).. (bags); warps w, w+4,
+      // w+8 and w+12 split the 32-column groups
       const int q = (warp & 3) * 32 + lane;
       const bool is_over = q < nbag && ((over[q >> 5] >> (q & 31)) & 1u);
       OutT* orow = reinterpret_cast<OutT*>(a.out) + (int64_t)(b0 + q) * a.sumD + m.col_off;
       const int ngroups = (D + 31) / 32;
-      const int per_warp = (ngroups + 1) / 2;
+      const int per_warp = (ngroups + 3) / 4;
       const bool vec = a.out_vec_ok;
       for (int gq = 0; gq < per_warp; ++gq) {
         const int cg = (warp >> 2) * per_warp + gq;
@@ -425,42 +672,46 @@ __global__ void __launch_bounds__(kThreads, 2) hist_kernel(const FwdArgs a, cons
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-    __syncthreads();
+    consumers_sync();
+  }
+  if (stop) {
+    // a wait ran out: stop the producer, then wait (bounded) for the copies it
+    // has in flight, so that none lands after the CTA's shared memory is gone
+    if (tid == 0) {
+      flags[0] = 1;
+      for (int it = 0; it < kWaitLimit && !flags[1]; ++it) __nanosleep(64);
+      // only the last R chunks issued can still be in flight: a slot is
+      // refilled only after its previous chunk landed and was released
+      const uint32_t issued = (uint32_t)flags[2];
+      for (uint32_t sq = issued > (uint32_t)R ? issued - R : 0u; sq < issued; ++sq)
+        mbar_wait(&full[sq % R], (sq / R) & 1u, kWaitLimit);
+    }
   }
   if (!COUNTS_ONLY) {
-    __syncthreads();
+    consumers_sync();
     if (warp == 0) tmem_dealloc(tmem, ncols);
   }
 }
 
 template <typename OutT, bool COUNTS_ONLY>
-int launch_hist(const FwdArgs& a, const HistShape& h, int32_t* counts, cudaStream_t s) {
-  const size_t smem = HistLayout(h.maxD, h.b_esz).total + 1024;  // + alignment slack
-  if (cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(hist_kernel<OutT, COUNTS_ONLY>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+int launch_hist(const FwdArgs& a, HistShape h, int32_t* counts, cudaStream_t s) {
+  auto kern = hist_kernel<OutT, COUNTS_ONLY>;
+  // one CTA per SM (persistent); the id ring takes what shared memory is left
+  int dev = 0, smem_max = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return TBE_ERR_CUDA;
+  const size_t fixed = (size_t)HistLayout(h.maxD, h.b_esz, 0).total + 1024;  // + alignment slack
+  if ((size_t)smem_max < fixed + (size_t)kRingMin * kChunk) return TBE_ERR_UNSUPPORTED;
+  h.ring = (int)std::min<size_t>(kRingMax, ((size_t)smem_max - fixed) / kChunk);
+  const size_t smem = fixed + (size_t)h.ring * kChunk;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+          cudaSuccess)
     return TBE_ERR_CUDA;
   const int64_t ntiles = (int64_t)a.T * h.tpt;
-  // CTAs per SM from the kernel's registers and shared memory (the launch
-  // bounds keep it at <= 128 registers, so two fit the register file),
-  // capped so that their TMEM accumulators fit the 512 columns of an SM
-  int per_sm = 2;
-  {
-    cudaFuncAttributes fa;
-    int dev = 0, smem_sm = 0;
-    cudaGetDevice(&dev);
-    if (cudaFuncGetAttributes(&fa, hist_kernel<OutT, COUNTS_ONLY>) == cudaSuccess &&
-        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess) {
-      const int by_regs = 65536 / std::max(1, fa.numRegs * kThreads);
-      const int by_smem = smem_sm / (int)(smem + 1024);
-      per_sm = std::max(1, std::min(by_regs, by_smem));
-    }
-  }
-  const int ncols = h.maxD <= 32 ? 32 : (h.maxD <= 64 ? 64 : (h.maxD <= 128 ? 128 : 256));
-  if (!COUNTS_ONLY) per_sm = std::min(per_sm, 512 / ncols);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, (int64_t)sm_count() * per_sm));
-  hist_kernel<OutT, COUNTS_ONLY><<<grid, kThreads, smem, s>>>(a, h, counts);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, (int64_t)sm_count()));
+  kern<<<grid, kThreads, smem, s>>>(a, h, counts);
   return check_launch();
 }
 
@@ -470,7 +721,13 @@ int launch_forward_histogram(const Plan& p, const FwdArgs& a, int32_t* counts_ou
   HistShape h;
   h.maxD = p.maxD;
   h.b_esz = (!counts_out && a.psw != nullptr && p.any_weighted) ? 4 : 2;
-  h.tpt = (a.B + kM - 1) / kM;
+  // bags per tile: at most kM, and as few as make the tiles a whole number
+  // of waves of one CTA per SM, so that every CTA counts about as many ids
+  const int64_t waves = std::max<int64_t>(1, ((int64_t)p.T * ((a.B + kM - 1) / kM) + sm_count() - 1) / sm_count());
+  const int64_t per_table = std::max<int64_t>(1, (waves * sm_count() + p.T - 1) / p.T);
+  h.mb = (int)std::min<int64_t>(kM, std::max<int64_t>(1, (a.B + per_table - 1) / per_table));
+  h.tpt = (a.B + h.mb - 1) / h.mb;
+  h.ring = kRingMin;
   if (counts_out) return launch_hist<float, true>(a, h, counts_out, s);
   switch (p.out_dtype) {
     case TBE_F32: return launch_hist<float, false>(a, h, nullptr, s);

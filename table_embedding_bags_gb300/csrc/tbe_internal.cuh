@@ -107,6 +107,19 @@ struct IdxPtr {
     asm volatile("ld.global.nc.L1::no_allocate.s64 %0, [%1];" : "=l"(v) : "l"(static_cast<const int64_t*>(p) + i));
     return v;
   }
+  // A row id as raw bits, read once: int64 ids as stored, int32 ids
+  // zero-extended by the load itself.  A negative int32 id then reads as a
+  // value of at least 2^31, out of range for every table exactly like its
+  // int64 form, so callers compare it (unsigned) with a row count and use
+  // only in-range values; nothing has to wait for the load to extend it.
+  __device__ __forceinline__ uint64_t id_bits(int64_t i) const {
+    uint64_t v;
+    if (i32)
+      asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=l"(v) : "l"(static_cast<const int32_t*>(p) + i));
+    else
+      asm volatile("ld.global.nc.L1::no_allocate.u64 %0, [%1];" : "=l"(v) : "l"(static_cast<const int64_t*>(p) + i));
+    return v;
+  }
   // read-only path (cached)
   __device__ __forceinline__ int64_t ldg(int64_t i) const {
     return i32 ? (int64_t)__ldg(static_cast<const int32_t*>(p) + i) : __ldg(static_cast<const int64_t*>(p) + i);

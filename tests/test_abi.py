@@ -139,3 +139,17 @@ def test_plan_create_checks_its_metadata_buffer(lib):
                                ctypes.byref(h)) == tbe.TBE_ERR_INVALID_ARG
     assert lib.tbe_plan_create(ctypes.byref(L), ctypes.c_void_p(base + 4), need, None,
                                ctypes.byref(h)) == tbe.TBE_ERR_INVALID_ARG
+
+
+def test_argument_checks_before_the_abi():
+    """The binding's tensor checks (no GPU needed: host tensors are refused
+    first, then dtype and size)."""
+    import torch
+
+    import table_embedding_bags_gb300 as tbe
+
+    with pytest.raises(tbe.TBEError, match="CUDA"):
+        tbe._need(torch.zeros(4, dtype=torch.int64), (torch.int64,), 4, "indices")
+    with pytest.raises(tbe.TBEError, match="required"):
+        tbe._need(None, (torch.int64,), 4, "indices")
+    tbe._need(None, (torch.float32,), 4, "per_sample_weights", optional=True)

@@ -120,3 +120,59 @@ def test_mixed_widths_rejected(tbe):
     plan = tbe.Plan.from_problem(p)
     with pytest.raises(tbe.TBEError):
         tbe.tbe_forward(plan, w_dev, d32["indices"], d["offsets"], p.B)
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["sgd", "adagrad"])
+def test_fused_update_matches_int64(tbe, kind):
+    p = make_config("mid_skewed", B=300)
+    w_a, _ = parity.weights_pair(p)
+    w_b = w_a.clone()
+    d, d32 = _both_widths(p)
+    plan = tbe.Plan.from_problem(p)
+    m_a = torch.rand(plan.total_rows, device="cuda") if kind == 1 else None
+    m_b = m_a.clone() if kind == 1 else None
+    a = tbe.tbe_backward_update(plan, w_a, kind, 0.05, d["grad"], d["indices"], d["offsets"], p.B, eps=1e-6,
+                                momentum=m_a)
+    b = tbe.tbe_backward_update(plan, w_b, kind, 0.05, d32["grad"], d32["indices"], d32["offsets"], p.B, eps=1e-6,
+                                momentum=m_b)
+    torch.cuda.synchronize()
+    U = int(a.unique_count[-1].item())
+    assert torch.equal(a.unique_rows[:U], b.unique_rows[:U])
+    assert torch.equal(w_a, w_b)
+    if kind == 1:
+        assert torch.equal(m_a.view(torch.int32), m_b.view(torch.int32))
+
+
+def test_wrappers_reject_arrays_the_kernels_would_overrun(tbe):
+    """A wrong dtype, a short buffer or a host tensor is refused before any
+    pointer reaches the library (the kernels would read or write past it)."""
+    p = make_config("tiny")
+    w_dev, _ = parity.weights_pair(p)
+    d, d32 = _both_widths(p)
+    plan = tbe.Plan.from_problem(p)
+    fwd = lambda **kw: tbe.tbe_forward(plan, kw.get("w", w_dev), kw.get("ind", d["indices"]),  # noqa: E731
+                                       kw.get("off", d["offsets"]), p.B, kw.get("psw"), out=kw.get("out"))
+    bad = [dict(ind=d["indices"].to(torch.int16), off=d["offsets"].to(torch.int16)),
+           dict(off=d["offsets"][:-1]),
+           dict(ind=d["indices"].cpu(), off=d["offsets"].cpu()),
+           dict(w=w_dev[: plan.weights_bytes - 1]),
+           dict(psw=torch.ones(p.N, dtype=torch.float16, device="cuda")),
+           dict(psw=torch.ones(p.N - 1, device="cuda")),
+           dict(out=torch.empty((p.B, plan.sumD), dtype=torch.float16, device="cuda")),
+           dict(out=torch.empty((p.B - 1, plan.sumD), device="cuda"))]
+    for kw in bad:
+        with pytest.raises(tbe.TBEError):
+            fwd(**kw)
+    with pytest.raises(tbe.TBEError):
+        tbe.tbe_backward(plan, d["grad"].half(), d["indices"], d["offsets"], p.B)
+    with pytest.raises(tbe.TBEError):
+        tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p.B,
+                         bufs=tbe.BackwardBuffers(plan, p.B, p.N - 1))
+    with pytest.raises(tbe.TBEError):  # int64-only entry points
+        tbe.tbe_backward_static_workspace(plan, d["grad"], d32["indices"], d32["offsets"], p.B)
+    with pytest.raises(tbe.TBEError):
+        tbe.tbe_histogram_counts(plan, d32["indices"], d32["offsets"], p.B)
+    with pytest.raises(tbe.TBEError):  # momentum shorter than the tables' rows
+        tbe.tbe_backward_update(plan, w_dev, 1, 0.1, d["grad"], d["indices"], d["offsets"], p.B,
+                                momentum=torch.zeros(plan.total_rows - 1, device="cuda"))
+    torch.cuda.synchronize()
