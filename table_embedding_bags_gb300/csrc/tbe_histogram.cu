@@ -50,7 +50,8 @@ namespace {
 
 constexpr int kConsumers = 512;                 // threads that count, multiply and store
 constexpr int kWarps = kConsumers / 32;         // consumer warps
-constexpr int kThreads = kConsumers + 32;       // + one producer warp streaming the ids
+constexpr int kProducers = 128;                 // threads streaming the ids into the ring
+constexpr int kThreads = kConsumers + kProducers;
 constexpr int kM = 128;                // bags per tile (MMA M)
 constexpr int kMaxK = 64;              // table rows, padded to a multiple of 16
 constexpr uint32_t kExactCount = 2048; // largest count both 16-bit count forms hold exactly
@@ -82,7 +83,7 @@ struct HistLayout {
     stage = over + (kM / 32) * 4 + ((kM + 1) * 4 + 15) / 16 * 16 + kLut;  // float [kWarps][32]
     mbar = (stage + kWarps * 32 * 4 + 7) & ~7u;               // uint64: MMA, full[kRingMax], empty[kRingMax]
     tmem = mbar + 8 * (1 + 2 * kRingMax);                     // uint32
-    flags = tmem + 4;                                         // int32 [4]: stop, producer done, chunks issued
+    flags = tmem + 4;                                         // int32 [4]: [0] stop
     total = flags + 16;
   }
 };
@@ -204,20 +205,6 @@ struct ChunkPlan {
   __device__ uint32_t bytes(int c) const { return (uint32_t)min((uintptr_t)kChunk, end - beg - (uintptr_t)c * kChunk); }
 };
 
-// The producer's arrival on a ring barrier, announcing the bytes its copy brings.
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple
-// of 16); its bytes complete the transaction count of `bar`.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
-}
-
 // Bag of position p within a tile: the last q < nbag with off[q] <= p.
 __device__ __forceinline__ int tile_bag(const int64_t* off, int nbag, int64_t p) {
   int lo = 0, hi = nbag - 1;
@@ -295,6 +282,29 @@ __device__ void load_table(unsigned char* b_tile, const unsigned char* table, in
   }
 }
 
+// Two adjacent outputs rounded to the output type (one 8- or 4-byte store
+// when the row segment is 16-byte aligned).
+template <typename OutT>
+__device__ __forceinline__ void store_pair(OutT* dst, float x, float y, bool vec);
+
+template <>
+__device__ __forceinline__ void store_pair<float>(float* dst, float x, float y, bool vec) {
+  if (vec) *reinterpret_cast<float2*>(dst) = make_float2(x, y);
+  else { dst[0] = x; dst[1] = y; }
+}
+
+template <>
+__device__ __forceinline__ void store_pair<__half>(__half* dst, float x, float y, bool vec) {
+  if (vec) *reinterpret_cast<__half2*>(dst) = __floats2half2_rn(x, y);
+  else { dst[0] = __float2half_rn(x); dst[1] = __float2half_rn(y); }
+}
+
+template <>
+__device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* dst, float x, float y, bool vec) {
+  if (vec) *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(x, y);
+  else { dst[0] = __float2bfloat16_rn(x); dst[1] = __float2bfloat16_rn(y); }
+}
+
 // Counts this thread's run of a staged id chunk: the 16 bytes at tid * 16
 // (2 int64 or 4 int32 ids).  Positions are relative to the tile's first id,
 // in 32 bits.  The bag of the run's first position starts from the tile's
@@ -334,17 +344,25 @@ __device__ __forceinline__ void count_run(const unsigned char* chunk, int bytes,
   }
 }
 
-// The producer (one lane of the last warp): streams the id chunks of every
-// unweighted tile of the CTA's range through the ring, running ahead of the
-// consumers across tiles; a slot is refilled once all consumer warps have
-// released it.  Every wait is bounded; on a timeout, or once the consumers
-// stop, it issues nothing more.
+// One 16-byte piece of an id chunk, global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async16_cg(uint32_t dst, uintptr_t src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// The producer warps: stream the id chunks of every unweighted tile of the
+// CTA's range through the ring, running ahead of the consumers across tiles.
+// Each producer thread copies its 16-byte pieces of a chunk and has the
+// chunk's full barrier count its arrival once they have landed; a slot is
+// refilled once all consumer warps have released it.  Every wait is bounded;
+// on a timeout, or once the consumers stop, nothing more is issued, and no
+// thread leaves before its copies have landed.
 __device__ void produce_ids(const FwdArgs& a, const HistShape& h, int64_t tile_begin, int64_t tile_end, bool counts_only,
-                            unsigned char* ring, uint64_t* full, uint64_t* empty, volatile int32_t* flags) {
+                            unsigned char* ring, uint64_t* full, uint64_t* empty, volatile int32_t* flags, int ptid) {
   const int w = a.indices.i32 ? 4 : 8;
   const int R = h.ring;
+  const uint32_t ring_u32 = smem_u32(ring);
   uint32_t seq = 0, slot = 0, par = 0;  // chunks issued; slot and fill parity of the next
-  for (int64_t tile = tile_begin; tile < tile_end; ++tile) {
+  for (int64_t tile = tile_begin; tile < tile_end && !flags[0]; ++tile) {
     const int t = (int)(tile / h.tpt);
     const int b0 = (int)(tile - (int64_t)t * h.tpt) * h.mb;
     const int nbag = min(h.mb, a.B - b0);
@@ -357,28 +375,28 @@ __device__ void produce_ids(const FwdArgs& a, const HistShape& h, int64_t tile_b
         report(a.status, TBE_DEV_TIMEOUT);
         flags[0] = 1;
       }
-      if (flags[0]) {
-        flags[1] = 1;
-        return;
-      }
-      mbar_expect_tx(&full[slot], cp.bytes(c));
-      bulk_g2s(ring + slot * kChunk, reinterpret_cast<const void*>(cp.beg + (uintptr_t)c * kChunk), cp.bytes(c),
-               &full[slot]);
-      flags[2] = (int32_t)(seq + 1);
+      if (flags[0]) break;
+      const uint32_t bytes = cp.bytes(c);
+      const uintptr_t src = cp.beg + (uintptr_t)c * kChunk;
+      for (uint32_t j = (uint32_t)ptid * 16; j < bytes; j += kProducers * 16)
+        cp_async16_cg(ring_u32 + slot * kChunk + j, src + j);
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&full[slot])) : "memory");
       if (++slot == (uint32_t)R) {
         slot = 0;
         par ^= 1u;
       }
     }
   }
-  flags[1] = 1;
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <typename OutT, bool COUNTS_ONLY>
 __global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, const HistShape h, int32_t* counts_out) {
   extern __shared__ unsigned char smem_raw[];
   const HistLayout L(h.maxD, h.b_esz, h.ring);
-  unsigned char* base = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned by pointer arithmetic on the shared array itself, so that every
+  // access through `base` stays a shared-memory access
+  unsigned char* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   int32_t* counts = reinterpret_cast<int32_t*>(base + L.counts);
   unsigned char* a32 = base + L.counts;  // the tf32 A tile spans the counts and 16-bit A regions
   unsigned char* a16 = base + L.a16;
@@ -405,17 +423,17 @@ __global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, cons
   if (tid == 0) {
     mbar_init(mbar);
     for (int k = 0; k < R; ++k) {
-      mbar_init_count(&full[k], 1);
+      mbar_init_count(&full[k], kProducers);
       mbar_init_count(&empty[k], kWarps);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    flags[0] = flags[1] = flags[2] = 0;
+    flags[0] = 0;
   }
   if (!COUNTS_ONLY && warp == 0) tmem_alloc(tmem_slot, ncols);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();  // the only barrier of all threads: from here the producer warp runs on its own
-  if (warp == kWarps) {
-    if (lane == 0) produce_ids(a, h, tile_begin, tile_end, COUNTS_ONLY, ring, full, empty, flags);
+  if (tid >= kConsumers) {
+    produce_ids(a, h, tile_begin, tile_end, COUNTS_ONLY, ring, full, empty, flags, tid - kConsumers);
     return;
   }
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -638,55 +656,56 @@ __global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, cons
     }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     {
-      // epilogue: warp w reads TMEM lanes 32*(w%4).. (bags); warps w, w+4,
-      // w+8 and w+12 split the 32-column groups
-      const int q = (warp & 3) * 32 + lane;
+      // epilogue, 64 columns at a time through the 16-bit A region (free
+      // once the MMA has read it): warps w and w+4 (w < 4) read the two
+      // 32-column halves of TMEM lanes 32w.. (bag q = 32w + lane) into row q
+      // of a [kM][64] fp32 staging tile, its 16-byte units XOR-swizzled by
+      // q & 7 so that neither the row writes nor the row reads conflict;
+      // then every warp stores whole bag rows, coalesced
+      const int quarter = warp & 3, half = warp >> 2;
+      const int q = quarter * 32 + lane;
       const bool is_over = q < nbag && ((over[q >> 5] >> (q & 31)) & 1u);
-      OutT* orow = reinterpret_cast<OutT*>(a.out) + (int64_t)(b0 + q) * a.sumD + m.col_off;
-      const int ngroups = (D + 31) / 32;
-      const int per_warp = (ngroups + 3) / 4;
+      float* stg = reinterpret_cast<float*>(a16);
       const bool vec = a.out_vec_ok;
-      for (int gq = 0; gq < per_warp; ++gq) {
-        const int cg = (warp >> 2) * per_warp + gq;
-        if (cg >= ngroups) break;
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(cg * 32), v);
-        if (is_over) {  // exact recount of an unweighted bag too long for 16-bit counts
+      for (int c0 = 0; c0 < D; c0 += 64) {
+        if (half < 2 && c0 + half * 32 < D) {  // warp-uniform
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(c0 + half * 32), v);
+          if (is_over) {  // exact recount of an unweighted bag too long for 16-bit counts
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (cg * 32 + c < D) {
-              float acc = 0.f;
-              for (int r = 0; r < rows; ++r) {
-                const uint16_t bits = *reinterpret_cast<const uint16_t*>(b_tile + kmajor_byte(cg * 32 + c, r, D, 2));
-                acc = __fadd_rn(acc, __fmul_rn((float)counts[q * kMaxK + r], table_value(bits, m.dtype)));
+            for (int c = 0; c < 32; ++c) {
+              if (c0 + half * 32 + c < D) {
+                float acc = 0.f;
+                for (int r = 0; r < rows; ++r) {
+                  const uint16_t bits =
+                      *reinterpret_cast<const uint16_t*>(b_tile + kmajor_byte(c0 + half * 32 + c, r, D, 2));
+                  acc = __fadd_rn(acc, __fmul_rn((float)counts[q * kMaxK + r], table_value(bits, m.dtype)));
+                }
+                v[c] = acc;
               }
-              v[c] = acc;
             }
           }
-        }
-        if (q < nbag) {
 #pragma unroll
-          for (int c = 0; c < 32; c += 8)
-            if (cg * 32 + c < D) store_out<OutT>(orow + cg * 32 + c, v + c, 8, vec);
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stg + q * 64 + (((half * 8 + j) ^ (q & 7)) << 2)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
+        consumers_sync();
+        const int ncol = min(64, D - c0);
+        if (2 * lane < ncol) {
+          for (int r = warp; r < nbag; r += kWarps) {
+            const float2 x = *reinterpret_cast<const float2*>(stg + r * 64 + (((lane >> 1) ^ (r & 7)) << 2) + ((lane & 1) << 1));
+            OutT* dst = reinterpret_cast<OutT*>(a.out) + (int64_t)(b0 + r) * a.sumD + m.col_off + c0 + 2 * lane;
+            store_pair<OutT>(dst, x.x, x.y, vec);
+          }
+        }
+        consumers_sync();
       }
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     consumers_sync();
   }
-  if (stop) {
-    // a wait ran out: stop the producer, then wait (bounded) for the copies it
-    // has in flight, so that none lands after the CTA's shared memory is gone
-    if (tid == 0) {
-      flags[0] = 1;
-      for (int it = 0; it < kWaitLimit && !flags[1]; ++it) __nanosleep(64);
-      // only the last R chunks issued can still be in flight: a slot is
-      // refilled only after its previous chunk landed and was released
-      const uint32_t issued = (uint32_t)flags[2];
-      for (uint32_t sq = issued > (uint32_t)R ? issued - R : 0u; sq < issued; ++sq)
-        mbar_wait(&full[sq % R], (sq / R) & 1u, kWaitLimit);
-    }
-  }
+  if (stop && tid == 0) flags[0] = 1;  // a wait ran out: the producers issue nothing more
   if (!COUNTS_ONLY) {
     consumers_sync();
     if (warp == 0) tmem_dealloc(tmem, ncols);
