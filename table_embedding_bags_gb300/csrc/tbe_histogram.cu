@@ -56,7 +56,7 @@ constexpr int kM = 128;                // bags per tile (MMA M)
 constexpr int kMaxK = 64;              // table rows, padded to a multiple of 16
 constexpr uint32_t kExactCount = 2048; // largest count both 16-bit count forms hold exactly
 constexpr int kWaitLimit = 1 << 24;    // mbarrier polls before giving up (TBE_DEV_TIMEOUT)
-constexpr int kChunk = 8192;           // bytes per id chunk (16 bytes per consumer thread)
+constexpr int kChunk = 16384;          // bytes per id chunk (32 bytes per consumer thread)
 constexpr int kRingMin = 2;            // chunks in the id ring: as many as shared memory leaves room for
 constexpr int kRingMax = 24;
 constexpr int kLut = 4096;             // bag of every 32nd position of a tile (tiles of up to 128 Ki ids)
@@ -155,7 +155,8 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-static_assert(kChunk == kConsumers * 16, "a chunk is one 16-byte run per consumer thread");
+constexpr int kRun = kChunk / kConsumers;  // bytes of a chunk one consumer thread counts
+static_assert(kRun == 32, "a chunk is one 32-byte run per consumer thread");
 
 __device__ __forceinline__ void mbar_init_count(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -305,43 +306,67 @@ __device__ __forceinline__ void store_pair<__nv_bfloat16>(__nv_bfloat16* dst, fl
   else { dst[0] = __float2bfloat16_rn(x); dst[1] = __float2bfloat16_rn(y); }
 }
 
-// Counts this thread's run of a staged id chunk: the 16 bytes at tid * 16
-// (2 int64 or 4 int32 ids).  Positions are relative to the tile's first id,
-// in 32 bits.  The bag of the run's first position starts from the tile's
-// lookup of every 32nd position (lut, when the tile has one) and moves
-// forward past the bag starts up to it.
+// Counts this thread's runs of the tile's staged id chunks: of each chunk,
+// the kRun bytes at tid * kRun (4 int64 or 8 int32 ids), and releases each
+// chunk (per warp) when done.  Positions are relative to the tile's first
+// id, in 32 bits.  The bag of a run's first position comes from the tile's
+// lookup of every 32nd position (lut, when the tile has one) or from the
+// previous run, and moves forward past the bag starts up to it.  Returns
+// false when a chunk never arrived (decided per warp).
 template <int W>
-__device__ __forceinline__ void count_run(const unsigned char* chunk, int bytes, int32_t pc, const int32_t* off32,
-                                          const uint8_t* lut, int nbag, int rows, int32_t* counts, int tid, int& q,
-                                          int32_t& nb, bool& bad_id) {
-  constexpr int kPer = 16 / W;
-  const int b0 = tid * 16;
-  if (b0 >= bytes) return;  // chunk sizes are multiples of 16: a run is whole or absent
-  const uint4 v = *reinterpret_cast<const uint4*>(chunk + b0);
-  uint32_t id[kPer];  // an int64 id is in range only if its high word is 0
-  if (W == 8) {
-    id[0] = v.y ? 0xffffffffu : v.x;
-    id[1 % kPer] = v.w ? 0xffffffffu : v.z;
-  } else {
-    id[0] = v.x;
-    id[1] = v.y;
-    id[2 % kPer] = v.z;
-    id[3 % kPer] = v.w;
-  }
-  const int32_t p0 = pc + b0 / W;
-  if (lut) {
-    q = lut[p0 >> 5];
-    nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
-  }
+__device__ __forceinline__ bool consume_chunks(const unsigned char* ring, uint64_t* full, uint64_t* empty, int R,
+                                               uint32_t& slot, uint32_t& par, int nch, uint32_t last_bytes,
+                                               int32_t pa, bool count, const int32_t* off32, const uint8_t* lut,
+                                               int nbag, int rows, int32_t* counts, int tid, int lane,
+                                               bool& bad_id) {
+  constexpr int kPer = kRun / W;
+  int q = 0;  // this thread's bag, and where the next one starts
+  int32_t nb = nbag > 1 ? off32[1] : INT32_MAX;
+  const int b0 = tid * kRun;
+  int32_t p0 = pa + b0 / W;  // the first position of this thread's run in chunk c
+  for (int c = 0; c < nch; ++c, p0 += kChunk / W) {
+    const bool got = mbar_wait(&full[slot], par, kWaitLimit);
+    if (!__all_sync(0xffffffffu, got)) return false;
+    const uint32_t bytes = c == nch - 1 ? last_bytes : (uint32_t)kChunk;
+    if (count && (uint32_t)b0 < bytes) {  // chunk sizes are multiples of 16: a run is whole, half or absent
+      const unsigned char* chunk = ring + slot * kChunk + b0;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(chunk);
+      const uint4 v1 = (uint32_t)b0 + 16 < bytes ? *reinterpret_cast<const uint4*>(chunk + 16) : make_uint4(0, 0, 0, 0);
+      const int n = (uint32_t)b0 + 16 < bytes ? kPer : kPer / 2;
+      uint32_t id[kPer];  // an int64 id is in range only if its high word is 0
+      if (W == 8) {
+        id[0] = v0.y ? 0xffffffffu : v0.x;
+        id[1] = v0.w ? 0xffffffffu : v0.z;
+        id[2 % kPer] = v1.y ? 0xffffffffu : v1.x;
+        id[3 % kPer] = v1.w ? 0xffffffffu : v1.z;
+      } else {
+        const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    while (p0 + k >= nb) {
-      ++q;
-      nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
+        for (int k = 0; k < kPer; ++k) id[k] = u[k];
+      }
+      if (lut) {
+        q = lut[p0 >> 5];
+        nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if (k >= n) break;
+        while (p0 + k >= nb) {
+          ++q;
+          nb = q < nbag - 1 ? off32[q + 1] : INT32_MAX;
+        }
+        if (id[k] < (uint32_t)rows) atomicAdd(&counts[q * kMaxK + (int)id[k]], 1);
+        else bad_id = true;
+      }
     }
-    if (id[k] < (uint32_t)rows) atomicAdd(&counts[q * kMaxK + (int)id[k]], 1);
-    else bad_id = true;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (++slot == (uint32_t)R) {
+      slot = 0;
+      par ^= 1u;
+    }
   }
+  return true;
 }
 
 // One 16-byte piece of an id chunk, global -> shared, cached in L2 only.
@@ -511,29 +536,14 @@ __global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, cons
           else bad_id = true;
         }
       }
-      int q = 0;  // this thread's bag, and where the next one starts (tile-relative)
-      int32_t nb = nbag > 1 ? off32[1] : INT32_MAX;
       const int32_t pa = bad ? 0 : (int32_t)(cp.pa - off[0]);
       const uint8_t* tl = (off[nbag] - off[0] <= (int64_t)kLut * 32) ? lut : nullptr;  // else walk from run to run
-      for (int c = 0; c < cp.nch; ++c) {
-        const bool got = mbar_wait(&full[slot], par, kWaitLimit);
-        if (!__all_sync(0xffffffffu, got)) {  // chunk c never arrived (decided per warp)
-          stop = true;
-          break;
-        }
-        if (!bad) {
-          const unsigned char* chunk = ring + slot * kChunk;
-          const int32_t pc = pa + c * (kChunk / w);
-          if (w == 8) count_run<8>(chunk, (int)cp.bytes(c), pc, off32, tl, nbag, rows, counts, tid, q, nb, bad_id);
-          else count_run<4>(chunk, (int)cp.bytes(c), pc, off32, tl, nbag, rows, counts, tid, q, nb, bad_id);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if (++slot == (uint32_t)R) {
-          slot = 0;
-          par ^= 1u;
-        }
-      }
+      const uint32_t last = cp.nch > 0 ? cp.bytes(cp.nch - 1) : 0u;
+      const bool ok = w == 8 ? consume_chunks<8>(ring, full, empty, R, slot, par, cp.nch, last, pa, !bad, off32, tl,
+                                                 nbag, rows, counts, tid, lane, bad_id)
+                             : consume_chunks<4>(ring, full, empty, R, slot, par, cp.nch, last, pa, !bad, off32, tl,
+                                                 nbag, rows, counts, tid, lane, bad_id);
+      if (!ok) stop = true;
       for (int b = tid; b < nbag; b += kConsumers)
         if (off[b + 1] - off[b] > (int64_t)kExactCount) atomicOr(&over[b >> 5], 1u << (b & 31));
     } else {
