@@ -340,8 +340,8 @@ int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void
  *                        of the kernel with a smaller register budget)
  *   hist_min_mean_bag  : TBE_PATH_AUTO takes the histogram path only when
  *                        N / (T * B) reaches this; 0 (default) = the
- *                        measured gate: 16 when no table has more than 32
- *                        rows, 32 above
+ *                        measured gate: 16, or 32 when weighted tables get
+ *                        per-sample weights
  *   short_item_lookups : lookups per work item of the short-run tier (runs
  *                        are grouped by 32 and cut into parts of about this
  *                        many lookups; raised to long_run_threshold if lower)

@@ -18,8 +18,9 @@ namespace tbe {
 //    mid-size, backward-skew and three run-length band workloads; a threshold
 //    of 256 was 1.34x slower on runs of 32..255 lookups;
 //  - hist_min_mean_bag 0 selects the measured gate: the histogram path beat
-//    the gather path from a mean bag length of 16 on tables of up to 32 rows
-//    and from 32 on tables of 33..64 rows (fp16, D = 128).
+//    the gather path from a mean bag length of 16 on fp16 and bf16 tables of
+//    8..64 rows, one or four tables (D = 128), and with per-sample weights
+//    from 16 on 16-row tables but only from 32 on 64-row tables.
 static Tuning g_tuning = {/*long_run_threshold=*/32, /*long_chunk=*/0, /*fwd_unroll=*/4,
                           /*fwd_blocks_per_sm=*/0, /*hist_min_mean_bag=*/0,
                           /*short_item_lookups=*/32, /*fwd_lanes_per_row=*/16,
@@ -343,11 +344,9 @@ static int check_common(const tbe_plan* plan, const void* indices, int64_t N, co
 }
 
 // Mean bag length from which TBE_PATH_AUTO takes the histogram path.
-static int64_t hist_gate(const tbe_plan& plan) {
+static int64_t hist_gate(const tbe_plan& plan, const float* psw) {
   if (g_tuning.hist_min_mean_bag > 0) return g_tuning.hist_min_mean_bag;
-  int32_t max_rows = 0;
-  for (int32_t t = 0; t < plan.T; ++t) max_rows = std::max(max_rows, plan.hmeta[t].rows);
-  return max_rows <= 32 ? 16 : 32;
+  return psw != nullptr && plan.any_weighted ? 32 : 16;
 }
 
 static bool hist_eligible(const tbe_plan* plan) { return plan->hist_ok; }
@@ -383,7 +382,7 @@ static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indice
     if (!hist_eligible(plan)) return TBE_ERR_UNSUPPORTED;
     hist = true;
   } else if (path == TBE_PATH_AUTO) {
-    hist = hist_eligible(plan) && N >= hist_gate(*plan) * (int64_t)plan->T * B;
+    hist = hist_eligible(plan) && N >= hist_gate(*plan, per_sample_weights) * (int64_t)plan->T * B;
   }
   trace_begin(s);
   st = hist ? launch_forward_histogram(*plan, a, nullptr, s) : launch_forward_gather(*plan, a, s);
