@@ -333,8 +333,10 @@ int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void
  *                        a shared-memory ring), 1 = per-bag ring (16 rows in
  *                        flight per lane group), 0 = rows loaded into
  *                        registers, 3 = automatic (stream when every row
- *                        is at most 256 bytes, else per-bag ring); rows
- *                        wider than 512 bytes always use the register kernel
+ *                        is at most 256 bytes, or at most 512 bytes with a
+ *                        mean bag under 32 lookups; else per-bag ring);
+ *                        rows wider than 512 bytes always use the register
+ *                        kernel
  *   fwd_blocks_per_sm  : resident blocks per SM of the gather grid (0 = as
  *                        many as fit; 4 with fwd_unroll 4 selects a build
  *                        of the kernel with a smaller register budget)

@@ -1026,8 +1026,17 @@ int launch_dtsel(const Plan& p, const FwdArgs& a, cudaStream_t s) {
 // faster at every batch size measured (2 K .. 33 K lookups per SM).
 constexpr int kStreamMaxRowBytes = 256;
 
+// Automatic kernel choice (fwd_ring 3), measured: the stream kernel for rows
+// of at most 256 bytes; for rows of up to 512 bytes it still wins on short
+// bags (mean under 32 lookups), where it overlaps rows across bags, and the
+// per-bag ring, with its deeper queue per bag, wins on long ones.
+constexpr int kStreamMaxMeanBag = 32;
+
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s) {
-  const int mode = tuning().fwd_ring == 3 ? (p.max_row_bytes <= kStreamMaxRowBytes ? 2 : 1) : tuning().fwd_ring;
+  const bool short_bags = a.N < (int64_t)kStreamMaxMeanBag * a.T * a.B;
+  const int mode = tuning().fwd_ring == 3
+                       ? ((p.max_row_bytes <= kStreamMaxRowBytes || (p.max_row_bytes <= 512 && short_bags)) ? 2 : 1)
+                       : tuning().fwd_ring;
   if (mode == 2 && ring_eligible(p)) {
     switch (p.out_dtype) {
       case TBE_F32: return launch_stream_dt<float>(p, a, s);
