@@ -313,6 +313,45 @@ int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void
                             size_t workspace_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * The backward in two calls ([FBT] "Using it, and the import that stops you":
+ * the index transpose hoisted ahead of the gradient).  Everything up to the
+ * reduction -- linearize, sort, segmentation, classification -- reads only
+ * the ids, offsets and per-sample weights, so it can run before grad_out
+ * exists, e.g. on a second stream beside the forward:
+ *   tbe_backward_index  : those stages; writes unique_rows, run_starts,
+ *                         sorted_positions (each optional as in
+ *                         tbe_backward), unique_count and the workspace.
+ *                         row_grads_capacity is the capacity the reduction
+ *                         will get (INT64_MAX when it applies an optimizer);
+ *                         a shortfall is reported here (TBE_DEV_CAPACITY).
+ *   tbe_backward_reduce : the reduction, on the same plan, N, B, presence of
+ *                         per-sample weights, unique_rows, run_starts,
+ *                         unique_count and workspace, launched after the
+ *                         index call has completed or on the same stream
+ *                         after it.  With opt == NULL it writes row_grads
+ *                         as tbe_backward; with an optimizer it updates
+ *                         weights (and momentum) in place as
+ *                         tbe_backward_update and writes no row gradients.
+ * The pair gives exactly tbe_backward's (or tbe_backward_update's) results.
+ * Errors: as tbe_backward / tbe_backward_update. */
+int tbe_backward_index(const tbe_plan* plan, const int64_t* indices, int64_t N, const int64_t* offsets, int32_t B,
+                       const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                       int32_t* sorted_positions, int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+/* tbe_backward_index with 32-bit ids and offsets. */
+int tbe_backward_index_i32(const tbe_plan* plan, const int32_t* indices, int64_t N, const int32_t* offsets,
+                           int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                           int32_t* sorted_positions, int64_t row_grads_capacity, int64_t* unique_count,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream);
+
+int tbe_backward_reduce(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                        const float* grad_out, int64_t N, int32_t B, const float* per_sample_weights,
+                        int64_t* unique_rows, int32_t* run_starts, float* row_grads, int64_t row_grads_capacity,
+                        int64_t* unique_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream);
+
+/*
  * Tuning knobs (process-wide; set them before launching work that should
  * use them, not concurrently with launches).
  *   long_run_threshold : runs with at least this many lookups take the

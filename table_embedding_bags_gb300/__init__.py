@@ -31,7 +31,8 @@ EXPORTED = [
     "tbe_histogram_counts", "tbe_backward_workspace_bytes", "tbe_backward", "tbe_get_tuning",
     "tbe_set_tuning", "tbe_trace_enable", "tbe_trace_read", "tbe_status_string", "tbe_version",
     "tbe_backward_static_workspace", "tbe_exact_update", "tbe_wait_selftest", "tbe_backward_update",
-    "tbe_forward_i32", "tbe_backward_i32", "tbe_backward_update_i32",
+    "tbe_forward_i32", "tbe_backward_i32", "tbe_backward_update_i32", "tbe_backward_index", "tbe_backward_index_i32",
+    "tbe_backward_reduce",
 ]
 TBE_STATIC_WORKSPACE_BYTES = 32 << 20
 
@@ -114,6 +115,12 @@ def load_library(path: str = LIB_PATH):
     lib.tbe_backward_update.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, P, i64, P, i32, P, P, P, P, P, P, sz,
                                         P, P]
     lib.tbe_backward_update_i32.argtypes = lib.tbe_backward_update.argtypes
+    for name in ("tbe_backward_index", "tbe_backward_index_i32"):
+        getattr(lib, name).restype = ctypes.c_int
+        getattr(lib, name).argtypes = [P, P, i64, P, i32, P, P, P, P, i64, P, P, sz, P, P]
+    lib.tbe_backward_reduce.restype = ctypes.c_int
+    lib.tbe_backward_reduce.argtypes = [P, ctypes.POINTER(Optimizer), P, P, P, i64, i32, P, P, P, P, i64, P, P, sz, P,
+                                        P]
     lib.tbe_wait_selftest.restype = ctypes.c_int
     lib.tbe_wait_selftest.argtypes = [i32, i32, P, P]
     _lib = lib
@@ -405,6 +412,66 @@ def tbe_backward_update(plan: Plan, weights, kind: int, learning_rate: float, gr
                                  _ptr(bufs.unique_count), _ptr(bufs.workspace), bufs.workspace.numel(),
                                  _ptr(dev_status), _stream(stream))
     _check(rc, "tbe_backward_update")
+    return bufs
+
+
+def tbe_backward_index(plan: Plan, indices, offsets, B: int, per_sample_weights=None, bufs=None, dev_status=None,
+                       fused=False, want_run_starts=True, want_sorted_positions=True, stream=None):
+    """The index stages of the backward (everything before the reduction;
+    no grad_out needed).  Returns the BackwardBuffers to pass to
+    tbe_backward_reduce; ``fused`` when the reduction will apply an
+    optimizer (no row gradients, so no capacity check)."""
+    import torch
+
+    lib = load_library()
+    N = int(indices.numel())
+    i32 = _is_i32(plan, indices, offsets, B)
+    if bufs is None:
+        bufs = BackwardBuffers(plan, B, N, device=indices.device, row_grads_capacity=0 if fused else None)
+    _need(per_sample_weights, (torch.float32,), N, "per_sample_weights", optional=True)
+    _need(dev_status, (torch.int32,), 1, "dev_status", optional=True)
+    if bufs.N < N:
+        raise TBEError(f"bufs were sized for {bufs.N} lookups; this batch has {N}")
+    _need(bufs.unique_count, (torch.int64,), plan.T + 1, "bufs.unique_count")
+    _need(bufs.workspace, (torch.uint8,), 1, "bufs.workspace")
+    fn = lib.tbe_backward_index_i32 if i32 else lib.tbe_backward_index
+    cap = (1 << 63) - 1 if fused else bufs.row_grads_capacity
+    rc = fn(plan.handle, _ptr(indices), N, _ptr(offsets), int(B), _ptr(per_sample_weights), _ptr(bufs.unique_rows),
+            _ptr(bufs.run_starts) if want_run_starts else None,
+            _ptr(bufs.sorted_positions) if want_sorted_positions else None, cap, _ptr(bufs.unique_count),
+            _ptr(bufs.workspace), bufs.workspace.numel(), _ptr(dev_status), _stream(stream))
+    _check(rc, "tbe_backward_index")
+    bufs._index_call = (N, int(B), per_sample_weights is not None, want_run_starts)
+    return bufs
+
+
+def tbe_backward_reduce(plan: Plan, grad_out, bufs: BackwardBuffers, kind: int = -1, learning_rate: float = 0.0,
+                        weights=None, eps: float = 0.0, momentum=None, per_sample_weights=None, dev_status=None,
+                        stream=None):
+    """The reduction after tbe_backward_index on the same ``bufs``: row
+    gradients into ``bufs.row_grads`` (kind < 0), or the exact optimizer
+    ``kind`` applied in place on ``weights`` (and ``momentum``)."""
+    import torch
+
+    if getattr(bufs, "_index_call", None) is None:
+        raise TBEError("tbe_backward_reduce needs the BackwardBuffers of a tbe_backward_index call")
+    N, B, weighted, want_run_starts = bufs._index_call
+    if weighted != (per_sample_weights is not None):
+        raise TBEError("per_sample_weights must be given to both calls or to neither")
+    lib = load_library()
+    _need_backward(plan, grad_out, N, B, per_sample_weights, bufs, dev_status)
+    opt = None
+    if kind >= 0:
+        _need_weights(plan, weights)
+        _need(momentum, (torch.float32,), plan.total_rows, "momentum", optional=True)
+        opt = ctypes.byref(Optimizer(int(kind), float(learning_rate), float(eps)))
+    rc = lib.tbe_backward_reduce(plan.handle, opt, _ptr(weights), _ptr(momentum), _ptr(grad_out), N, B,
+                                 _ptr(per_sample_weights), _ptr(bufs.unique_rows),
+                                 _ptr(bufs.run_starts) if want_run_starts else None,
+                                 None if kind >= 0 else _ptr(bufs.row_grads), 0 if kind >= 0 else bufs.row_grads_capacity,
+                                 _ptr(bufs.unique_count), _ptr(bufs.workspace), bufs.workspace.numel(),
+                                 _ptr(dev_status), _stream(stream))
+    _check(rc, "tbe_backward_reduce")
     return bufs
 
 

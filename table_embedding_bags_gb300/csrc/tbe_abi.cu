@@ -442,17 +442,21 @@ size_t tbe_backward_workspace_bytes(const tbe_plan* plan, int32_t B, int64_t N) 
 
 // Shared by tbe_backward and tbe_backward_update: checks and launches the
 // backward; `opt` (may be null) fuses the exact optimizer into the reducer.
+// stages: kBwdIndex and/or kBwdReduce (tbe_backward runs both; the index
+// stages read no grad_out, the reduction no ids or offsets).
 static int backward_call(const tbe_plan* plan, const float* grad_out, IdxPtr indices, int64_t N,
                          IdxPtr offsets, int32_t B, const float* per_sample_weights, int64_t* unique_rows,
                          int32_t* run_starts, int32_t* sorted_positions, float* row_grads,
                          int64_t row_grads_capacity, int64_t* unique_count, void* workspace, size_t workspace_bytes,
                          int32_t* dev_status, void* stream, const tbe_optimizer* opt, void* weights,
-                         float* momentum) {
-  int st = check_common(plan, indices.p, N, offsets.p, B);
+                         float* momentum, int stages = kBwdIndex | kBwdReduce) {
+  const bool index = stages & kBwdIndex, reduce = stages & kBwdReduce;
+  // the reduction alone reads no ids or offsets: check the rest as for a full call
+  int st = check_common(plan, index ? indices.p : (const void*)plan, N, index ? offsets.p : (const void*)plan, B);
   if (st != TBE_OK) return st;
   if (!unique_count || row_grads_capacity < 0) return TBE_ERR_INVALID_ARG;
-  if (N > 0 && (!unique_rows || !grad_out || (!opt && !row_grads && row_grads_capacity > 0)))
-    return TBE_ERR_INVALID_ARG;
+  if (N > 0 && !unique_rows) return TBE_ERR_INVALID_ARG;
+  if (N > 0 && reduce && (!grad_out || (!opt && !row_grads && row_grads_capacity > 0))) return TBE_ERR_INVALID_ARG;
   if ((uintptr_t)grad_out & 15) return TBE_ERR_UNSUPPORTED;
   if ((plan->sumD % 4) != 0) return TBE_ERR_UNSUPPORTED;
   for (int t = 0; t < plan->T; ++t)
@@ -486,7 +490,7 @@ static int backward_call(const tbe_plan* plan, const float* grad_out, IdxPtr ind
   a.momentum = momentum;
   cudaStream_t s = (cudaStream_t)stream;
   trace_begin(s);
-  return launch_backward(*plan, a, s);
+  return launch_backward(*plan, a, s, stages);
 }
 
 int tbe_backward(const tbe_plan* plan, const float* grad_out, const int64_t* indices, int64_t N,
@@ -548,6 +552,40 @@ int tbe_backward_update_i32(const tbe_plan* plan, const tbe_optimizer* opt, void
   return backward_update_call(plan, opt, weights, momentum, grad_out, IdxPtr{indices, 1}, N, IdxPtr{offsets, 1}, B,
                               per_sample_weights, unique_rows, run_starts, sorted_positions, unique_count,
                               workspace, workspace_bytes, dev_status, stream);
+}
+
+int tbe_backward_index(const tbe_plan* plan, const int64_t* indices, int64_t N, const int64_t* offsets, int32_t B,
+                       const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                       int32_t* sorted_positions, int64_t row_grads_capacity, int64_t* unique_count, void* workspace,
+                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return backward_call(plan, nullptr, IdxPtr{indices, 0}, N, IdxPtr{offsets, 0}, B, per_sample_weights, unique_rows,
+                       run_starts, sorted_positions, nullptr, row_grads_capacity, unique_count, workspace,
+                       workspace_bytes, dev_status, stream, nullptr, nullptr, nullptr, kBwdIndex);
+}
+
+int tbe_backward_index_i32(const tbe_plan* plan, const int32_t* indices, int64_t N, const int32_t* offsets,
+                           int32_t B, const float* per_sample_weights, int64_t* unique_rows, int32_t* run_starts,
+                           int32_t* sorted_positions, int64_t row_grads_capacity, int64_t* unique_count,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  return backward_call(plan, nullptr, IdxPtr{indices, 1}, N, IdxPtr{offsets, 1}, B, per_sample_weights, unique_rows,
+                       run_starts, sorted_positions, nullptr, row_grads_capacity, unique_count, workspace,
+                       workspace_bytes, dev_status, stream, nullptr, nullptr, nullptr, kBwdIndex);
+}
+
+int tbe_backward_reduce(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,
+                        const float* grad_out, int64_t N, int32_t B, const float* per_sample_weights,
+                        int64_t* unique_rows, int32_t* run_starts, float* row_grads, int64_t row_grads_capacity,
+                        int64_t* unique_count, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream) {
+  if (opt) {
+    if (!plan || !opt_ok(opt)) return TBE_ERR_INVALID_ARG;
+    if (plan->maxD > 128) return TBE_ERR_UNSUPPORTED;  // a row gradient is one quad per lane of one warp
+    if (N > 0 && (!weights || (opt->kind == TBE_OPT_EXACT_ROWWISE_ADAGRAD && !momentum))) return TBE_ERR_INVALID_ARG;
+    if ((uintptr_t)weights & 15) return TBE_ERR_UNSUPPORTED;
+  }
+  return backward_call(plan, grad_out, IdxPtr{nullptr, 0}, N, IdxPtr{nullptr, 0}, B, per_sample_weights, unique_rows,
+                       run_starts, nullptr, row_grads, row_grads_capacity, unique_count, workspace, workspace_bytes,
+                       dev_status, stream, opt, weights, momentum, kBwdReduce);
 }
 
 int tbe_exact_update(const tbe_plan* plan, const tbe_optimizer* opt, void* weights, float* momentum,

@@ -1683,153 +1683,162 @@ size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N) {
   return make_layout(p, B, N).total;
 }
 
-int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s) {
+// stages: kBwdIndex (memset .. classify: everything that reads only the ids,
+// offsets and per-sample weights) and/or kBwdReduce (the reduction, which
+// reads grad_out); the workspace carries the index stages' results to the
+// reduction, so the two may be launched separately, in order.
+int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages) {
   const int64_t N = a.N;
   if (N == 0) {
-    if (cudaMemsetAsync(a.unique_count, 0, sizeof(int64_t) * (p.T + 1), s) != cudaSuccess) return TBE_ERR_CUDA;
-    if (a.run_starts && cudaMemsetAsync(a.run_starts, 0, sizeof(int32_t), s) != cudaSuccess) return TBE_ERR_CUDA;
+    if (stages & kBwdIndex) {
+      if (cudaMemsetAsync(a.unique_count, 0, sizeof(int64_t) * (p.T + 1), s) != cudaSuccess) return TBE_ERR_CUDA;
+      if (a.run_starts && cudaMemsetAsync(a.run_starts, 0, sizeof(int32_t), s) != cudaSuccess) return TBE_ERR_CUDA;
+    }
     trace_mark(s, "bwd_empty");
     return TBE_OK;
   }
   const Layout L = make_layout(p, a.B, N);
   void* ws = a.workspace;
-  if (cudaMemsetAsync(at<char>(ws, L.zero_begin), 0, L.zero_end - L.zero_begin, s) != cudaSuccess)
-    return TBE_ERR_CUDA;
-  trace_mark(s, "bwd_memset");
   uint32_t* counters = at<uint32_t>(ws, L.counters);
   const uint32_t sentinel = (uint32_t)p.total_rows;
+  int32_t* run_starts = a.run_starts ? a.run_starts : at<int32_t>(ws, L.run_starts);
+  const Tuning& tu = tuning();
+  unsigned long long* long_counter = reinterpret_cast<unsigned long long*>(counters + kCntLong * kCntStride);
+  if (stages & kBwdIndex) {
+    if (cudaMemsetAsync(at<char>(ws, L.zero_begin), 0, L.zero_end - L.zero_begin, s) != cudaSuccess)
+      return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_memset");
 
-  LinArgs la;
-  la.indices = a.indices;
-  la.offsets = a.offsets;
-  la.meta = a.meta;
-  la.keys = at<uint32_t>(ws, L.keys_a);
-  la.bag_of = at<int32_t>(ws, L.bag_of);
-  la.hist = at<uint32_t>(ws, L.hist);
-  la.counters = counters;
-  la.status = a.status;
-  la.zero = at<char>(ws, L.lin_zero_begin);
-  la.zero_words4 = (int64_t)((L.lin_zero_end - L.lin_zero_begin) / 16);
-  la.N = N;
-  la.T = a.T;
-  la.B = a.B;
-  la.npass = L.npass;
-  la.sentinel = sentinel;
-  la.seg_dbits = L.seg_dbits;
-  la.seg_hist = at<uint32_t>(ws, L.seg_hist);
-  la.seg_inv = at<uint32_t>(ws, L.seg_inv);
-  if (L.small)
-    linearize_kernel<4><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
-  else
-    linearize_kernel<8><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
-  if (check_launch()) return TBE_ERR_CUDA;
-  trace_mark(s, "bwd_linearize");
+    LinArgs la;
+    la.indices = a.indices;
+    la.offsets = a.offsets;
+    la.meta = a.meta;
+    la.keys = at<uint32_t>(ws, L.keys_a);
+    la.bag_of = at<int32_t>(ws, L.bag_of);
+    la.hist = at<uint32_t>(ws, L.hist);
+    la.counters = counters;
+    la.status = a.status;
+    la.zero = at<char>(ws, L.lin_zero_begin);
+    la.zero_words4 = (int64_t)((L.lin_zero_end - L.lin_zero_begin) / 16);
+    la.N = N;
+    la.T = a.T;
+    la.B = a.B;
+    la.npass = L.npass;
+    la.sentinel = sentinel;
+    la.seg_dbits = L.seg_dbits;
+    la.seg_hist = at<uint32_t>(ws, L.seg_hist);
+    la.seg_inv = at<uint32_t>(ws, L.seg_inv);
+    if (L.small)
+      linearize_kernel<4><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
+    else
+      linearize_kernel<8><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
+    if (check_launch()) return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_linearize");
 
-  int32_t* final_pos = a.sorted_positions ? a.sorted_positions : at<int32_t>(ws, L.vals_b);
-  uint32_t* kin = at<uint32_t>(ws, L.keys_a);
-  uint32_t* kout = at<uint32_t>(ws, L.keys_b);
-  int32_t* vin = nullptr;
-  int32_t* vbuf[2] = {at<int32_t>(ws, L.vals_a), at<int32_t>(ws, L.vals_b)};
-  for (int pass = 0; pass < L.npass; ++pass) {
-    const bool last = pass == L.npass - 1;
-    int32_t* vout = last ? final_pos : vbuf[pass & 1];
-    if (!last && vout == final_pos) vout = vbuf[(pass + 1) & 1];
-    if (vout == vin) vout = (vin == vbuf[0]) ? vbuf[1] : vbuf[0];
-    if (L.seg_dbits > 0) {
-      SegSortArgs ga;
-      ga.keys_in = kin;
-      ga.vals_in = vin;
-      ga.keys_out = kout;
-      ga.vals_out = vout;
-      ga.hist = at<uint32_t>(ws, L.seg_hist);
-      ga.inv = at<uint32_t>(ws, L.seg_inv);
-      ga.offsets = a.offsets;
-      ga.meta = a.meta;
-      ga.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * kSegBk;
-      ga.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
-      ga.status = a.status;
-      ga.bag_of = at<int32_t>(ws, L.bag_of);
-      ga.psw = a.psw;
-      ga.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
-      ga.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
-      ga.N = (int32_t)N;
-      ga.T = p.T;
-      ga.B = a.B;
-      ga.pass = pass;
-      ga.dbits = L.seg_dbits;
-      ga.last = last ? 1 : 0;
-      ga.sentinel = sentinel;
-      if (launch_pdl(L.small ? seg_sort_pass_kernel<6> : seg_sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s,
-                     ga))
+    int32_t* final_pos = a.sorted_positions ? a.sorted_positions : at<int32_t>(ws, L.vals_b);
+    uint32_t* kin = at<uint32_t>(ws, L.keys_a);
+    uint32_t* kout = at<uint32_t>(ws, L.keys_b);
+    int32_t* vin = nullptr;
+    int32_t* vbuf[2] = {at<int32_t>(ws, L.vals_a), at<int32_t>(ws, L.vals_b)};
+    for (int pass = 0; pass < L.npass; ++pass) {
+      const bool last = pass == L.npass - 1;
+      int32_t* vout = last ? final_pos : vbuf[pass & 1];
+      if (!last && vout == final_pos) vout = vbuf[(pass + 1) & 1];
+      if (vout == vin) vout = (vin == vbuf[0]) ? vbuf[1] : vbuf[0];
+      if (L.seg_dbits > 0) {
+        SegSortArgs ga;
+        ga.keys_in = kin;
+        ga.vals_in = vin;
+        ga.keys_out = kout;
+        ga.vals_out = vout;
+        ga.hist = at<uint32_t>(ws, L.seg_hist);
+        ga.inv = at<uint32_t>(ws, L.seg_inv);
+        ga.offsets = a.offsets;
+        ga.meta = a.meta;
+        ga.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * kSegBk;
+        ga.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
+        ga.status = a.status;
+        ga.bag_of = at<int32_t>(ws, L.bag_of);
+        ga.psw = a.psw;
+        ga.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
+        ga.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+        ga.N = (int32_t)N;
+        ga.T = p.T;
+        ga.B = a.B;
+        ga.pass = pass;
+        ga.dbits = L.seg_dbits;
+        ga.last = last ? 1 : 0;
+        ga.sentinel = sentinel;
+        if (launch_pdl(L.small ? seg_sort_pass_kernel<6> : seg_sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s,
+                       ga))
+          return TBE_ERR_CUDA;
+        trace_mark(s, "bwd_sort_pass");
+        std::swap(kin, kout);
+        vin = vout;
+        continue;
+      }
+      SortArgs sa;
+      sa.keys_in = kin;
+      sa.vals_in = vin;
+      sa.keys_out = kout;
+      sa.vals_out = vout;
+      sa.hist = at<uint32_t>(ws, L.hist) + 256 * pass;
+      sa.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * 256;
+      sa.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
+      sa.status = a.status;
+      sa.bag_of = at<int32_t>(ws, L.bag_of);
+      sa.psw = a.psw;
+      sa.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
+      sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+      sa.N = (int32_t)N;
+      sa.shift = 8 * pass;
+      if (launch_pdl(L.small ? sort_pass_kernel<6> : sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s, sa))
         return TBE_ERR_CUDA;
       trace_mark(s, "bwd_sort_pass");
       std::swap(kin, kout);
       vin = vout;
-      continue;
     }
-    SortArgs sa;
-    sa.keys_in = kin;
-    sa.vals_in = vin;
-    sa.keys_out = kout;
-    sa.vals_out = vout;
-    sa.hist = at<uint32_t>(ws, L.hist) + 256 * pass;
-    sa.lookback = at<uint32_t>(ws, L.sort_lookback) + (size_t)pass * L.sort_ntiles * 256;
-    sa.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
-    sa.status = a.status;
-    sa.bag_of = at<int32_t>(ws, L.bag_of);
-    sa.psw = a.psw;
-    sa.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
-    sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
-    sa.N = (int32_t)N;
-    sa.shift = 8 * pass;
-    if (launch_pdl(L.small ? sort_pass_kernel<6> : sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s, sa))
-      return TBE_ERR_CUDA;
-    trace_mark(s, "bwd_sort_pass");
-    std::swap(kin, kout);
-    vin = vout;
+    const uint32_t* sorted_keys = kin;
+
+    RleArgs ra;
+    ra.keys = sorted_keys;
+    ra.meta = a.meta;
+    ra.unique_count = a.unique_count;
+    ra.T = a.T;
+    ra.unique_rows = a.unique_rows;
+    ra.run_starts = run_starts;
+    ra.run_table = at<int32_t>(ws, L.run_table);
+    ra.lookback = at<uint32_t>(ws, L.rle_lookback);
+    ra.tile_counter = at<uint32_t>(ws, L.rle_tile);
+    ra.counters = counters;
+    ra.status = a.status;
+    ra.N = (int32_t)N;
+    ra.ntiles = L.rle_ntiles;
+    ra.sentinel = sentinel;
+    if (launch_pdl(L.small ? rle_kernel<4> : rle_kernel<8>, L.rle_ntiles, kRleThreads, s, ra)) return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_rle");
+
+    ClsArgs ca;
+    ca.unique_rows = a.unique_rows;
+    ca.run_starts = run_starts;
+    ca.meta = a.meta;
+    ca.long_list = at<int4>(ws, L.long_list);
+    ca.long_counter = long_counter;
+    ca.counters = counters;
+    ca.unique_count = a.unique_count;
+    ca.gofs = at<int64_t>(ws, L.gofs);
+    ca.status = a.status;
+    ca.capacity = a.row_grads_capacity;
+    ca.T = a.T;
+    ca.tau = tu.long_run_threshold;
+    ca.chunk = L.chunk;
+    ca.item_lookups = L.item_lookups;
+    ca.sub_list = at<int2>(ws, L.sub_list);
+    const int cls_blocks = (int)std::min<int64_t>((N + kClsThreads - 1) / kClsThreads, 4 * sm_count());
+    if (launch_pdl(classify_kernel, std::max(cls_blocks, 1), kClsThreads, s, ca)) return TBE_ERR_CUDA;
+    trace_mark(s, "bwd_classify");
   }
-  const uint32_t* sorted_keys = kin;
-
-  int32_t* run_starts = a.run_starts ? a.run_starts : at<int32_t>(ws, L.run_starts);
-  RleArgs ra;
-  ra.keys = sorted_keys;
-  ra.meta = a.meta;
-  ra.unique_count = a.unique_count;
-  ra.T = a.T;
-  ra.unique_rows = a.unique_rows;
-  ra.run_starts = run_starts;
-  ra.run_table = at<int32_t>(ws, L.run_table);
-  ra.lookback = at<uint32_t>(ws, L.rle_lookback);
-  ra.tile_counter = at<uint32_t>(ws, L.rle_tile);
-  ra.counters = counters;
-  ra.status = a.status;
-  ra.N = (int32_t)N;
-  ra.ntiles = L.rle_ntiles;
-  ra.sentinel = sentinel;
-  if (launch_pdl(L.small ? rle_kernel<4> : rle_kernel<8>, L.rle_ntiles, kRleThreads, s, ra)) return TBE_ERR_CUDA;
-  trace_mark(s, "bwd_rle");
-
-  const Tuning& tu = tuning();
-  unsigned long long* long_counter = reinterpret_cast<unsigned long long*>(counters + kCntLong * kCntStride);
-  ClsArgs ca;
-  ca.unique_rows = a.unique_rows;
-  ca.run_starts = run_starts;
-  ca.meta = a.meta;
-  ca.long_list = at<int4>(ws, L.long_list);
-  ca.long_counter = long_counter;
-  ca.counters = counters;
-  ca.unique_count = a.unique_count;
-  ca.gofs = at<int64_t>(ws, L.gofs);
-  ca.status = a.status;
-  ca.capacity = a.row_grads_capacity;
-  ca.T = a.T;
-  ca.tau = tu.long_run_threshold;
-  ca.chunk = L.chunk;
-  ca.item_lookups = L.item_lookups;
-  ca.sub_list = at<int2>(ws, L.sub_list);
-  const int cls_blocks = (int)std::min<int64_t>((N + kClsThreads - 1) / kClsThreads, 4 * sm_count());
-  if (launch_pdl(classify_kernel, std::max(cls_blocks, 1), kClsThreads, s, ca)) return TBE_ERR_CUDA;
-  trace_mark(s, "bwd_classify");
+  if (!(stages & kBwdReduce)) return TBE_OK;
 
   RedArgs rd;
   rd.grad_out = a.grad_out;

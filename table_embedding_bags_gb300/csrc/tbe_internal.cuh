@@ -435,7 +435,9 @@ struct BwdArgs {
 };
 
 size_t backward_workspace_bytes(const Plan& p, int32_t B, int64_t N);
-int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s);
+constexpr int kBwdIndex = 1;   // backward stages that read only ids, offsets and weights
+constexpr int kBwdReduce = 2;  // the reduction (reads grad_out)
+int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages = kBwdIndex | kBwdReduce);
 
 struct UpdArgs {
   uint8_t* weights;
