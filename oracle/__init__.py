@@ -73,6 +73,8 @@ def load(path: str | None = None):
     lib.orc_histogram_counts.argtypes = [i32, i32, i32, i64, P, i64, P, P]
     lib.orc_counts_times_table.restype = None
     lib.orc_counts_times_table.argtypes = [i32, i64, i32, P, P, i64, i32, P]
+    lib.orc_scale_by_bag_length.restype = None
+    lib.orc_scale_by_bag_length.argtypes = [i32, i32, P, P, P]
     lib.orc_backward_indexing.restype = ctypes.c_int
     lib.orc_backward_indexing.argtypes = [i32, i32, P, P, i64, P, P, P, P, P, P]
     lib.orc_backward_values.restype = ctypes.c_int
@@ -156,9 +158,32 @@ def forward(layout: dict, weights, indices, offsets, B: int, per_sample_weights=
                          ind.shape[0], _p(off), _p(psw), _p(g), g.shape[0], _p(pos), _p(s), _p(a),
                          nthreads)
     s, a = s[:n_out], a[:n_out]
+    mean = int(layout.get("pooling", POOL_SUM)) == POOL_MEAN
     if bags is None:
-        return st, s.reshape(B, sumD), a.reshape(B, sumD)
+        s, a = s.reshape(B, sumD), a.reshape(B, sumD)
+        if mean:
+            s, a = scale_by_bag_length(T, B, doff, off, s, lib), scale_by_bag_length(T, B, doff, off, a, lib)
+        return st, s, a
+    if mean:  # scale each listed bag's block by its length
+        lens = (off[g + 1] - off[g]).astype(np.float64)
+        for k in range(g.size):
+            if lens[k] > 0:
+                w_k = int(D[g[k] // max(B, 1)])
+                s[pos[k]:pos[k] + w_k] /= lens[k]
+                a[pos[k]:pos[k] + w_k] /= lens[k]
     return st, s, a, pos
+
+
+POOL_SUM, POOL_MEAN = 0, 1
+
+
+def scale_by_bag_length(T, B, D_offsets, offsets, values, lib=None):
+    """Mean pooling: each bag's block of a [B, sum D] float64 array divided by
+    the bag's number of lookups (orc_scale_by_bag_length); returns a copy."""
+    lib = lib or load()
+    v = np.array(values, dtype=np.float64, order="C", copy=True)
+    lib.orc_scale_by_bag_length(int(T), int(B), _p(_c(D_offsets, np.int32)), _p(_c(offsets, np.int64)), _p(v))
+    return v
 
 
 def histogram_counts(T, B, t, rows_t, indices, offsets, lib=None):
@@ -214,7 +239,9 @@ def backward_values(layout: dict, offsets, B: int, grad_out, idx: dict, per_samp
     tw = _c(layout.get("table_weighted"), np.uint8)
     off = _c(offsets, np.int64)
     psw = _c(per_sample_weights, np.float32)
-    G = _c(grad_out, np.float32)
+    G = _c(np.asarray(grad_out, np.float32), np.float64)  # fp32 gradients, exactly in double
+    if int(layout.get("pooling", POOL_SUM)) == POOL_MEAN:  # the mean's backward: the sum's on G / L
+        G = scale_by_bag_length(T, B, doff, off, G, lib)
     ur = _c(idx["unique_rows"], np.int64)
     rs = _c(idx["run_starts"], np.int32)
     sp = _c(idx["sorted_pos"], np.int32)

@@ -235,6 +235,26 @@ int orc_histogram_counts(int32_t T, int32_t B, int32_t t, int64_t rows_t, const 
   return bad_index ? ORC_BAD_INDEX : 0;
 }
 
+/* Mean pooling (reading: the page pools "usually by summing"; the other
+ * pooling mode, the mean, is the sum divided by the bag's number of lookups,
+ * L_{t,b} = offsets[t*B+b+1] - offsets[t*B+b]): divides each bag's block of
+ * a [B, sum D] array -- a pooled output, its absolute-term sums, or the
+ * output gradient before the backward -- by L_{t,b}.  An empty bag's block
+ * is left as it is (it holds zeros, and no lookup reads its gradient).  The
+ * backward of the mean is the backward of the sum on the scaled gradient:
+ * each lookup of bag (t,b) receives (w_i / L_{t,b}) * grad_out[b]. */
+void orc_scale_by_bag_length(int32_t T, int32_t B, const int32_t* D_offsets, const int64_t* offsets,
+                             double* values /* [B, sum D] */) {
+  const int32_t sumD = D_offsets[T];
+  for (int32_t t = 0; t < T; ++t)
+    for (int32_t b = 0; b < B; ++b) {
+      const int64_t g = (int64_t)t * B + b;
+      const int64_t len = offsets[g + 1] - offsets[g];
+      if (len <= 0) continue;
+      for (int32_t c = D_offsets[t]; c < D_offsets[t + 1]; ++c) values[(int64_t)b * sumD + c] /= (double)len;
+    }
+}
+
 /* out[b, c] = sum_r cnt[b][r] * W_t[r, c]  (counts times table) */
 void orc_counts_times_table(int32_t B, int64_t rows_t, int32_t D, const int32_t* counts,
                             const uint8_t* weights, int64_t w_off, int32_t dt, double* out) {
@@ -331,7 +351,7 @@ int orc_backward_indexing(int32_t T, int32_t B, const int64_t* table_row_base,
 int orc_backward_values(int32_t T, int32_t B, const int64_t* table_row_base,
                         const int32_t* D_offsets, const uint8_t* table_weighted,
                         const int64_t* offsets, int64_t N, const float* per_sample_weights,
-                        const float* grad_out, const int64_t* unique_rows,
+                        const double* grad_out, const int64_t* unique_rows,
                         const int32_t* run_starts, const int32_t* sorted_pos, const int64_t* runs,
                         int64_t n_runs, const int64_t* rg_pos, double* rg_sum, double* rg_abs,
                         int32_t nthreads) {
@@ -364,7 +384,7 @@ int orc_backward_values(int32_t T, int32_t B, const int64_t* table_row_base,
       if (g / B != t) { bad = 1; continue; } /* would mean an inconsistent key */
       int64_t b = g % B;
       double w = weighted ? (double)per_sample_weights[pos] : 1.0;
-      const float* grow = grad_out + b * sumD + D_offsets[t];
+      const double* grow = grad_out + b * sumD + D_offsets[t];
       for (int32_t c = 0; c < D; ++c) {
         double term = w * (double)grow[c];
         s[c] += term;

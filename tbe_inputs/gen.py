@@ -48,6 +48,7 @@ class TBEProblem:
     weight_dist: list = field(default_factory=list)  # per table: ("usym", a) or ("normal", std)
     host_tables: dict = field(default_factory=dict)  # t -> raw table bytes made on the host
     recipe: str = ""
+    pooling: int = 0  # 0 sum, 1 mean (each bag's sum divided by its number of lookups)
 
     # ---- derived layout -------------------------------------------------
     @property
@@ -98,6 +99,7 @@ class TBEProblem:
             weights_dtype=self.weights_dtype.astype(np.int32),
             table_weighted=self.table_weighted.astype(np.uint8),
             out_dtype=self.out_dtype,
+            pooling=self.pooling,
         )
 
 
@@ -404,7 +406,7 @@ def make_config(name: str, B: int | None = None, rows_scale: float = 1.0, batch:
 
 
 def make_problem(T, B, rows, D, weights_dtype, out_dtype, lengths, ids, psw=None, grad_out=None,
-                 table_weighted=None, seed=7, host_tables=None, name="custom") -> TBEProblem:
+                 table_weighted=None, seed=7, host_tables=None, name="custom", pooling=0) -> TBEProblem:
     """Assemble a problem from explicit per-table lengths [T,B] and id lists."""
     rows = np.asarray(rows, np.int64)
     D = np.asarray(D, np.int32)
@@ -419,4 +421,4 @@ def make_problem(T, B, rows, D, weights_dtype, out_dtype, lengths, ids, psw=None
                       per_sample_weights=None if psw is None else np.asarray(psw, np.float32),
                       grad_out=None if grad_out is None else np.asarray(grad_out, np.float32),
                       weight_seed=seed, weight_dist=[("usym", 0.05)] * T,
-                      host_tables=dict(host_tables or {}), recipe="explicit")
+                      host_tables=dict(host_tables or {}), recipe="explicit", pooling=int(pooling))

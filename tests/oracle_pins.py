@@ -19,6 +19,11 @@ AssertionError on a mismatch.  What pins what:
   search.
 * ``pin_special_cases`` -- all-empty batch, single-id bags, one id repeated
   n times, out-of-range ids, broken offsets.
+* ``pin_mean_hand``     -- mean pooling worked by hand: each bag's mean of its
+  rows, an empty bag 0, and a lookup of bag b receiving grad_out[b] / L_b.
+* ``pin_mean_dense``    -- mean pooling in the textbook form: with M_t =
+  diag(1 / L_b) A_t (empty bags: a zero row), the forward is M_t @ W_t and
+  the table gradient M_t^T @ G_t (numpy float64 matmul).
 * ``pin_optimizer_hand`` -- exact SGD and row-wise Adagrad steps worked by
   hand (tests/golden/optimizer_example.json), with momentum carried over
   from an earlier step and with and without eps.
@@ -153,6 +158,58 @@ def pin_dense_onehot(lib, trials=40, seed=5):
             for j, u in enumerate(range(int(uc[t]), int(uc[t + 1]))):
                 got = rg[rpos[u]: rpos[u] + Dt]
                 np.testing.assert_allclose(got, dense[occurring[j]], rtol=1e-12, atol=1e-12)
+
+
+def pin_mean_hand(lib):
+    """T=1, three rows of D=2, table [[1,2],[3,4],[5,6]] (fp32); bags [0,2],
+    [1,1,2] and []; grad_out rows (1,1), (3,3), (7,7).  By hand: outputs
+    (3,4), (11/3, 14/3), (0,0); row gradients row0 = (1,1)/2 = (0.5,0.5),
+    row1 = 2*(3,3)/3 = (2,2), row2 = (1,1)/2 + (3,3)/3 = (1.5,1.5)."""
+    import torch
+
+    table = torch.tensor([[1.0, 2.0], [3.0, 4.0], [5.0, 6.0]], dtype=torch.float32)
+    G = np.array([[1.0, 1.0], [3.0, 3.0], [7.0, 7.0]], np.float32)
+    p = make_problem(1, 3, rows=[3], D=[2], weights_dtype=[DT_F32], out_dtype=DT_F32, lengths=[[2, 3, 0]],
+                     ids=[[0, 2, 1, 1, 2]], grad_out=G, host_tables={0: table}, pooling=1)
+    w = materialize_weights(p)
+    st, out, _ = oracle.problem_forward(p, w, lib=lib)
+    assert st == 0
+    np.testing.assert_allclose(out, [[3.0, 4.0], [11 / 3, 14 / 3], [0.0, 0.0]], rtol=1e-15)
+    idx, st2, rg, _, rpos = oracle.problem_backward(p, lib=lib)
+    assert st2 == 0
+    np.testing.assert_array_equal(idx["unique_rows"], [0, 1, 2])
+    np.testing.assert_allclose(rg.reshape(3, 2), [[0.5, 0.5], [2.0, 2.0], [1.5, 1.5]], rtol=1e-15)
+
+
+def pin_mean_dense(lib, trials=30, seed=13):
+    rng = np.random.default_rng(seed)
+    for k in range(trials):
+        T = int(rng.integers(1, 5))
+        B = int(rng.integers(1, 6))
+        p = _random_problem(rng, T, B, [DT_F32, DT_F16, DT_BF16], bool(k % 2))
+        p.pooling = 1
+        w = materialize_weights(p)
+        st, out, _ = oracle.problem_forward(p, w, lib=lib)
+        idx, st2, rg, _, rpos = oracle.problem_backward(p, lib=lib)
+        assert st == 0 and st2 == 0
+        doff, trb, uc = p.D_offsets, p.table_row_base, idx["unique_count"]
+        for t in range(T):
+            R = int(p.rows[t])
+            M = np.zeros((B, R), np.float64)
+            for b in range(B):
+                g = t * B + b
+                L = int(p.offsets[g + 1] - p.offsets[g])
+                for i in range(int(p.offsets[g]), int(p.offsets[g + 1])):
+                    wi = 1.0
+                    if p.per_sample_weights is not None and p.table_weighted[t]:
+                        wi = float(p.per_sample_weights[i])
+                    M[b, p.indices[i]] += wi / L
+            np.testing.assert_allclose(out[:, doff[t]: doff[t + 1]], M @ _table_f64(p, w, t), rtol=1e-12, atol=1e-12)
+            dense = M.T @ p.grad_out[:, doff[t]: doff[t + 1]].astype(np.float64)
+            Dt = int(p.D[t])
+            for u in range(int(uc[t]), int(uc[t + 1])):
+                r = int(idx["unique_rows"][u] - trb[t])
+                np.testing.assert_allclose(rg[rpos[u]: rpos[u] + Dt], dense[r], rtol=1e-12, atol=1e-12)
 
 
 def pin_invariants(lib, trials=30, seed=11):
@@ -432,4 +489,4 @@ def pin_optimizer_invariants(lib, trials=20, seed=23):
 
 
 ALL_PINS = [pin_hand_example, pin_dense_onehot, pin_invariants, pin_sort_vs_numpy, pin_formats,
-            pin_special_cases, pin_optimizer_hand, pin_optimizer_invariants]
+            pin_special_cases, pin_mean_hand, pin_mean_dense, pin_optimizer_hand, pin_optimizer_invariants]

@@ -54,6 +54,10 @@ MUTANTS = {
     "adagrad_rms_of_update": ("step = lr / (sqrt(m) + eps);", "step = lr / (m + eps);"),
     "update_sign": ("table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) - step * g[c];",
                     "table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) + step * g[c];"),
+    "mean_divides_by_len_plus_one": ("values[(int64_t)b * sumD + c] /= (double)len;",
+                                     "values[(int64_t)b * sumD + c] /= (double)(len + 1);"),
+    "mean_scales_first_column_only": ("for (int32_t c = D_offsets[t]; c < D_offsets[t + 1]; ++c) values",
+                                      "for (int32_t c = D_offsets[t]; c < D_offsets[t] + 1; ++c) values"),
     "update_reads_first_row": ("table_elem(weights, weights_offsets[t], weights_dtype[t], D, id, c) - step * g[c];",
                                "table_elem(weights, weights_offsets[t], weights_dtype[t], D, 0, c) - step * g[c];"),
 }
