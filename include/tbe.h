@@ -78,6 +78,10 @@ extern "C" {
 #define TBE_PATH_GATHER 1    /* always the gather kernel                   */
 #define TBE_PATH_HISTOGRAM 2 /* histogram path; TBE_ERR_UNSUPPORTED if not eligible */
 
+/* ---- pooling ------------------------------------------------------------- */
+#define TBE_POOL_SUM 0  /* a bag's output is the (weighted) sum of its rows     */
+#define TBE_POOL_MEAN 1 /* ... divided by the bag's number of lookups (empty: 0) */
+
 /*
  * Description of the packed tables (all HOST arrays; copied by
  * tbe_plan_create, so they may be freed afterwards).
@@ -93,6 +97,10 @@ extern "C" {
  *   table_weighted   : [T] 1 if table t uses per_sample_weights; NULL means
  *                      every table does when per_sample_weights is given
  *   out_dtype        : forward output element type
+ *   pooling          : TBE_POOL_SUM or TBE_POOL_MEAN.  Mean pooling divides
+ *                      each bag's fp32 sum by its number of lookups L (one
+ *                      IEEE division; an empty bag stays 0); its backward
+ *                      gives each lookup (w_i / L) * grad_out[b]
  */
 typedef struct tbe_layout {
   int32_t T;
@@ -102,6 +110,7 @@ typedef struct tbe_layout {
   const int32_t* weights_dtype;
   const uint8_t* table_weighted;
   int32_t out_dtype;
+  int32_t pooling;
 } tbe_layout;
 
 /* Opaque plan: validated layout, packed per-table metadata and kernel

@@ -22,6 +22,7 @@ TBE_OK, TBE_ERR_INVALID_ARG, TBE_ERR_UNSUPPORTED, TBE_ERR_CUDA, TBE_ERR_WORKSPAC
 TBE_DEV_BAD_INDEX, TBE_DEV_BAD_OFFSETS, TBE_DEV_TIMEOUT, TBE_DEV_CAPACITY = 1, 2, 4, 8
 TBE_F32, TBE_F16, TBE_BF16 = 0, 1, 2
 TBE_PATH_AUTO, TBE_PATH_GATHER, TBE_PATH_HISTOGRAM = 0, 1, 2
+TBE_POOL_SUM, TBE_POOL_MEAN = 0, 1
 TBE_MAX_TABLES = 4096
 TBE_OPT_EXACT_SGD, TBE_OPT_EXACT_ROWWISE_ADAGRAD = 0, 1
 
@@ -44,7 +45,7 @@ class TBEError(RuntimeError):
 class _Layout(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("table_row_base", ctypes.c_void_p), ("D_offsets", ctypes.c_void_p),
                 ("weights_offsets", ctypes.c_void_p), ("weights_dtype", ctypes.c_void_p),
-                ("table_weighted", ctypes.c_void_p), ("out_dtype", ctypes.c_int32)]
+                ("table_weighted", ctypes.c_void_p), ("out_dtype", ctypes.c_int32), ("pooling", ctypes.c_int32)]
 
 
 class Tuning(ctypes.Structure):
@@ -191,7 +192,7 @@ class Plan:
     """A validated table layout with its packed metadata on the device."""
 
     def __init__(self, T, table_row_base, D_offsets, weights_offsets, weights_dtype, out_dtype,
-                 table_weighted=None, device="cuda", stream=None):
+                 table_weighted=None, device="cuda", stream=None, pooling=TBE_POOL_SUM):
         import torch
 
         lib = load_library()
@@ -202,6 +203,7 @@ class Plan:
         self.weights_dtype = _np(weights_dtype, np.int32)
         self.table_weighted = None if table_weighted is None else _np(table_weighted, np.uint8)
         self.out_dtype = int(out_dtype)
+        self.pooling = int(pooling)
         self.sumD = int(self.D_offsets[-1])
         self.D = np.diff(self.D_offsets).astype(np.int64)
         esz = np.array([{TBE_F32: 4, TBE_F16: 2, TBE_BF16: 2}.get(int(d), 4) for d in self.weights_dtype], np.int64)
@@ -215,7 +217,7 @@ class Plan:
         L = _Layout(self.T, self.table_row_base.ctypes.data, self.D_offsets.ctypes.data,
                     self.weights_offsets.ctypes.data, self.weights_dtype.ctypes.data,
                     None if self.table_weighted is None else self.table_weighted.ctypes.data,
-                    self.out_dtype)
+                    self.out_dtype, self.pooling)
         h = ctypes.c_void_p()
         with torch.cuda.device(self.dev_meta.device):
             _check(lib.tbe_plan_create(ctypes.byref(L), _ptr(self.dev_meta), nbytes, _stream(stream),
@@ -226,7 +228,8 @@ class Plan:
     def from_problem(cls, p, device="cuda"):
         lay = p.layout_arrays()
         return cls(lay["T"], lay["table_row_base"], lay["D_offsets"], lay["weights_offsets"],
-                   lay["weights_dtype"], lay["out_dtype"], lay["table_weighted"], device=device)
+                   lay["weights_dtype"], lay["out_dtype"], lay["table_weighted"], device=device,
+                   pooling=lay.get("pooling", TBE_POOL_SUM))
 
     @property
     def handle(self):

@@ -228,6 +228,7 @@ int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, 
   if (!L->table_row_base || !L->D_offsets || !L->weights_offsets || !L->weights_dtype)
     return TBE_ERR_INVALID_ARG;
   if (L->out_dtype < TBE_F32 || L->out_dtype > TBE_BF16) return TBE_ERR_INVALID_ARG;
+  if (L->pooling != TBE_POOL_SUM && L->pooling != TBE_POOL_MEAN) return TBE_ERR_INVALID_ARG;
   if (dev_meta_bytes < tbe_plan_device_bytes(T) || ((uintptr_t)dev_meta & 15)) return TBE_ERR_INVALID_ARG;
   if (L->table_row_base[0] != 0 || L->D_offsets[0] != 0) return TBE_ERR_INVALID_ARG;
 
@@ -277,6 +278,7 @@ int tbe_plan_create(const tbe_layout* L, void* dev_meta, size_t dev_meta_bytes, 
   p->hmeta[T].row_base = total_rows;
   p->T = T;
   p->out_dtype = L->out_dtype;
+  p->pooling = L->pooling;
   p->sumD = L->D_offsets[T];
   p->maxD = maxD;
   p->total_rows = total_rows;
@@ -377,6 +379,7 @@ static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indice
   a.out_vec_ok = plan->out_vec_ok && (((uintptr_t)out & 15) == 0);
   a.lpr_max = g_tuning.fwd_lanes_per_row;
   a.balance = plan->uniform ? 0 : 1;
+  a.mean = plan->pooling == TBE_POOL_MEAN;
   bool hist = false;
   if (path == TBE_PATH_HISTOGRAM) {
     if (!hist_eligible(plan)) return TBE_ERR_UNSUPPORTED;

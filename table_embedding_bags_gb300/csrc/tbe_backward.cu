@@ -177,7 +177,8 @@ __device__ __forceinline__ int32_t table_of_row(const TableMeta* meta, int32_t T
 // workspace layout
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t keys_a, keys_b, vals_a, vals_b, bag_of, bag_sorted, psw_sorted, run_starts, run_table, long_list, sub_list, gofs, partials;
+  size_t keys_a, keys_b, vals_a, vals_b, bag_of, bag_sorted, psw_sorted, coef, run_starts, run_table, long_list, sub_list,
+      gofs, partials;
   size_t zero_begin, hist, sort_tiles, rle_tile, counters, zero_end;
   size_t lin_zero_begin, sort_lookback, rle_lookback, combine, lin_zero_end;
   size_t total;
@@ -245,6 +246,7 @@ Layout make_layout(const Plan& p, int32_t B, int64_t N) {
   L.bag_of = take(4 * (size_t)N);
   L.bag_sorted = take(4 * (size_t)N);
   L.psw_sorted = take(4 * (size_t)N);
+  L.coef = take(p.pooling == TBE_POOL_MEAN ? 4 * (size_t)N : 0);
   L.run_starts = take(4 * (size_t)(N + 1));
   L.run_table = take(4 * (size_t)N);
   L.long_list = take(16 * (size_t)L.chunk_cap);  // one record per chunk
@@ -295,6 +297,9 @@ struct LinArgs {
   int32_t seg_dbits;
   uint32_t* seg_hist;  // [T][2][kSegBk]
   uint32_t* seg_inv;   // [T] ids outside their table
+  // mean pooling: coef[i] = (weight of lookup i, or 1) / (its bag's lookups)
+  const float* psw;
+  float* coef;         // null: sum pooling
 };
 
 // largest g in [lo, hi] with offsets[g] <= pos (global memory)
@@ -388,6 +393,11 @@ __global__ void __launch_bounds__(kLinThreads) linearize_kernel(const LinArgs a)
     }
     const int32_t t = g / a.B;
     const int32_t b = g - t * a.B;
+    if (a.coef) {  // mean pooling: the lookup's share of its bag
+      const int64_t len = a.offsets.ldg(g + 1) - a.offsets.ldg(g);
+      const float w = (a.psw && __ldg(&a.meta[t].weighted)) ? __ldg(a.psw + i) : 1.f;
+      a.coef[i] = len > 0 ? __fdiv_rn(w, (float)len) : 0.f;
+    }
     const int32_t rows = __ldg(&a.meta[t].rows);
     const bool valid = id[q] < (uint64_t)rows;
     if (!valid) { bad = 1; ++invalid; }
@@ -1156,6 +1166,7 @@ struct RedArgs {
   const TableMeta* meta;
   const int32_t* bag_sorted;  // bag sample index of every sorted lookup
   const float* psw_sorted;    // weight of every sorted lookup (null: unweighted)
+  int32_t coef_all;           // psw_sorted holds a coefficient for every table's lookups (mean pooling)
   const int64_t* unique_rows;
   const int32_t* run_starts;
   const int32_t* run_table;
@@ -1200,7 +1211,7 @@ __device__ __forceinline__ RunInfo run_info(const RedArgs& a, int32_t u) {
   r.t = t;
   r.D = __ldg(&a.meta[t].D);
   r.col_off = __ldg(&a.meta[t].col_off);
-  r.weighted = (a.psw_sorted != nullptr) && __ldg(&a.meta[t].weighted);
+  r.weighted = (a.psw_sorted != nullptr) && (a.coef_all || __ldg(&a.meta[t].weighted));
   const bool staged = a.T <= kRedSmemT;
   const int64_t go = staged ? s_red_gofs[t] : a.gofs[t];
   const int64_t uc = staged ? s_red_uc[t] : a.unique_count[t];
@@ -1728,6 +1739,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages)
     la.seg_dbits = L.seg_dbits;
     la.seg_hist = at<uint32_t>(ws, L.seg_hist);
     la.seg_inv = at<uint32_t>(ws, L.seg_inv);
+    const bool mean = p.pooling == TBE_POOL_MEAN;
+    la.psw = a.psw;
+    la.coef = mean ? at<float>(ws, L.coef) : nullptr;
     if (L.small)
       linearize_kernel<4><<<L.lin_blocks, kLinThreads, 0, s>>>(la);
     else
@@ -1759,9 +1773,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages)
         ga.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
         ga.status = a.status;
         ga.bag_of = at<int32_t>(ws, L.bag_of);
-        ga.psw = a.psw;
+        ga.psw = mean ? at<float>(ws, L.coef) : a.psw;
         ga.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
-        ga.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+        ga.psw_sorted = (last && (mean || (a.psw && p.any_weighted))) ? at<float>(ws, L.psw_sorted) : nullptr;
         ga.N = (int32_t)N;
         ga.T = p.T;
         ga.B = a.B;
@@ -1787,9 +1801,9 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages)
       sa.tile_counter = at<uint32_t>(ws, L.sort_tiles) + pass;
       sa.status = a.status;
       sa.bag_of = at<int32_t>(ws, L.bag_of);
-      sa.psw = a.psw;
+      sa.psw = mean ? at<float>(ws, L.coef) : a.psw;
       sa.bag_sorted = last ? at<int32_t>(ws, L.bag_sorted) : nullptr;
-      sa.psw_sorted = (last && a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+      sa.psw_sorted = (last && (mean || (a.psw && p.any_weighted))) ? at<float>(ws, L.psw_sorted) : nullptr;
       sa.N = (int32_t)N;
       sa.shift = 8 * pass;
       if (launch_pdl(L.small ? sort_pass_kernel<6> : sort_pass_kernel<12>, L.sort_ntiles, kSortThreads, s, sa))
@@ -1844,7 +1858,8 @@ int launch_backward(const Plan& p, const BwdArgs& a, cudaStream_t s, int stages)
   rd.grad_out = a.grad_out;
   rd.meta = a.meta;
   rd.bag_sorted = at<int32_t>(ws, L.bag_sorted);
-  rd.psw_sorted = (a.psw && p.any_weighted) ? at<float>(ws, L.psw_sorted) : nullptr;
+  rd.psw_sorted = (p.pooling == TBE_POOL_MEAN || (a.psw && p.any_weighted)) ? at<float>(ws, L.psw_sorted) : nullptr;
+  rd.coef_all = p.pooling == TBE_POOL_MEAN;
   rd.unique_rows = a.unique_rows;
   rd.run_starts = run_starts;
   rd.run_table = at<int32_t>(ws, L.run_table);

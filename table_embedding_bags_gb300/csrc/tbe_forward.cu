@@ -146,6 +146,7 @@ __device__ __forceinline__ void pool_bag(const FwdArgs& a, const TableMeta& m, i
         float f[E];
 #pragma unroll
         for (int e = 0; e < E; ++e) f[e] = NS == 2 ? __fadd_rn(acc[0][k][e], acc[NS - 1][k][e]) : acc[0][k][e];
+        if (a.mean) mean_scale(f, E, end - start);
         store_out<OutT>(out_row + (int64_t)c * E, f, E, a.out_vec_ok);
       }
     }
@@ -414,6 +415,7 @@ __device__ __forceinline__ void pool_bag_ring(const FwdArgs& a, const TableMeta&
     if (c < C) {
 #pragma unroll
       for (int e = 0; e < E; e += 2) add2(acc[k][e], acc[k][e + 1], tot[k][e], tot[k][e + 1]);
+      if (a.mean) mean_scale(acc[k], E, end - start);
       store_out<OutT>(out_row + (int64_t)c * E, acc[k], E, a.out_vec_ok);
     }
   }
@@ -787,6 +789,7 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
             for (int e = 0; e < E; e += 2)
               add2(res[e], res[e + 1], __shfl_xor_sync(kFull, res[e], o), __shfl_xor_sync(kFull, res[e + 1], o));
           }
+          if (a.mean) mean_scale(res, E, __shfl_sync(kFull, len, bag));  // lane k holds bag k's length
           if (grp == 0 && live) store_out<OutT>(out_ptr + (int64_t)bag * a.sumD, res, E, a.out_vec_ok);
 #pragma unroll
           for (int e = 0; e < E; ++e) acc[e] = 0.f;

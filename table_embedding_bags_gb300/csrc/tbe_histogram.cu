@@ -695,6 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) hist_kernel(const FwdArgs a, cons
               }
             }
           }
+          if (a.mean && q < nbag) mean_scale(v, 32, off[q + 1] - off[q]);
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<float4*>(stg + q * 64 + (((half * 8 + j) ^ (q & 7)) << 2)) =

@@ -44,6 +44,7 @@ struct Plan {
   int32_t uniform;       // every table has the same width, dtype and weighting
   int32_t max_row_bytes; // widest row of the layout
   int32_t hist_ok;       // static part of the histogram-path eligibility
+  int32_t pooling;       // TBE_POOL_SUM or TBE_POOL_MEAN
   int32_t device;        // device the plan was created on
   const TableMeta* dmeta;  // device copy (caller memory)
   TableMeta* hmeta;        // host copy (T+1 records)
@@ -403,7 +404,18 @@ struct FwdArgs {
   int32_t out_vec_ok;
   int32_t lpr_max;  // lanes per row cap of the gather (a power of two <= 32)
   int32_t balance;  // tables differ in shape: size each table's tasks by its own mean bag length
+  int32_t mean;     // mean pooling: each bag's sum divided by its number of lookups
 };
+
+// Mean pooling: the bag's fp32 sum divided by its number of lookups, one IEEE
+// division per element (the count is exact in fp32); an empty bag stays 0.
+__device__ __forceinline__ void mean_scale(float* v, int n, int64_t len) {
+  if (len > 0) {
+    const float d = (float)len;
+#pragma unroll
+    for (int e = 0; e < n; ++e) v[e] = __fdiv_rn(v[e], d);
+  }
+}
 
 int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s);
 int launch_forward_histogram(const Plan& p, const FwdArgs& a, int32_t* counts_out, cudaStream_t s);

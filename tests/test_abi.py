@@ -88,12 +88,12 @@ def test_exact_update_rejects_without_plan(lib):
     assert rc == tbe.TBE_ERR_INVALID_ARG
 
 
-def _layout(T, trb, doff, woff, wdt, out_dtype=0):
+def _layout(T, trb, doff, woff, wdt, out_dtype=0, pooling=0):
     import numpy as np
 
     keep = [np.ascontiguousarray(trb, np.int64), np.ascontiguousarray(doff, np.int32),
             np.ascontiguousarray(woff, np.int64), np.ascontiguousarray(wdt, np.int32)]
-    L = tbe._Layout(T, *(a.ctypes.data for a in keep), None, out_dtype)
+    L = tbe._Layout(T, *(a.ctypes.data for a in keep), None, out_dtype, pooling)
     return L, keep
 
 
@@ -109,6 +109,7 @@ BAD_LAYOUTS = {
     "unknown_dtype": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[7]), tbe.TBE_ERR_INVALID_ARG),
     "unknown_out_dtype": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[0], out_dtype=9),
                           tbe.TBE_ERR_INVALID_ARG),
+    "unknown_pooling": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[0], pooling=2), tbe.TBE_ERR_INVALID_ARG),
     "row_not_16_bytes": (dict(T=1, trb=[0, 10], doff=[0, 3], woff=[0], wdt=[0]), tbe.TBE_ERR_UNSUPPORTED),
     "half_row_not_16_bytes": (dict(T=1, trb=[0, 10], doff=[0, 4], woff=[0], wdt=[1]), tbe.TBE_ERR_UNSUPPORTED),
     "table_not_aligned": (dict(T=2, trb=[0, 10, 20], doff=[0, 4, 8], woff=[0, 8], wdt=[0, 0]),
@@ -120,7 +121,7 @@ BAD_LAYOUTS = {
 @pytest.mark.parametrize("name", sorted(BAD_LAYOUTS))
 def test_plan_create_refuses_bad_layouts(lib, name):
     kw, want = BAD_LAYOUTS[name]
-    L, _keep = _layout(kw["T"], kw["trb"], kw["doff"], kw["woff"], kw["wdt"], kw.get("out_dtype", 0))
+    L, _keep = _layout(kw["T"], kw["trb"], kw["doff"], kw["woff"], kw["wdt"], kw.get("out_dtype", 0), kw.get("pooling", 0))
     meta = (ctypes.c_uint8 * (1 << 20))()
     base = (ctypes.addressof(meta) + 15) // 16 * 16
     h = ctypes.c_void_p()
