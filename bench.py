@@ -16,8 +16,7 @@ outputs and the unique-row gradients written; see effective_bytes().
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank runs an independent replica on its own GPU (the
-operator has no exchange step in this build); rank 0 prints the whole-job
-line.  ``--impl reference`` times the CPU oracle on the same workload.
+operator has no exchange step); rank 0 prints the whole-job line.  ``--impl reference`` times the CPU oracle on the same workload.
 """
 
 from __future__ import annotations
