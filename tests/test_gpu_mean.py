@@ -137,3 +137,19 @@ def test_mean_is_the_sum_over_the_length(tbe):
     assert torch.all(m[Lc == 0] == 0) and torch.all(s[Lc == 0] == 0)
     nz = Lc > 0
     assert torch.allclose((m * Lc)[nz], s[nz], rtol=2e-3, atol=1e-3)  # fp16 output rounding
+
+
+def test_all_bags_empty(tbe):
+    """Mean of no lookups is 0 on every path, and the backward has no rows."""
+    p = make_problem(2, 4, rows=[5, 7], D=[16, 32], weights_dtype=[DT_F16, DT_BF16], out_dtype=DT_F32,
+                     lengths=[[0] * 4, [0] * 4], ids=[[], []], grad_out=np.ones((4, 48), np.float32), pooling=1)
+    w_dev, _ = parity.weights_pair(p)
+    d = parity.upload(p)
+    plan = tbe.Plan.from_problem(p)
+    for path in (tbe.TBE_PATH_GATHER, tbe.TBE_PATH_HISTOGRAM):
+        out = tbe.tbe_forward(plan, w_dev, d["indices"], d["offsets"], p.B, path=path)
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(out) == 0
+    bufs = tbe.tbe_backward(plan, d["grad"], d["indices"], d["offsets"], p.B)
+    torch.cuda.synchronize()
+    assert bufs.unique_count.cpu().tolist() == [0, 0, 0]

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import parity
-from tbe_inputs import make_config
+from tbe_inputs import DT_F32, make_config, make_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -114,3 +114,18 @@ def test_split_misuse_is_refused(tbe):
     with pytest.raises(tbe.TBEError):  # weights given to one call only
         tbe.tbe_backward_reduce(plan, d["grad"], bufs, per_sample_weights=torch.ones(p.N, device="cuda"))
     torch.cuda.synchronize()
+
+
+def test_split_with_no_lookups(tbe):
+    """Every bag empty (N = 0): the index call clears the counts and the
+    reduction has nothing to do."""
+    p = make_problem(2, 3, rows=[5, 7], D=[4, 8], weights_dtype=[DT_F32, DT_F32], out_dtype=DT_F32,
+                     lengths=[[0, 0, 0], [0, 0, 0]], ids=[[], []], grad_out=np.ones((3, 12), np.float32))
+    d = parity.upload(p)
+    plan = tbe.Plan.from_problem(p)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bufs = tbe.tbe_backward_index(plan, d["indices"], d["offsets"], p.B, dev_status=st)
+    tbe.tbe_backward_reduce(plan, d["grad"], bufs, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert bufs.unique_count.cpu().tolist() == [0, 0, 0]
