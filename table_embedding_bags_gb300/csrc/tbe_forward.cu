@@ -42,6 +42,18 @@ __device__ __forceinline__ TableMeta load_meta(const TableMeta* p) {
   return m;
 }
 
+// The same, issued where it stands (the compiler may not sink it to its
+// first use, behind loads that the caller waits on first).
+__device__ __forceinline__ TableMeta load_meta_now(const TableMeta* p) {
+  TableMeta m;
+  uint4 x, y;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "l"(p));
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4+16];" : "=r"(y.x), "=r"(y.y), "=r"(y.z), "=r"(y.w) : "l"(p));
+  *reinterpret_cast<uint4*>(&m) = x;
+  *(reinterpret_cast<uint4*>(&m) + 1) = y;
+  return m;
+}
+
 constexpr int kIdsPerLane = 4;  // id window of a VW: kIdsPerLane * lpr ids
 
 // One id window of a bag held by the lanes of its VW: lane `sub` holds ids
@@ -696,12 +708,13 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
     const int32_t ngroups = (nsteps + kSGroup - 1) / kSGroup;
     const int32_t npad = (ngroups * kSGroup) << rsh;  // positions of whole groups (<= kSWinAlloc - 31)
     // row addresses (and weights) of positions win0 .. win0 + nwin - 1, then
-    // the zero row to npad; 128 positions per round, all loads issued first
+    // the zero row to npad, 128 positions per round.  The ids (and weights)
+    // of every round are copied into the window's slots first and waited for
+    // once, so a window waits for one round trip of id loads, not one per
+    // round; each slot is then turned into its row's address in place.
+    uint32_t valid = 0;  // bit 4 * round + u: slot q0 + 32u + lane holds a lookup
 #pragma unroll 1
-    for (int32_t q0 = 0; q0 < npad; q0 += 128) {
-      uint64_t raw[4];
-      int32_t iu[4];
-      bool vu[4];
+    for (int32_t q0 = 0, rd = 0; q0 < npad; q0 += 128, ++rd) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int32_t q = q0 + u * 32 + lane;
@@ -709,22 +722,28 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
         const int kb = stream_bag_of(pincl, min(p, P - 1));
         const int32_t r = p - __shfl_sync(kFull, pst, kb);
         const int32_t lk = __shfl_sync(kFull, len, kb);
-        iu[u] = __shfl_sync(kFull, st, kb) + r;
-        vu[u] = q < nwin && r < lk;
-        raw[u] = vu[u] ? a.indices.id_bits(iu[u]) : 0;
+        const int32_t iu = __shfl_sync(kFull, st, kb) + r;
+        if (q0 + u * 32 < npad && q < nwin && r < lk) {
+          valid |= 1u << (4 * rd + u);
+          a.indices.copy_id(smem_u32(srcs + q), iu);
+          if (WT && weighted) cp_async4(smem_u32(wts + q), a.psw + iu);
+        }
       }
-      float wv[4];
-      if (WT) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) wv[u] = (weighted && vu[u]) ? ld_stream_f32(a.psw + iu[u]) : 0.f;
-      }
+    }
+    cp_commit();
+    cp_wait<0>();
+#pragma unroll 1
+    for (int32_t q0 = 0, rd = 0; q0 < npad; q0 += 128, ++rd) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (q0 + u * 32 < npad) {
-          const bool ok = vu[u] && raw[u] < (uint64_t)m.rows;
-          bad |= vu[u] && !ok;  // reported; contributes nothing
-          srcs[q0 + u * 32 + lane] = ok ? reinterpret_cast<uint64_t>(tbl) + raw[u] * row_bytes : zero_row;
-          if (WT) wts[q0 + u * 32 + lane] = ok ? wv[u] : 0.f;
+          const int32_t q = q0 + u * 32 + lane;
+          const bool vu = (valid >> (4 * rd + u)) & 1u;
+          const uint64_t raw = vu ? srcs[q] : 0;
+          const bool ok = vu && raw < (uint64_t)m.rows;
+          bad |= vu && !ok;  // reported; contributes nothing
+          srcs[q] = ok ? reinterpret_cast<uint64_t>(tbl) + raw * row_bytes : zero_row;
+          if (WT && weighted && !ok) wts[q] = 0.f;
         }
       }
     }
@@ -890,6 +909,8 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
     stream_bounds(a, cur, lane, cs, ce);
   }
   while (task < ntasks) {
+    // the table's meta is requested before anything waits on the bounds
+    const TableMeta m = load_meta_now(a.meta + cur.t);
     // the next task's bounds are requested while this one is pooled
     const int32_t next = task + nw;
     StreamTask nxt{0, 0, 0};
@@ -905,7 +926,6 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
         cs = ce = 0;  // pooled as empty
       }
     }
-    const TableMeta m = load_meta(a.meta + cur.t);
     if (DTSEL >= 0) {
       stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid);
     } else {

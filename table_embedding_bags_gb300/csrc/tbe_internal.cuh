@@ -121,6 +121,10 @@ struct IdxPtr {
       asm volatile("ld.global.nc.L1::no_allocate.u64 %0, [%1];" : "=l"(v) : "l"(static_cast<const int64_t*>(p) + i));
     return v;
   }
+  // Id i copied into the 8-byte shared-memory slot at dst (asynchronously,
+  // cp.async): int64 ids as stored, int32 ids into the low word with the
+  // high word zeroed, so the slot reads as id_bits(i) once the copy landed.
+  __device__ __forceinline__ void copy_id(uint32_t dst, int64_t i) const;
   // read-only path (cached)
   __device__ __forceinline__ int64_t ldg(int64_t i) const {
     return i32 ? (int64_t)__ldg(static_cast<const int32_t*>(p) + i) : __ldg(static_cast<const int64_t*>(p) + i);
@@ -264,10 +268,25 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // all but the N most recent groups of this thread have landed
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void IdxPtr::copy_id(uint32_t dst, int64_t i) const {
+  if (i32) {
+    asm volatile("st.shared.u32 [%0+4], %1;" ::"r"(dst), "r"(0u) : "memory");
+    cp_async4(dst, static_cast<const int32_t*>(p) + i);
+  } else {
+    cp_async8(dst, static_cast<const int64_t*>(p) + i);
+  }
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
