@@ -380,6 +380,7 @@ static int forward_call(const tbe_plan* plan, const void* weights, IdxPtr indice
   a.lpr_max = g_tuning.fwd_lanes_per_row;
   a.balance = plan->uniform ? 0 : 1;
   a.mean = plan->pooling == TBE_POOL_MEAN;
+  a.split = 0;  // chosen by the stream kernel's launch
   bool hist = false;
   if (path == TBE_PATH_HISTOGRAM) {
     if (!hist_eligible(plan)) return TBE_ERR_UNSUPPORTED;

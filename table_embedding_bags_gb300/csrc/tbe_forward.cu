@@ -659,13 +659,24 @@ __device__ __forceinline__ int stream_bag_of(int32_t pincl, int32_t p) {
   return k;
 }
 
+// Start of part `part` of a task's padded stream cut into `nparts` parts of
+// equal length (multiples of R; part nparts starts at the end, P).
+__device__ __forceinline__ int32_t stream_cut(int part, int nparts, int32_t P, int R) {
+  if (part >= nparts) return P;
+  return (int32_t)(((int64_t)part * P / nparts) & ~(int64_t)(R - 1));
+}
+
 // One task: bags b0 .. b0 + nb - 1 of table m; lane k < nb holds the bounds
 // [st, en) of bag b0 + k (already checked).  `ring`: this thread's slot 0;
 // `srcs` / `wts`: the warp's stream window (row addresses and weights).
+// With nparts > 1 every warp of the block pools part `part` (its warp index)
+// of the same task: a bag cut by a part boundary is summed in pieces, and
+// after a block barrier the part holding its end adds the pieces in part
+// order and stores it.
 template <int DT, bool WT, typename OutT, int RG>
 __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m, const StreamTask& k, int lane,
                                             int32_t st, int32_t en, uint32_t ring, unsigned long long* srcs,
-                                            float* wts, float* tot) {
+                                            float* wts, float* tot, int part = 0, int nparts = 1) {
   constexpr int E = Chunk<DT>::kElems;
   const int C = m.D / E;  // 16-byte chunks per row (<= 32)
   const int lsh = C <= 1 ? 0 : 32 - __clz(C - 1);
@@ -687,6 +698,15 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
   }
   const int32_t P = __shfl_sync(kFull, pincl, 31);
   const int32_t pst = pincl - plen;
+  // this part's positions [lo, hi); its first bag may have begun in an
+  // earlier part (head_bag: the piece from lo to its end is kept in the
+  // window's spare slots, past any position a window stages) and its last
+  // may run on into the next
+  const int32_t lo = stream_cut(part, nparts, P, R), hi = stream_cut(part + 1, nparts, P, R);
+  int bag = lo < hi && lo > 0 ? stream_bag_of(pincl, lo) : 0;  // bag of the next position pooled
+  const int head_bag = lo < hi && __shfl_sync(kFull, pst, bag) < lo ? bag : -1;
+  bool head_done = false;
+  float* head_piece = reinterpret_cast<float*>(srcs + kSWin + 32) + sub * E;
   bool bad = false;
   // acc: the running sum since the bag's start or the last fold; tot (this
   // thread's column of shared memory, stride kSThreads): the folded part,
@@ -695,15 +715,14 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   bool tot_live = false;
-  int bag = 0;  // bags stored so far
   OutT* out_ptr = reinterpret_cast<OutT*>(a.out) + (int64_t)k.b0 * a.sumD + m.col_off + sub * E;
   const unsigned long long* my_srcs = srcs + grp;
   const float* my_wts = wts + grp;
   const uint32_t sub16 = (uint32_t)sub * 16u;
 
 #pragma unroll 1
-  for (int32_t win0 = 0; win0 < P; win0 += kSWin) {
-    const int32_t nwin = min(kSWin, P - win0);
+  for (int32_t win0 = lo; win0 < hi; win0 += kSWin) {
+    const int32_t nwin = min(kSWin, hi - win0);
     const int32_t nsteps = nwin >> rsh;
     const int32_t ngroups = (nsteps + kSGroup - 1) / kSGroup;
     const int32_t npad = (ngroups * kSGroup) << rsh;  // positions of whole groups (<= kSWinAlloc - 31)
@@ -808,8 +827,16 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
             for (int e = 0; e < E; e += 2)
               add2(res[e], res[e + 1], __shfl_xor_sync(kFull, res[e], o), __shfl_xor_sync(kFull, res[e + 1], o));
           }
-          if (a.mean) mean_scale(res, E, __shfl_sync(kFull, len, bag));  // lane k holds bag k's length
-          if (grp == 0 && live) store_out<OutT>(out_ptr + (int64_t)bag * a.sumD, res, E, a.out_vec_ok);
+          if (bag == head_bag) {  // the end of a bag begun in an earlier part: kept for the combine
+            if (grp == 0 && live) {
+#pragma unroll
+              for (int e = 0; e < E; ++e) head_piece[e] = res[e];
+            }
+            head_done = true;
+          } else {
+            if (a.mean) mean_scale(res, E, __shfl_sync(kFull, len, bag));  // lane k holds bag k's length
+            if (grp == 0 && live) store_out<OutT>(out_ptr + (int64_t)bag * a.sumD, res, E, a.out_vec_ok);
+          }
 #pragma unroll
           for (int e = 0; e < E; ++e) acc[e] = 0.f;
           tot_live = false;
@@ -833,6 +860,67 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
     __syncwarp();  // the window is rewritten next
   }
   if (__any_sync(kFull, bad) && lane == 0) report(a.status, TBE_DEV_BAD_INDEX);
+  if (nparts == 1) return;
+  // the last bag runs on into the next part: its piece goes to this thread's
+  // ring slots (every copy into them has landed)
+  if (lo < hi && hi < P && __shfl_sync(kFull, pincl, stream_bag_of(pincl, hi - 1)) > hi) {
+    float res[E];
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      res[e] = acc[e];
+      res[e + 1] = acc[e + 1];
+      if (tot_live) add2(res[e], res[e + 1], tot[e * kSThreads], tot[(e + 1) * kSThreads]);
+    }
+    for (int o = lpr; o < 32; o <<= 1) {
+#pragma unroll
+      for (int e = 0; e < E; e += 2)
+        add2(res[e], res[e + 1], __shfl_xor_sync(kFull, res[e], o), __shfl_xor_sync(kFull, res[e + 1], o));
+    }
+    if (grp == 0 && live) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ring + (uint32_t)(e / 4) * kSRingStride),
+                     "f"(res[e]), "f"(res[e + 1]), "f"(res[e + 2]), "f"(res[e + 3])
+                     : "memory");
+    }
+  }
+  __syncthreads();  // every part's pieces are in shared memory
+  if (head_done) {  // add the pieces of the bag in part order: the parts before this one, then this one's
+    const int32_t bstart = __shfl_sync(kFull, pst, head_bag);
+    const int32_t hlen = __shfl_sync(kFull, len, head_bag);
+    int v0 = part - 1;  // the part holding the bag's first position
+    while (v0 > 0 && stream_cut(v0, nparts, P, R) > bstart) --v0;
+    if (grp == 0 && live) {
+      float res[E];
+      bool first = true;
+      for (int v = v0; v < part; ++v) {
+        if (stream_cut(v, nparts, P, R) == stream_cut(v + 1, nparts, P, R)) continue;  // an empty part
+        const uint32_t src = ring - (uint32_t)((part - v) * 32 * 16);  // the same lane of warp v
+#pragma unroll
+        for (int e = 0; e < E; e += 4) {
+          const uint4 x = lds128(src + (uint32_t)(e / 4) * kSRingStride);
+          const float y[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
+          if (first) {
+            res[e] = y[0], res[e + 1] = y[1], res[e + 2] = y[2], res[e + 3] = y[3];
+          } else {
+            add2(res[e], res[e + 1], y[0], y[1]);
+            add2(res[e + 2], res[e + 3], y[2], y[3]);
+          }
+        }
+        first = false;
+      }
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        if (first) {
+          res[e] = head_piece[e], res[e + 1] = head_piece[e + 1];
+        } else {
+          add2(res[e], res[e + 1], head_piece[e], head_piece[e + 1]);
+        }
+      }
+      if (a.mean) mean_scale(res, E, hlen);
+      store_out<OutT>(out_ptr + (int64_t)head_bag * a.sumD, res, E, a.out_vec_ok);
+    }
+  }
 }
 
 template <typename OutT, int DTSEL, bool WT, int RG, int MINB>
@@ -902,6 +990,37 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
   const uint32_t ring = smem_u32(dsm) + tid * 16;
   unsigned long long* srcs = s_srcs + warp * kSWinAlloc;
   float* wts = s_wts + warp * kSWinAlloc;
+  if (a.split) {  // one task per block, its padded stream cut into one part per warp
+    const int32_t nbb = a.split;
+    const int32_t tpb = (a.B + nbb - 1) / nbb;
+    const int32_t bt = (int32_t)blockIdx.x;
+    if (bt < a.T * tpb) {  // the same for the whole block: every warp reaches the combine's barrier
+      StreamTask k{bt / tpb, (bt % tpb) * nbb, 0};
+      k.nb = min(nbb, a.B - k.b0);
+      const TableMeta m = load_meta_now(a.meta + k.t);
+      int64_t cs = 0, ce = 0;
+      stream_bounds(a, k, lane, cs, ce);
+      if (lane < k.nb) {
+        const int32_t g = k.t * a.B + k.b0 + lane;
+        if (cs < 0 || ce < cs || ce > a.N || (g == 0 && cs != 0) || (g == nb_all - 1 && ce != a.N)) {
+          if (warp == 0) report(a.status, TBE_DEV_BAD_OFFSETS);
+          cs = ce = 0;
+        }
+      }
+      if (DTSEL >= 0) {
+        stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts,
+                                                           s_tot + tid, warp, kSWarps);
+      } else {
+        switch (m.dtype) {
+          case TBE_F32: stream_task<TBE_F32, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
+          case TBE_F16: stream_task<TBE_F16, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
+          default: stream_task<TBE_BF16, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    return;
+  }
   StreamTask cur{0, 0, 0};
   int64_t cs = 0, ce = 0;
   if (task < ntasks) {
@@ -943,6 +1062,29 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
   asm volatile("cp.async.wait_all;" ::: "memory");  // no copy outlives the block's shared memory
 }
 
+// Split tasks.  The task sizes of the stream kernel are whole bags, so the
+// warp that drew the most lookups ends the launch (tasks of 5 Poisson(20)
+// bags: 102 positions on average, up to 150).  Where the layout has one
+// table shape and a bag per lane covers a block's share of the batch, each
+// block instead takes one run of at most 32 bags and its four warps pool
+// equal quarters of the run's padded stream (the largest about 118).  The
+// piece of a bag that spans two parts is kept in shared memory (at most
+// kSplitMaxD fp32 sums in a window's spare slots).
+constexpr int kSplitMaxD = (kSWinAlloc - kSWin - 32) * 8 / 4;  // 192
+constexpr int64_t kSplitMinPart = 32;                           // positions per part on average, at least
+
+// Bags per block of a split launch of `grid` blocks (0: no split): the
+// fewest with which the tables' runs fit in one wave of blocks.
+int32_t stream_split_bags(const FwdArgs& a, int grid) {
+  if (a.balance || a.N <= 0 || a.T <= 0 || a.B <= 0) return 0;
+  int64_t nbb = std::max<int64_t>(1, ((int64_t)a.T * a.B + grid - 1) / grid);
+  while (nbb <= 32 && (int64_t)a.T * ((a.B + nbb - 1) / nbb) > grid) ++nbb;
+  if (nbb > 32) return 0;
+  const int64_t runs = (int64_t)a.T * ((a.B + nbb - 1) / nbb);
+  if (a.N < kSplitMinPart * kSWarps * runs) return 0;
+  return (int32_t)nbb;
+}
+
 constexpr int kStreamRG = 2;    // copy groups in the ring (8 steps in flight per lane)
 constexpr int kStreamMinB = 6;  // resident blocks per SM the register budget targets
 
@@ -971,7 +1113,9 @@ int launch_stream(const FwdArgs& a, cudaStream_t s) {
   if (tuning().fwd_blocks_per_sm > 0) per_sm = std::min(per_sm, tuning().fwd_blocks_per_sm);
   const int64_t want = ((int64_t)a.T * a.B + kSWarps - 1) / kSWarps;  // a bag per warp at least
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * per_sm));
-  kern<<<grid, kSThreads, smem, s>>>(a);
+  FwdArgs b = a;
+  b.split = a.split ? stream_split_bags(a, grid) : 0;
+  kern<<<grid, kSThreads, smem, s>>>(b);
   return check_launch();
 }
 
@@ -1061,10 +1205,12 @@ int launch_forward_gather(const Plan& p, const FwdArgs& a, cudaStream_t s) {
                        ? ((p.max_row_bytes <= kStreamMaxRowBytes || (p.max_row_bytes <= 512 && short_bags)) ? 2 : 1)
                        : tuning().fwd_ring;
   if (mode == 2 && ring_eligible(p)) {
+    FwdArgs b = a;
+    b.split = p.uniform && p.hmeta[0].D <= kSplitMaxD ? 1 : 0;  // a run's bags are chosen at launch
     switch (p.out_dtype) {
-      case TBE_F32: return launch_stream_dt<float>(p, a, s);
-      case TBE_F16: return launch_stream_dt<__half>(p, a, s);
-      default: return launch_stream_dt<__nv_bfloat16>(p, a, s);
+      case TBE_F32: return launch_stream_dt<float>(p, b, s);
+      case TBE_F16: return launch_stream_dt<__half>(p, b, s);
+      default: return launch_stream_dt<__nv_bfloat16>(p, b, s);
     }
   }
   if (mode == 1 && ring_eligible(p)) {

@@ -113,6 +113,69 @@ def test_narrow_rows_long_bags(tbe, gather_mode, out_dt, weighted):
     check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
 
 
+def split_bags(T, B, N, grid):
+    """Bags per block with which the stream kernel splits its tasks (0: it
+    does not): the fewest that fit every table's runs in one wave, at most
+    32, with 32 positions per warp on average at least."""
+    nbb = max(1, -(-T * B // grid))
+    while nbb <= 32 and T * -(-B // nbb) > grid:
+        nbb += 1
+    runs = T * -(-B // nbb)
+    return nbb if nbb <= 32 and N >= 32 * 4 * runs else 0
+
+
+@pytest.mark.parametrize("dt,D", [(DT_F16, 128), (DT_BF16, 64), (DT_F32, 64), (DT_F16, 8), (DT_F32, 4)])
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("pooling", [0, 1])
+def test_split_tasks(tbe, dt, D, weighted, pooling):
+    """The stream kernel's split tasks: a block pools one run of bags in four
+    equal parts of its padded stream, so bags are cut by part boundaries --
+    one bag longer than the rest of its run, runs of empty bags, bags of one
+    lookup -- and the pieces are added after a block barrier."""
+    rng = np.random.default_rng(31 + D + 2 * weighted + pooling)
+    T, B, rows = 3, 96, 300
+    lens = rng.poisson(40, size=(T, B))
+    lens[0, 5] = 3000
+    lens[1, ::7] = 0
+    lens[2, 10:20] = 1
+    lens[1, 40:48] = 0
+    N = int(lens.sum())
+    assert split_bags(T, B, N, -(-T * B // 4)) > 0
+    ids = [rng.integers(0, rows, size=int(lens[t].sum())) for t in range(T)]
+    psw = rng.standard_normal(N).astype(np.float32) if weighted else None
+    p = make_problem(T, B, rows=[rows] * T, D=[D] * T, weights_dtype=[dt] * T, out_dtype=DT_F32, lengths=lens,
+                     ids=ids, psw=psw, table_weighted=[1] * T if weighted else None, seed=7, pooling=pooling)
+    old = tbe.get_tuning()
+    tbe.set_tuning(fwd_ring=2)
+    try:
+        check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
+    finally:
+        tbe.set_tuning(**old)
+
+
+def test_split_tasks_bad_id_in_a_cut_bag(tbe):
+    """A bad id inside the bag that spans the parts is reported and adds
+    nothing; every other output still matches."""
+    T, B, rows, D = 2, 64, 100, 32
+    lens = np.full((T, B), 40)
+    lens[0, 3] = 2000
+    ids = [np.arange(int(lens[t].sum())) % rows for t in range(T)]
+    ids[0][int(lens[0, :3].sum()) + 1500] = rows + 5
+    p = make_problem(T, B, rows=[rows] * T, D=[D] * T, weights_dtype=[DT_F16] * T, out_dtype=DT_F32, lengths=lens,
+                     ids=ids, seed=3)
+    assert split_bags(T, B, p.N, -(-T * B // 4)) > 0
+    old = tbe.get_tuning()
+    tbe.set_tuning(fwd_ring=2)
+    try:
+        out, st, w_host = run_forward(tbe, p, tbe.TBE_PATH_GATHER)
+    finally:
+        tbe.set_tuning(**old)
+    assert st == tbe.TBE_DEV_BAD_INDEX
+    ost, ref, ref_abs = oracle.problem_forward(p, w_host)
+    assert ost == oracle.BAD_INDEX
+    parity.compare_forward(p, parity.to_f64(out), ref, ref_abs)
+
+
 def test_repeated_ids_and_empty(tbe, gather_mode):
     p = make_problem(2, 3, rows=[5, 7], D=[8, 4], weights_dtype=[DT_F16, DT_F32], out_dtype=DT_F32,
                      lengths=[[0, 40, 1], [3, 0, 0]], ids=[[2] * 40 + [4], [6, 6, 0]])
