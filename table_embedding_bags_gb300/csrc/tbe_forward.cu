@@ -673,7 +673,7 @@ __device__ __forceinline__ int32_t stream_cut(int part, int nparts, int32_t P, i
 // of the same task: a bag cut by a part boundary is summed in pieces, and
 // after a block barrier the part holding its end adds the pieces in part
 // order and stores it.
-template <int DT, bool WT, typename OutT, int RG>
+template <int DT, bool WT, typename OutT, int RG, bool MEAN>
 __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m, const StreamTask& k, int lane,
                                             int32_t st, int32_t en, uint32_t ring, unsigned long long* srcs,
                                             float* wts, float* tot, int part = 0, int nparts = 1) {
@@ -704,9 +704,8 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
   // may run on into the next
   const int32_t lo = stream_cut(part, nparts, P, R), hi = stream_cut(part + 1, nparts, P, R);
   int bag = lo < hi && lo > 0 ? stream_bag_of(pincl, lo) : 0;  // bag of the next position pooled
-  const int head_bag = lo < hi && __shfl_sync(kFull, pst, bag) < lo ? bag : -1;
+  const int head_bag = nparts > 1 && lo < hi && __shfl_sync(kFull, pst, bag) < lo ? bag : -1;
   bool head_done = false;
-  float* head_piece = reinterpret_cast<float*>(srcs + kSWin + 32) + sub * E;
   bool bad = false;
   // acc: the running sum since the bag's start or the last fold; tot (this
   // thread's column of shared memory, stride kSThreads): the folded part,
@@ -827,14 +826,15 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
             for (int e = 0; e < E; e += 2)
               add2(res[e], res[e + 1], __shfl_xor_sync(kFull, res[e], o), __shfl_xor_sync(kFull, res[e + 1], o));
           }
-          if (bag == head_bag) {  // the end of a bag begun in an earlier part: kept for the combine
+          if (nparts > 1 && bag == head_bag) {  // the end of a bag begun in an earlier part: kept for the combine
             if (grp == 0 && live) {
+              float* head_piece = reinterpret_cast<float*>(srcs + kSWin + 32) + sub * E;
 #pragma unroll
               for (int e = 0; e < E; ++e) head_piece[e] = res[e];
             }
             head_done = true;
           } else {
-            if (a.mean) mean_scale(res, E, __shfl_sync(kFull, len, bag));  // lane k holds bag k's length
+            if (MEAN) mean_scale(res, E, __shfl_sync(kFull, len, bag));  // lane k holds bag k's length
             if (grp == 0 && live) store_out<OutT>(out_ptr + (int64_t)bag * a.sumD, res, E, a.out_vec_ok);
           }
 #pragma unroll
@@ -891,6 +891,7 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
     int v0 = part - 1;  // the part holding the bag's first position
     while (v0 > 0 && stream_cut(v0, nparts, P, R) > bstart) --v0;
     if (grp == 0 && live) {
+      const float* head_piece = reinterpret_cast<const float*>(srcs + kSWin + 32) + sub * E;
       float res[E];
       bool first = true;
       for (int v = v0; v < part; ++v) {
@@ -917,13 +918,15 @@ __device__ __forceinline__ void stream_task(const FwdArgs& a, const TableMeta& m
           add2(res[e], res[e + 1], head_piece[e], head_piece[e + 1]);
         }
       }
-      if (a.mean) mean_scale(res, E, hlen);
+      if (MEAN) mean_scale(res, E, hlen);
       store_out<OutT>(out_ptr + (int64_t)head_bag * a.sumD, res, E, a.out_vec_ok);
     }
   }
 }
 
-template <typename OutT, int DTSEL, bool WT, int RG, int MINB>
+// MEAN: mean pooling (a template parameter: the division's code, inlined,
+// raised the register pressure of the pooling loop of sum-pooling launches)
+template <typename OutT, int DTSEL, bool WT, int RG, int MINB, bool SPLIT, bool MEAN>
 __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdArgs a) {
   extern __shared__ __align__(16) unsigned char dsm[];
   constexpr size_t kRingB = (size_t)RG * kSGroup * kSThreads * 16;
@@ -990,7 +993,7 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
   const uint32_t ring = smem_u32(dsm) + tid * 16;
   unsigned long long* srcs = s_srcs + warp * kSWinAlloc;
   float* wts = s_wts + warp * kSWinAlloc;
-  if (a.split) {  // one task per block, its padded stream cut into one part per warp
+  if (SPLIT) {  // one task per block, its padded stream cut into one part per warp
     const int32_t nbb = a.split;
     const int32_t tpb = (a.B + nbb - 1) / nbb;
     const int32_t bt = (int32_t)blockIdx.x;
@@ -1007,16 +1010,9 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
           cs = ce = 0;
         }
       }
-      if (DTSEL >= 0) {
-        stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts,
-                                                           s_tot + tid, warp, kSWarps);
-      } else {
-        switch (m.dtype) {
-          case TBE_F32: stream_task<TBE_F32, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
-          case TBE_F16: stream_task<TBE_F16, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
-          default: stream_task<TBE_BF16, WT, OutT, RG>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid, warp, kSWarps); break;
-        }
-      }
+      // split launches take layouts of one table shape, so one dtype
+      stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG, MEAN>(a, m, k, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts,
+                                                         s_tot + tid, warp, kSWarps);
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     return;
@@ -1046,12 +1042,12 @@ __global__ void __launch_bounds__(kSThreads, MINB) fwd_stream_kernel(const FwdAr
       }
     }
     if (DTSEL >= 0) {
-      stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid);
+      stream_task<(DTSEL < 0 ? 0 : DTSEL), WT, OutT, RG, MEAN>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid);
     } else {
       switch (m.dtype) {
-        case TBE_F32: stream_task<TBE_F32, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
-        case TBE_F16: stream_task<TBE_F16, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
-        default: stream_task<TBE_BF16, WT, OutT, RG>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+        case TBE_F32: stream_task<TBE_F32, WT, OutT, RG, MEAN>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+        case TBE_F16: stream_task<TBE_F16, WT, OutT, RG, MEAN>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
+        default: stream_task<TBE_BF16, WT, OutT, RG, MEAN>(a, m, cur, lane, (int32_t)cs, (int32_t)ce, ring, srcs, wts, s_tot + tid); break;
       }
     }
     cur = nxt;
@@ -1087,23 +1083,31 @@ int32_t stream_split_bags(const FwdArgs& a, int grid) {
 
 constexpr int kStreamRG = 2;    // copy groups in the ring (8 steps in flight per lane)
 constexpr int kStreamMinB = 6;  // resident blocks per SM the register budget targets
+// The weighted kernel's shared memory (the window's weights too) leaves room
+// for 5 blocks per SM, so its register budget targets 5: capped for 6 it
+// spilled in the hot loop for no extra residency.
+constexpr int kStreamMinBWeighted = 5;
 
 size_t stream_smem_bytes(bool weighted, int32_t T) {
   return (size_t)kStreamRG * kSGroup * kSThreads * 16 + kSTotBytes + kSSrcBytes + (weighted ? kSWtsBytes : 0) +
          5 * ((size_t)T + 1) + 16;
 }
 
-template <typename OutT, int DTSEL, bool WT>
-int launch_stream(const FwdArgs& a, cudaStream_t s) {
-  auto kern = fwd_stream_kernel<OutT, DTSEL, WT, kStreamRG, kStreamMinB>;
+template <typename OutT, int DTSEL, bool WT, bool MEAN>
+int launch_stream_m(const FwdArgs& a, cudaStream_t s) {
+  constexpr int kMinB = WT ? kStreamMinBWeighted : kStreamMinB;
+  auto kern = fwd_stream_kernel<OutT, DTSEL, WT, kStreamRG, kMinB, false, MEAN>;
+  // split launches need one dtype (a layout of one table shape)
+  auto kern_split = fwd_stream_kernel<OutT, DTSEL, WT, kStreamRG, kMinB, (DTSEL >= 0), MEAN>;
   const size_t smem = stream_smem_bytes(WT, a.T);
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64) dev = 63;
   if (!configured[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem_bytes(WT, TBE_MAX_TABLES)) != cudaSuccess)
+    const int most = (int)stream_smem_bytes(WT, TBE_MAX_TABLES);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess ||
+        cudaFuncSetAttribute(kern_split, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess)
       return TBE_ERR_CUDA;
     configured[dev] = true;
   }
@@ -1114,9 +1118,18 @@ int launch_stream(const FwdArgs& a, cudaStream_t s) {
   const int64_t want = ((int64_t)a.T * a.B + kSWarps - 1) / kSWarps;  // a bag per warp at least
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)sm_count() * per_sm));
   FwdArgs b = a;
-  b.split = a.split ? stream_split_bags(a, grid) : 0;
-  kern<<<grid, kSThreads, smem, s>>>(b);
+  b.split = a.split && DTSEL >= 0 ? stream_split_bags(a, grid) : 0;
+  if (b.split) {
+    kern_split<<<grid, kSThreads, smem, s>>>(b);
+  } else {
+    kern<<<grid, kSThreads, smem, s>>>(b);
+  }
   return check_launch();
+}
+
+template <typename OutT, int DTSEL, bool WT>
+int launch_stream(const FwdArgs& a, cudaStream_t s) {
+  return a.mean ? launch_stream_m<OutT, DTSEL, WT, true>(a, s) : launch_stream_m<OutT, DTSEL, WT, false>(a, s);
 }
 
 template <typename OutT, int DTSEL>
