@@ -337,6 +337,31 @@ def pin_formats(lib, seed=17):
     pos_vals = bf[pos_codes.astype(np.int64)]
     want = _nearest_even_codes(xb, pos_codes, pos_vals)
     np.testing.assert_array_equal(oursb, want)
+    # rounding to fp32: the nearest fp32 value by exact rational distance among
+    # the cast's neighbours, ties to the even code; midpoints of adjacent fp32
+    # values (exact in fp64), their neighbours, subnormals and random doubles
+    from fractions import Fraction
+
+    f32 = (rng.integers(0, 0x7F7FFFFF, 3000, dtype=np.uint32)).view(np.float32).astype(np.float64)
+    nxt = np.nextafter(f32.astype(np.float32), np.float32(np.inf)).astype(np.float64)
+    mid32 = (f32 + nxt) / 2
+    x32 = np.concatenate([mid32, -mid32, np.nextafter(mid32, 0), np.nextafter(mid32, np.inf), f32,
+                          rng.standard_normal(3000) * 10.0 ** rng.integers(-44, 38, 3000),
+                          [1.5 * 2.0 ** -149, 2.0 ** -150, 0.0, -0.0]])
+    ours32 = oracle.round_to(x32, oracle.F32, lib=lib)
+    for x, got in zip(x32, ours32):
+        c = np.float32(x)
+        cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+        cands = [v for v in cands if np.isfinite(v)]
+        dist = [abs(Fraction(float(v)) - Fraction(float(x))) for v in cands]
+        best = min(dist)
+        near = [v for v, dd in zip(cands, dist) if dd == best]
+        want32 = near[0] if len(near) == 1 else [v for v in near if (int(np.float32(v).view(np.uint32)) & 1) == 0][0]
+        assert float(got) == float(want32) and (got == 0 or np.signbit(got) == np.signbit(x)), (x, got, want32)
+    # past the largest fp32 by half an ulp or more: infinity (ties go to the even code, 2^128)
+    big = float(np.finfo(np.float32).max)
+    np.testing.assert_array_equal(oracle.round_to(np.array([big + 2.0 ** 103, -(big + 2.0 ** 104)]), oracle.F32, lib=lib),
+                                  np.array([np.inf, -np.inf], np.float32))
 
 
 def pin_special_cases(lib):

@@ -35,6 +35,10 @@ MUTANTS = {
     "run_start_off_by_one": ("run_starts[U] = (int32_t)j;", "run_starts[U] = (int32_t)(j + (j > 0));"),
     "unique_count_inclusive": ("while (c < U && unique_rows[c] < table_row_base[t]) ++c;",
                                "while (c < U && unique_rows[c] <= table_row_base[t]) ++c;"),
+    "f32_rounds_toward_zero": ("((float*)out)[i] = (float)in[i]; /* C conversion: nearest-even */",
+                               "((float*)out)[i] = nextafterf((float)in[i], 0.0f) == (float)in[i] ? (float)in[i] : "
+                               "(fabs((double)(float)in[i]) > fabs(in[i]) ? nextafterf((float)in[i], 0.0f) : "
+                               "(float)in[i]);"),
     "f16_truncates": ("double q = rint(ldexp(a, 11 - e)); /* in [1024, 2048] */",
                       "double q = floor(ldexp(a, 11 - e));"),
     "bf16_rounds_up": ("double q = rint(ldexp(a, 8 - e)); /* in [128, 256] */",
