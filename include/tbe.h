@@ -378,7 +378,10 @@ int tbe_backward_reduce(const tbe_plan* plan, const tbe_optimizer* opt, void* we
  *   fwd_ring           : forward kernel for layouts whose rows are at most
  *                        512 bytes: 2 = stream (a warp pools a run of
  *                        consecutive bags as one stream of rows copied into
- *                        a shared-memory ring), 1 = per-bag ring (16 rows in
+ *                        a shared-memory ring; for tables of one shape with
+ *                        D <= 192 and a batch that fits one wave of blocks at
+ *                        <= 32 bags per block, a block's four warps pool equal
+ *                        quarters of one run of bags), 1 = per-bag ring (16 rows in
  *                        flight per lane group), 0 = rows loaded into
  *                        registers, 3 = automatic (stream when every row
  *                        is at most 256 bytes, or at most 512 bytes with a
