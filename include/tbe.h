@@ -224,20 +224,18 @@ int tbe_backward_i32(const tbe_plan* plan, const float* grad_out, const int32_t*
 /*
  * Backward without a caller-provided workspace (the page has no counterpart;
  * this is an entry point for callers that cannot allocate device memory,
- * such as a plugin that an engine hands only a stream and its tensors, or
- * code running while a global-mode stream capture forbids cudaMalloc).
+ * such as a plugin that an engine hands only a stream and its tensors).
  * Same arguments and results as tbe_backward, minus the workspace: the
  * scratch space is one array of TBE_STATIC_WORKSPACE_BYTES compiled into the
  * library, held on every GPU that loads it until the process exits.
  *   - Allocates nothing (no cudaMalloc / cudaFree, no allocating library
  *     call); inputs and outputs are still the caller's.
  *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current.
  *   - Batches whose scratch exceeds TBE_STATIC_WORKSPACE_BYTES (check with
  *     tbe_backward_workspace_bytes) are refused with TBE_ERR_WORKSPACE.
  *   - Every call on a device shares the array; calls whose work overlaps on
- *     the GPU (other streams, concurrent graph replays) race and must be
- *     serialised by the caller.
+ *     the GPU (on other streams) race and must be serialised by the caller.
  */
 #define TBE_STATIC_WORKSPACE_BYTES (32u << 20)
 int tbe_backward_static_workspace(const tbe_plan* plan, const float* grad_out, const int64_t* indices,

@@ -4,20 +4,18 @@
 // backward: a plugin inside a serving or training engine is handed a stream
 // and the tensors it reads and writes, while the engine owns every other
 // byte of device memory (allocating behind its back breaks its memory budget,
-// and cudaMalloc may synchronise the device in the middle of its pipeline);
-// and code that runs while a global-mode stream capture is active may not
-// call cudaMalloc at all.  For them this file provides
+// and cudaMalloc may synchronise the device in the middle of its pipeline).
+// For them this file provides
 // tbe_backward_static_workspace(): the same computation as tbe_backward(),
 // whose scratch space is one fixed array compiled into the library instead of
 // a caller-provided workspace.  The caller still passes every input and output.
 //
 // The array lives in every GPU that loads the library until the process
 // exits.  Its device address is looked up once per device, on the first call
-// made with that device current (so make that first call before any stream
-// capture begins).  All calls on a device share the one array: the backward
-// clears the parts that must start at zero itself, but two calls whose work
-// overlaps on the GPU (different streams, or graphs replayed concurrently)
-// race on it and must be serialised by the caller.
+// made with that device current.  All calls on a device share the one array:
+// the backward clears the parts that must start at zero itself, but two calls
+// whose work overlaps on the GPU (on different streams) race on it and must
+// be serialised by the caller.
 #include <mutex>
 
 #include "tbe_internal.cuh"

@@ -1,7 +1,6 @@
 """The backward for callers that cannot allocate device memory (GPU).
 
-Some callers -- a plugin that an engine hands only a stream and its tensors,
-or code running while a global-mode stream capture forbids cudaMalloc --
+Some callers -- a plugin that an engine hands only a stream and its tensors --
 cannot provide a workspace.  tbe_backward_static_workspace() serves them from
 an array compiled into the library.  This file checks, through the C ABI,
 that two calls in a row give the same rows, run boundaries, sorted positions
