@@ -424,7 +424,8 @@ struct FwdArgs {
   int32_t lpr_max;  // lanes per row cap of the gather (a power of two <= 32)
   int32_t balance;  // tables differ in shape: size each table's tasks by its own mean bag length
   int32_t mean;     // mean pooling: each bag's sum divided by its number of lookups
-  int32_t split;    // stream kernel: bags per block of a split launch (0: tasks per warp)
+  int32_t split;    // stream kernel: 1 when the layout allows split tasks (set where the kernel is
+                    // chosen); the launch replaces it by the bags per block (0: tasks per warp)
 };
 
 // Mean pooling: the bag's fp32 sum divided by its number of lookups, one IEEE
