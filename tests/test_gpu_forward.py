@@ -153,6 +153,27 @@ def test_split_tasks(tbe, dt, D, weighted, pooling):
         tbe.set_tuning(**old)
 
 
+def test_split_tasks_idle_blocks_and_short_last_run(tbe):
+    """A batch whose runs do not fill the grid (blocks without a run) and
+    whose tables end in a run shorter than the others."""
+    rng = np.random.default_rng(41)
+    T, B, rows, D = 5, 97, 500, 64
+    lens = rng.poisson(40, size=(T, B))
+    lens[3, -2:] = [700, 0]
+    ids = [rng.integers(0, rows, size=int(lens[t].sum())) for t in range(T)]
+    p = make_problem(T, B, rows=[rows] * T, D=[D] * T, weights_dtype=[DT_F16] * T, out_dtype=DT_F16, lengths=lens,
+                     ids=ids, seed=9)
+    grid = -(-T * B // 4)
+    nbb = split_bags(T, B, p.N, grid)
+    assert nbb > 0 and T * -(-B // nbb) < grid and B % nbb != 0
+    old = tbe.get_tuning()
+    tbe.set_tuning(fwd_ring=2)
+    try:
+        check_full(tbe, p, path=tbe.TBE_PATH_GATHER)
+    finally:
+        tbe.set_tuning(**old)
+
+
 def test_split_tasks_bad_id_in_a_cut_bag(tbe):
     """A bad id inside the bag that spans the parts is reported and adds
     nothing; every other output still matches."""
